@@ -1,0 +1,513 @@
+#!/usr/bin/env python
+"""Paged-KV GQA decode step on GB300: KV GB/s, % of HBM peak and steps/s.
+
+Default workload: the 70B-shape continuous batch (B = 256 sequences, 64 query
+heads on 8 KV heads, head_dim 128, bf16, block_size 16, context lengths
+log-uniform in [128, 8192], each step every sequence finishes with p = 0.02
+and a newcomer with a prompt log-uniform in [128, 2048] joins in its slot).
+The 32-iteration schedule is drawn once and replayed cyclically (replays
+re-write the same slots, so every step has the shape of its iteration).
+
+A step is one pass of the hot path over the batch: pa_kv_append of one new
+token per sequence, pa_decode over every sequence's paged context and, when
+the context is split, pa_decode_splitk_reduce. Joiners' prompt rows are
+written with pa_kv_append before their step, outside the step's timing (a
+prefill stand-in). Inputs are resident in HBM; each step streams ~2 GB of KV,
+far more than the 129 MB L2, so no L2 flush is needed between steps.
+
+  value   = algorithmic bytes (each attended token's K and V rows once, plus
+            q in and out) / device time of the step (append + decode + reduce)
+  e2e     = the same with the step's inputs copied from pinned host memory and
+            the output copied back inside the timed region
+  roofline: the decode kernel alone, timed with CUDA events on its stream.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (the
+reference arm): each step is the oracle's append + decode of one sequence of
+a sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged-decode KV GB/s (% of GB300 HBM peak) and decode steps/s, 70B-shape batch"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["cb70b", "8b", "long", "prefix"], default="cb70b")
+    ap.add_argument("--split", type=int, default=-1, help="split_tokens (-1: planned)")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=256)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="budget of the oracle's CPU baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# workloads as step lists (host side)
+# ---------------------------------------------------------------------------
+
+def describe(workload: str) -> str:
+    return {
+        "cb70b": "70B-shape continuous batching: B=256, 64 q heads / 8 KV heads, head_dim 128, "
+                 "bf16, block_size 16, ctx log-uniform [128, 8192], p_finish 0.02, joiner "
+                 "prompts log-uniform [128, 2048], 32-iteration schedule replayed",
+        "8b": "8B-shape decode layer: B=64, 32 q heads / 8 KV heads, head_dim 128, bf16, "
+              "block_size 16, ctx uniform [512, 4096] + 1 appended",
+        "long": "long-context split-K: B=4 x 131072 tokens, 32 q heads / 8 KV heads, head_dim "
+                "128, bf16, block_size 16, 1% of K rows x8, no append",
+        "prefix": "radix prefix sharing: B=128, 2048-token prefix in the same 128 blocks, "
+                  "private suffix uniform [64, 1024] + 1 appended, 8B heads",
+    }[workload]
+
+
+class Steps:
+    """Device-resident inputs of a workload's steps, cycled by index."""
+
+    def __init__(self, workload: str, seed: int, device):
+        import torch
+        from paged_kv_cache_45_gb300 import workloads as wl
+        self.workload = workload
+        self.items = []
+        if workload == "cb70b":
+            cb = wl.ContinuousBatching(seed=seed)
+            self.k_cache, self.v_cache = cb.initial_caches(device)
+            self.scale, self.hkv, self.hq, self.d = cb.scale, cb.Hkv, cb.Hq, cb.D
+            self.max_context = cb.max_blocks * cb.bs
+            for it in range(cb.iterations):
+                st = cb.step(it)
+                self.items.append(dict(
+                    fill=(st.fill_k.to(device), st.fill_v.to(device), st.fill_slots.to(device))
+                    if st.fill_slots.numel() else None,
+                    q=st.q, k_new=st.k_new, v_new=st.v_new, slots=st.slot_mapping,
+                    tables=st.block_tables, lens=st.context_lens))
+        else:
+            case = {"8b": lambda: wl.llama8b_case(seed),
+                    "long": lambda: wl.long_context_case(seed),
+                    "prefix": lambda: wl.prefix_sharing_case(seed)}[workload]()
+            self.k_cache, self.v_cache = case.k_cache.to(device), case.v_cache.to(device)
+            self.scale, self.hkv, self.hq, self.d = (case.scale, case.num_kv_heads,
+                                                     case.num_q_heads, case.head_dim)
+            self.max_context = case.max_blocks * case.block_size
+            self.items.append(dict(fill=None, q=case.q, k_new=case.k_new, v_new=case.v_new,
+                                   slots=case.slot_mapping, tables=case.block_tables,
+                                   lens=case.context_lens))
+        for it in self.items:   # host copies (pinned) for e2e, device copies for the step
+            it["host"] = {k: it[k].pin_memory() for k in ("q", "k_new", "v_new", "slots", "tables",
+                                                           "lens") if it[k] is not None}
+            it["dev"] = {k: v.to(device) for k, v in it["host"].items()}
+            it["kv_bytes"] = int(it["lens"].to(torch.int64).sum()) * 2 * self.hkv * self.d * 2
+            it["qo_bytes"] = 2 * it["q"].numel() * 2
+        self.batch = int(self.items[0]["q"].shape[0])
+
+    def __len__(self):
+        return len(self.items)
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled while the timed region runs
+# ---------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                "clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index: int, period_ms: int = 20):
+        self.proc = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                    f"-lms={period_ms}", *sel]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        rows = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                rows.append((float(f[0]), float(f[1]), float(f[2]), f[3:7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        loaded = [r for r in rows if r[2] > 0.3 * max(x[2] for x in rows)] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("pa_decode.cu", "pa_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_45_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(kv_tokens_per_launch: float):
+    """dram read+write bytes of one decode launch, scaled from the committed
+    ncu capture if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+    except Exception:
+        return None
+    if rec.get("source_sha") != decode_source_hash():
+        return None
+    return rec["dram_bytes_per_kv_token"] * kv_tokens_per_launch
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    from paged_kv_cache_45_gb300 import binding as b
+
+    # the oracle's CPU baseline runs first, in a fresh process with one BLAS thread
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_subprocess(args)
+
+    steps = Steps(args.workload, args.seed + rank, device)
+    sms = b.num_sms(local)
+    if args.split >= 0:
+        split = args.split
+    else:
+        split = max(b.plan_split(it["lens"].numpy(), steps.hkv, sms) for it in steps.items)
+    if args.workload == "long" and args.split < 0:
+        split = 4096
+    ws = b.DecodeWorkspace(steps.batch, steps.hq, steps.d, split, steps.max_context, device)
+    stream = torch.cuda.current_stream(device)
+
+    def fill(it):
+        if it["fill"] is not None:
+            fk, fv, fs = it["fill"]
+            b.pa_kv_append(fk, fv, fs, steps.k_cache, steps.v_cache)
+
+    def step(dv, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        if dv.get("k_new") is not None:
+            b.pa_kv_append(dv["k_new"], dv["v_new"], dv["slots"], steps.k_cache, steps.v_cache)
+        if ev is not None:
+            ev[1].record(stream)
+        b.pa_decode(dv["q"], steps.k_cache, steps.v_cache, dv["tables"], dv["lens"], steps.scale,
+                    ws.out, ws.split_tokens, ws.max_splits, ws.part_out, ws.part_lse)
+        if ev is not None:
+            ev[2].record(stream)
+        if ws.split_tokens:
+            b.pa_decode_splitk_reduce(ws.part_out, ws.part_lse, dv["lens"], ws.split_tokens, ws.out)
+        if ev is not None:
+            ev[3].record(stream)
+
+    n = len(steps)
+    for w in range(args.warmup):
+        it = steps.items[w % n]
+        fill(it)
+        step(it["dev"])
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    launches = 0
+    sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
+    if sampler:
+        sampler.__enter__()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for k in range(K):
+        it = steps.items[(args.warmup + k) % n]
+        if it["fill"] is not None:
+            fill(it)
+            launches += 1
+        step(it["dev"], evs[k])
+        launches += (1 if it["dev"].get("k_new") is not None else 0) + 1 + (1 if ws.split_tokens else 0)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    if sampler:
+        sampler.__exit__(None, None, None)
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    app_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    red_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    idx = [(args.warmup + k) % n for k in range(K)]
+    alg_bytes = sum(steps.items[i]["kv_bytes"] + steps.items[i]["qo_bytes"] for i in idx)
+    kv_tokens = sum(int(steps.items[i]["lens"].sum()) for i in idx)
+    total_s = sum(step_ms) / 1e3
+    dec_s = sum(dec_ms) / 1e3
+
+    # ------------------------------------------------------------ end to end
+    E = min(args.e2e_steps, K)
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(E)]
+    out_host = torch.empty(ws.out.shape, dtype=ws.out.dtype, pin_memory=True)
+    bi = bo = 0
+    e2e_bytes = 0
+    torch.cuda.synchronize()
+    for k in range(E):
+        it = steps.items[k % n]
+        fill(it)
+        e2e_ev[k][0].record(stream)
+        dv = {key: t.to(device, non_blocking=True) for key, t in it["host"].items()}
+        step(dv)
+        out_host.copy_(ws.out, non_blocking=True)
+        e2e_ev[k][1].record(stream)
+        if k == 0:
+            bi = sum(t.numel() * t.element_size() for t in it["host"].values())
+            bo = out_host.numel() * out_host.element_size()
+        e2e_bytes += it["kv_bytes"] + it["qo_bytes"]
+    torch.cuda.synchronize()
+    e2e_s = sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / 1e3
+
+    # ------------------------------------------------------------ across ranks
+    stats = torch.tensor([total_s, alg_bytes, e2e_s, e2e_bytes, dec_s, t_wall], dtype=torch.float64,
+                         device=device)
+    if world > 1:
+        mx = stats.clone()
+        sm = stats.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+        total_s, e2e_s = float(mx[0]), float(mx[2])
+        alg_bytes, e2e_bytes = float(sm[1]), float(sm[3])
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_hbm_peak()
+    gbs = alg_bytes / total_s / 1e9
+    dec_gbs_rank0 = float(stats[1]) / dec_s / 1e9 if world > 1 else alg_bytes / dec_s / 1e9
+    kv_tokens_per_launch = kv_tokens / K
+    traffic = traffic_per_launch(kv_tokens_per_launch)
+    clocks = sampler.summary() if sampler else None
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_s / K * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/K/V; seeded lengths and block placement)",
+        "config": {"workload": describe(args.workload), "split_tokens": ws.split_tokens,
+                   "max_splits": ws.max_splits, "batch": steps.batch,
+                   "l2": "no flush: each step reads ~2 GB of KV, inputs far larger than the 129 MB L2"
+                   if args.workload == "cb70b" else "inputs larger than L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_of_hbm_peak": round(100 * gbs / peak, 2),
+        "steps_per_s": round(K / total_s, 1),
+        "kv_bytes_per_step": int(alg_bytes / K / world),
+        "ms_breakdown": {"append": round(statistics.mean(app_ms), 5),
+                         "decode": round(statistics.mean(dec_ms), 5),
+                         "reduce": round(statistics.mean(red_ms), 5)},
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel",
+                     "achieved": round(dec_gbs_rank0, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(dec_gbs_rank0 / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                     "traffic": None if traffic is None else int(traffic),
+                     "algorithmic_bytes_per_launch": int(float(stats[1]) / K)},
+        "e2e": {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo), "steps": E},
+        "gpu_launches": launches,
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if clocks is not None:
+        line["clocks"] = clocks
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores: CPU baseline and the reference arm
+# ---------------------------------------------------------------------------
+
+def oracle_sample_case(seed: int, n_seqs: int = 48):
+    """A bounded sample of the 70B-shape batch: n_seqs sequences with lengths
+    drawn from the same log-uniform [128, 8192] law, one appended token."""
+    import numpy as np
+    from paged_kv_cache_45_gb300 import workloads as wl
+    rng = np.random.Generator(np.random.PCG64(seed + 3_000))
+    lens = wl.loguniform(rng, 128, 8192, n_seqs)
+    return wl.make_case("cb70b_sample", seed, lens, 64, 8, 128, 16)
+
+
+def oracle_steps(case, budget_s: float, max_steps: int | None = None):
+    """Time the oracle's append + decode of one sequence per step."""
+    from oracle import paged_attention as pa
+    from paged_kv_cache_45_gb300 import workloads as wl
+    q, kc, vc = wl.bits(case.q), wl.bits(case.k_cache), wl.bits(case.v_cache)
+    kn, vn = wl.bits(case.k_new), wl.bits(case.v_new)
+    bt, cl, slots = case.block_tables.numpy(), case.context_lens.numpy(), case.slot_mapping.numpy()
+    per_tok = 2 * case.num_kv_heads * case.head_dim * 2
+    times, nbytes = [], []
+    t_start = time.perf_counter()
+    i = 0
+    while True:
+        b = i % case.batch
+        t0 = time.perf_counter()
+        pa.kv_append_inplace(kc, vc, kn[b:b + 1], vn[b:b + 1], slots[b:b + 1])
+        pa.decode(q, kc, vc, bt, cl, case.scale, seqs=[b])
+        times.append(time.perf_counter() - t0)
+        nbytes.append(int(cl[b]) * per_tok + 2 * case.num_q_heads * case.head_dim * 2)
+        i += 1
+        if max_steps is not None and i >= max_steps:
+            break
+        if max_steps is None and time.perf_counter() - t_start > budget_s:
+            break
+    return times, nbytes
+
+
+def cpu_baseline_child(seed: int, budget_s: float) -> None:
+    case = oracle_sample_case(seed)
+    times, nbytes = oracle_steps(case, budget_s)
+    print(json.dumps({"value": round(sum(nbytes) / sum(times) / 1e9, 4), "unit": "GB/s",
+                      "cores": 1, "kind": "oracle",
+                      "sample": f"{len(times)} sequences of a 48-sequence sample of the 70B-shape "
+                                f"batch (log-uniform [128, 8192] tokens), fp64 oracle append + "
+                                f"decode, one BLAS thread, {sum(times):.1f} s",
+                      "seconds": round(sum(times), 2), "host_cpus": os.cpu_count()}))
+
+
+def single_thread_env():
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+              "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    return env
+
+
+def cpu_baseline_subprocess(args):
+    code = ("import bench; bench.cpu_baseline_child(%d, %f)" % (args.seed, args.cpu_seconds))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=single_thread_env(),
+                           capture_output=True, text=True, timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal: the GPU number stands on its own
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"failed: {type(e).__name__}: {e}"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    if os.environ.get("OPENBLAS_NUM_THREADS") != "1":   # one BLAS thread, set before numpy loads
+        os.execve(sys.executable, [sys.executable] + sys.argv, single_thread_env())
+    case = oracle_sample_case(args.seed)
+    oracle_steps(case, 0, max_steps=max(args.warmup, 0) or 1)
+    times, nbytes = oracle_steps(case, 0, max_steps=args.steps)
+    total = sum(times)
+    value = sum(nbytes) / total / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe("cb70b") + " (oracle: one sequence per step, cycling a "
+                                                   "48-sequence sample)", "batch": case.batch},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} steps of one sequence each from a 48-sequence "
+                                   f"sample of the 70B-shape batch"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

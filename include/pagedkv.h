@@ -1,0 +1,168 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) paged-KV decode-attention library.
+ *
+ * The operation: one decode step of attention for a continuously batched set
+ * of variable-length sequences whose K/V rows live in a shared pool of
+ * fixed-size physical blocks, reached through per-sequence block tables, with
+ * grouped-query heads (several query heads share one KV head).
+ *
+ * Sources, by page and section:
+ *   [TGI-PA]  "Text Generation Inference: Hugging Face's production-grade LLM
+ *             inference server", section "Under the Hood: PagedAttention"
+ *             (block table, shared pool, append into the current block, the
+ *             simplified paged forward pass).
+ *   [TGI-FA]  same page, section "Under the Hood: Flash Attention" (running
+ *             max / running sum / rescaled accumulator over K/V tiles).
+ *   [TGI-KV]  same page, section "Production Pattern: KV Cache Math".
+ *   [SPEED]   "How to Speed Up LLM Inference: KV Cache to Production Serving",
+ *             sections "The physics: why generating tokens is slow" (decode is
+ *             bandwidth-bound) and "The KV cache: the memory problem that runs
+ *             the show" (paging, GQA).
+ *   [LIFE]    "The inference request lifecycle", section "KV cache grows with
+ *             the sum of cached tokens" (GQA: fewer KV heads, same query heads).
+ *
+ * Conventions for every entry point:
+ *   - bf16 means IEEE bfloat16 (2 bytes). All tensors are dense, row-major,
+ *     in the shapes given, and DEVICE memory owned by the caller, except where
+ *     a parameter says "host".
+ *   - The library allocates no memory, keeps no state between calls (apart
+ *     from one 4-byte device error word per device, see pa_last_device_error)
+ *     and launches only on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). Calls return as soon as the kernels are queued; they do not
+ *     synchronise, except in validating mode (environment PA_VALIDATE=1),
+ *     where the small index tables are copied to the host and range-checked
+ *     before launching.
+ *   - Errors are returned, never raised on the device: bad arguments give
+ *     PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED without launching anything, a
+ *     failed launch gives PA_ERR_CUDA. Device code contains no traps or
+ *     asserts; out-of-range block ids or slots read zeros / are skipped.
+ *   - Layouts:
+ *       k_cache, v_cache : bf16 [num_blocks, block_size, num_kv_heads, head_dim]
+ *                          ([TGI-PA] stores K and V interleaved per token; here
+ *                          they are two pools with the same per-token layout)
+ *       block_tables     : int32 [num_seqs, max_blocks_per_seq]; entry [b][i] is
+ *                          the physical block holding logical tokens
+ *                          i*block_size .. i*block_size+block_size-1 of sequence b
+ *       context_lens     : int32 [num_seqs]; tokens attended over (after append)
+ *       q, out           : bf16 [num_seqs, num_q_heads, head_dim]
+ *     Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   - Supported: head_dim 64 or 128; num_q_heads / num_kv_heads in 1..8;
+ *     block_size a power of two in 1..256; num_blocks*block_size < 2^31.
+ *     q, out and both caches 16-byte aligned.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = -1, /* null pointer, bad size, misalignment, table out of range */
+  PA_ERR_UNSUPPORTED = -2, /* valid but not built: head_dim, group size, block size  */
+  PA_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed                    */
+  PA_ERR_WORKSPACE = -4,   /* split mode without partial buffers                      */
+  PA_ERR_DEVICE = -5       /* a kernel's bounded wait ran out (see pa_last_device_error) */
+} pa_status;
+
+/*
+ * pa_kv_append -- scatter the new tokens' K and V rows into their slots.
+ * [TGI-PA]: a new token's KV pair is appended into the sequence's current
+ * block (a fresh physical block when the current one is full; choosing it is
+ * the host allocator's job and arrives here as `slot_mapping`).
+ *
+ *   k_new, v_new  bf16 [num_tokens, num_kv_heads, head_dim]
+ *   slot_mapping  int64 [num_tokens]; token t goes to block slot/block_size,
+ *                 offset slot%block_size. slot < 0 marks a padded row: skipped.
+ *                 slot >= num_blocks*block_size is skipped too (and reported as
+ *                 PA_ERR_INVALID_ARG in validating mode).
+ *   k_cache, v_cache  written in place; bytes are copied unchanged.
+ * Rows of two tokens mapped to the same slot race; the caller must not do so.
+ */
+pa_status pa_kv_append(const void* k_new, const void* v_new,
+                       const int64_t* slot_mapping, int32_t num_tokens,
+                       void* k_cache, void* v_cache,
+                       int32_t num_blocks, int32_t block_size,
+                       int32_t num_kv_heads, int32_t head_dim, void* stream);
+
+/*
+ * pa_decode -- paged decode attention, out = softmax(scale * q K^T) V per query
+ * head over the first context_lens[b] logical tokens of sequence b, K/V rows
+ * gathered through block_tables[b] ([TGI-PA]), computed with the streaming
+ * softmax of [TGI-FA] in fp32 and rounded to bf16 (round to nearest even).
+ * One thread block serves one (sequence, KV head, context split) and every
+ * query head of that KV head's group ([SPEED], [LIFE]).
+ *
+ *   scale         the logit scale (1/sqrt(head_dim) in the pages).
+ *   split_tokens  0: one split per sequence, `out` written directly.
+ *                 > 0 (a multiple of 16): split s covers logical tokens
+ *                 [s*split_tokens, min((s+1)*split_tokens, ctx)); each split
+ *                 writes a partial to part_out/part_lse and `out` is NOT
+ *                 written -- call pa_decode_splitk_reduce next.
+ *   max_splits    splits per sequence in the partial buffers; must cover the
+ *                 longest context (ctx <= max_splits*split_tokens). Ignored
+ *                 when split_tokens == 0.
+ *   part_out      fp32 [num_seqs, num_q_heads, max_splits, head_dim]: the split's
+ *                 attention output over its own tokens, normalised.
+ *   part_lse      fp32 [num_seqs, num_q_heads, max_splits]: natural-log
+ *                 log-sum-exp of the split's scaled logits. Splits past the end
+ *                 of a sequence are not written.
+ *   context_lens[b] == 0 gives a zero output row (never NaN).
+ *   Contexts longer than max_blocks_per_seq*block_size are clamped to it.
+ */
+pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* context_lens, int32_t num_seqs,
+                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t block_size, int32_t num_blocks, float scale,
+                    int32_t split_tokens, int32_t max_splits,
+                    float* part_out, float* part_lse,
+                    void* out, void* stream);
+
+/*
+ * pa_decode_splitk_reduce -- merge split partials by log-sum-exp: per
+ * (sequence, query head) over the splits s < ceil(ctx/split_tokens):
+ * M = max lse_s, w_s = exp(lse_s - M), out = sum w_s O_s / sum w_s, rounded to
+ * bf16. This rescaling is the same algebra as the running-max correction of
+ * [TGI-FA]; the pages do not describe context splitting itself. A sequence
+ * with no tokens gets a zero row.
+ */
+pa_status pa_decode_splitk_reduce(const float* part_out, const float* part_lse,
+                                  const int32_t* context_lens, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t head_dim,
+                                  int32_t split_tokens, int32_t max_splits,
+                                  void* out, void* stream);
+
+/* Splits needed for contexts up to max_context tokens (0 if split_tokens <= 0). */
+int32_t pa_decode_num_splits(int32_t max_context, int32_t split_tokens);
+
+/* Bytes of part_out plus part_lse for the given shape (the caller may carve
+ * both from one buffer: part_lse starts at the 256-byte-aligned end of part_out). */
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                 int32_t head_dim, int32_t max_splits);
+
+/* KV bytes one token occupies over the whole model, 2*layers*kv_heads*head_dim*
+ * bytes_per_value ([TGI-KV]; [SPEED]; [LIFE]). */
+int64_t pa_kv_bytes_per_token(int32_t num_layers, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t bytes_per_value);
+
+/* Reads and clears the calling device's error word (synchronises the device).
+ * *code (host) receives 0 if no kernel's bounded wait has run out since the
+ * last call, else a nonzero bit set. Returns PA_ERR_DEVICE when nonzero. */
+pa_status pa_last_device_error(int32_t* code);
+
+/* Human-readable name of a status. Never NULL. */
+const char* pa_status_str(pa_status status);
+
+/* Library version string, e.g. "pagedkv 0.1.0 sm_103a". Never NULL. */
+const char* pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -18,6 +18,7 @@ from .paged_attention import (  # noqa: F401
     bf16_bits_to_f64,
     kv_bytes_per_token,
     kv_append,
+    kv_append_inplace,
     gather_sequence,
     decode,
     decode_online,

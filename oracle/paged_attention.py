@@ -79,15 +79,21 @@ def kv_append(k_cache: np.ndarray, v_cache: np.ndarray, k_new: np.ndarray,
     """
     kc = np.array(k_cache, copy=True)
     vc = np.array(v_cache, copy=True)
-    nb, bs = kc.shape[0], kc.shape[1]
+    kv_append_inplace(kc, vc, k_new, v_new, slot_mapping)
+    return kc, vc
+
+
+def kv_append_inplace(k_cache: np.ndarray, v_cache: np.ndarray, k_new: np.ndarray,
+                      v_new: np.ndarray, slot_mapping) -> None:
+    """:func:`kv_append` writing into the given caches instead of copies."""
+    nb, bs = k_cache.shape[0], k_cache.shape[1]
     for t, slot in enumerate(np.asarray(slot_mapping).tolist()):
         if slot < 0:
             continue
         if slot >= nb * bs:
             raise IndexError(f"slot {slot} outside a pool of {nb * bs} slots")
-        kc[slot // bs, slot % bs] = k_new[t]
-        vc[slot // bs, slot % bs] = v_new[t]
-    return kc, vc
+        k_cache[slot // bs, slot % bs] = k_new[t]
+        v_cache[slot // bs, slot % bs] = v_new[t]
 
 
 # ---------------------------------------------------------------------------

@@ -1,0 +1,238 @@
+"""Thin ctypes binding of ``libpagedkv.so`` (declared in ``include/pagedkv.h``).
+
+The functions carry the C names and only marshal arguments: they check that
+tensors are CUDA, contiguous and of the declared dtype, pass their
+``data_ptr()`` and the current torch stream, and raise ``PagedKVError`` on a
+non-OK status. Every step of the computation runs in the library's kernels.
+PyTorch supplies device memory and streams.
+
+Importing this module loads the library and raises ``ImportError`` if it has
+not been built (``python -m paged_kv_cache_45_gb300.build``): there is no
+fallback of any kind.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is missing; build it with "
+                      "`python -m paged_kv_cache_45_gb300.build` (needs nvcc)")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+_p, _i32, _i64, _f32, _sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                             ctypes.c_size_t)
+
+_SIGS = {
+    "pa_kv_append": (_i32, [_p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32, _p]),
+    "pa_decode": (_i32, [_p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32, _f32,
+                         _i32, _i32, _p, _p, _p, _p]),
+    "pa_decode_splitk_reduce": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _p, _p]),
+    "pa_decode_num_splits": (_i32, [_i32, _i32]),
+    "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
+    "pa_kv_bytes_per_token": (_i64, [_i32, _i32, _i32, _i32]),
+    "pa_last_device_error": (_i32, [ctypes.POINTER(_i32)]),
+    "pa_status_str": (ctypes.c_char_p, [_i32]),
+    "pa_version": (ctypes.c_char_p, []),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype, _fn.argtypes = _res, _args
+
+EXPORTS = tuple(_SIGS)
+LIBRARY_PATH = _LIB_PATH
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {pa_status_str(status)} ({status})")
+        self.status = status
+
+
+def pa_status_str(status: int) -> str:
+    return _lib.pa_status_str(int(status)).decode()
+
+
+def pa_version() -> str:
+    return _lib.pa_version().decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise PagedKVError(fn, status)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _t(x: torch.Tensor, dtype, name: str) -> int:
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if x.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {x.dtype}")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return x.data_ptr()
+
+
+def _opt(x, dtype, name):
+    return None if x is None else _t(x, dtype, name)
+
+
+# ---------------------------------------------------------------------------
+# the three entry points of the hot path
+# ---------------------------------------------------------------------------
+
+def pa_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    """Scatter ``k_new``/``v_new`` [T, Hkv, D] into the caches [NB, bs, Hkv, D]
+    at ``slot_mapping`` [T] (int64; negative = skip)."""
+    nb, bs, hkv, d = k_cache.shape
+    T = k_new.shape[0]
+    if tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d):
+        raise ValueError("k_new/v_new must be [T, num_kv_heads, head_dim] matching the caches")
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or slot_mapping.numel() != T:
+        raise ValueError("cache or slot_mapping shape mismatch")
+    _check("pa_kv_append", _lib.pa_kv_append(
+        _t(k_new, torch.bfloat16, "k_new"), _t(v_new, torch.bfloat16, "v_new"),
+        _t(slot_mapping, torch.int64, "slot_mapping"), T,
+        _t(k_cache, torch.bfloat16, "k_cache"), _t(v_cache, torch.bfloat16, "v_cache"),
+        nb, bs, hkv, d, _stream(stream)))
+
+
+def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, out,
+              split_tokens: int = 0, max_splits: int = 0, part_out=None, part_lse=None,
+              stream=None) -> None:
+    """Paged decode attention into ``out`` [B, Hq, D] bf16 (or, with
+    ``split_tokens > 0``, into the fp32 partials ``part_out``/``part_lse``)."""
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shapes do not match q")
+    if tuple(out.shape) != (B, hq, d) or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("out / block_tables shape mismatch")
+    if context_lens.numel() != B:
+        raise ValueError("context_lens must have one entry per sequence")
+    _check("pa_decode", _lib.pa_decode(
+        _t(q, torch.bfloat16, "q"), _t(k_cache, torch.bfloat16, "k_cache"),
+        _t(v_cache, torch.bfloat16, "v_cache"), _t(block_tables, torch.int32, "block_tables"),
+        int(block_tables.shape[1]), _t(context_lens, torch.int32, "context_lens"), B, hq, hkv, d,
+        bs, nb, float(scale), int(split_tokens), int(max_splits),
+        _opt(part_out, torch.float32, "part_out"), _opt(part_lse, torch.float32, "part_lse"),
+        _t(out, torch.bfloat16, "out"), _stream(stream)))
+
+
+def pa_decode_splitk_reduce(part_out, part_lse, context_lens, split_tokens: int, out,
+                            stream=None) -> None:
+    """Merge ``part_out`` [B, Hq, S, D] / ``part_lse`` [B, Hq, S] into ``out``."""
+    B, hq, S, d = part_out.shape
+    if tuple(part_lse.shape) != (B, hq, S) or tuple(out.shape) != (B, hq, d):
+        raise ValueError("partial / output shape mismatch")
+    _check("pa_decode_splitk_reduce", _lib.pa_decode_splitk_reduce(
+        _t(part_out, torch.float32, "part_out"), _t(part_lse, torch.float32, "part_lse"),
+        _t(context_lens, torch.int32, "context_lens"), B, hq, d, int(split_tokens), S,
+        _t(out, torch.bfloat16, "out"), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# sizes and diagnostics
+# ---------------------------------------------------------------------------
+
+def pa_decode_num_splits(max_context: int, split_tokens: int) -> int:
+    return int(_lib.pa_decode_num_splits(int(max_context), int(split_tokens)))
+
+
+def pa_decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int,
+                              max_splits: int) -> int:
+    return int(_lib.pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_splits))
+
+
+def pa_kv_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int,
+                          bytes_per_value: int) -> int:
+    return int(_lib.pa_kv_bytes_per_token(num_layers, num_kv_heads, head_dim, bytes_per_value))
+
+
+def pa_last_device_error() -> int:
+    """Read and clear the device error word (synchronises); 0 means none."""
+    code = _i32(0)
+    st = _lib.pa_last_device_error(ctypes.byref(code))
+    if st not in (0, -5):
+        raise PagedKVError("pa_last_device_error", st)
+    return int(code.value)
+
+
+# ---------------------------------------------------------------------------
+# convenience: one decode call with library-sized buffers
+# ---------------------------------------------------------------------------
+
+class DecodeWorkspace:
+    """Output and split partial buffers for repeated decode calls of one shape."""
+
+    def __init__(self, num_seqs: int, num_q_heads: int, head_dim: int, split_tokens: int = 0,
+                 max_context: int = 0, device="cuda"):
+        self.split_tokens = int(split_tokens)
+        self.max_splits = pa_decode_num_splits(max_context, split_tokens) if split_tokens else 0
+        self.out = torch.empty((num_seqs, num_q_heads, head_dim), dtype=torch.bfloat16,
+                               device=device)
+        if self.split_tokens:
+            self.part_out = torch.empty((num_seqs, num_q_heads, self.max_splits, head_dim),
+                                        dtype=torch.float32, device=device)
+            self.part_lse = torch.empty((num_seqs, num_q_heads, self.max_splits),
+                                        dtype=torch.float32, device=device)
+        else:
+            self.part_out = self.part_lse = None
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+           ws: DecodeWorkspace | None = None, split_tokens: int = 0, max_context: int | None = None,
+           stream=None) -> torch.Tensor:
+    """``pa_decode`` (+ ``pa_decode_splitk_reduce`` when split) into a workspace;
+    returns the bf16 output [B, Hq, D]."""
+    B, hq, d = q.shape
+    if ws is None:
+        if split_tokens and max_context is None:
+            max_context = int(block_tables.shape[1]) * int(k_cache.shape[1])
+        ws = DecodeWorkspace(B, hq, d, split_tokens, max_context or 0, q.device)
+    pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, ws.out, ws.split_tokens,
+              ws.max_splits, ws.part_out, ws.part_lse, stream)
+    if ws.split_tokens:
+        pa_decode_splitk_reduce(ws.part_out, ws.part_lse, context_lens, ws.split_tokens, ws.out,
+                                stream)
+    return ws.out
+
+
+# ---------------------------------------------------------------------------
+# launch planning (host side)
+# ---------------------------------------------------------------------------
+
+def num_sms(device=None) -> int:
+    return torch.cuda.get_device_properties(device or torch.cuda.current_device()).multi_processor_count
+
+
+def plan_split(context_lens_host, num_kv_heads: int, sms: int = 152, blocks_per_sm: int = 16,
+               lo: int = 256, hi: int = 8192) -> int:
+    """Pick ``split_tokens`` for a batch whose lengths the host scheduler knows.
+
+    Aims at about ``blocks_per_sm`` thread blocks' worth of KV per SM so the
+    last wave's blocks are short next to the whole step (the tail), with
+    powers of two in [lo, hi]. Returns 0 (no split, no reduce) when no
+    sequence is longer than the chosen split.
+    """
+    import numpy as np
+    lens = np.asarray(context_lens_host, dtype=np.int64)
+    if lens.size == 0 or lens.max() <= 0:
+        return 0
+    per_block = lens.sum() * num_kv_heads / (sms * blocks_per_sm)
+    split = lo
+    while split < per_block and split < hi:
+        split *= 2
+    return 0 if lens.max() <= split else int(split)

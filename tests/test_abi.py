@@ -1,0 +1,106 @@
+"""The C-ABI library builds, loads and exports what include/pagedkv.h declares.
+
+No kernel is launched here (these run without a GPU): only host-side sizes,
+strings and argument checks that return before any CUDA call.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from paged_kv_cache_45_gb300 import build as pk_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = pk_build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path():
+    names = declared_functions()
+    for fn in ("pa_kv_append", "pa_decode", "pa_decode_splitk_reduce"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_declared_symbol():
+    from paged_kv_cache_45_gb300 import binding
+    assert sorted(binding.EXPORTS) == declared_functions()
+
+
+def test_status_strings_and_version():
+    from paged_kv_cache_45_gb300 import binding as b
+    assert b.pa_status_str(0) == "PA_OK"
+    assert b.pa_status_str(-1) == "PA_ERR_INVALID_ARG"
+    assert b.pa_status_str(-5) == "PA_ERR_DEVICE"
+    assert b.pa_status_str(99) == "PA_ERR_UNKNOWN"
+    assert "sm_103a" in b.pa_version()
+
+
+def test_sizes_match_the_oracle_formula():
+    from paged_kv_cache_45_gb300 import binding as b
+    for args in [(32, 8, 128, 2), (80, 8, 128, 2), (80, 8, 128, 1), (1, 8, 128, 2)]:
+        assert b.pa_kv_bytes_per_token(*args) == oracle.kv_bytes_per_token(*args)
+    assert b.pa_decode_num_splits(131072, 4096) == 32
+    assert b.pa_decode_num_splits(131073, 4096) == 33
+    assert b.pa_decode_num_splits(0, 4096) == 0
+    assert b.pa_decode_num_splits(100, 0) == 0
+    rows = 4 * 32 * 32
+    assert b.pa_decode_workspace_bytes(4, 32, 128, 32) == rows * 128 * 4 + rows * 4
+
+
+def test_bad_arguments_are_rejected_before_any_launch(lib):
+    lib.pa_decode.restype = ctypes.c_int32
+    lib.pa_kv_append.restype = ctypes.c_int32
+    lib.pa_decode_splitk_reduce.restype = ctypes.c_int32
+    P = ctypes.c_void_p
+    fake = P(4096)           # never dereferenced: checks fail first
+    odd = P(4098)            # not 16-byte aligned
+
+    def decode(q=fake, k=fake, v=fake, bt=fake, mb=4, cl=fake, B=2, hq=8, hkv=2, d=128, bs=16,
+               nb=16, scale=0.1, split=0, ms=0, po=None, pl=None, out=fake):
+        return lib.pa_decode(q, k, v, bt, ctypes.c_int32(mb), cl, ctypes.c_int32(B),
+                             ctypes.c_int32(hq), ctypes.c_int32(hkv), ctypes.c_int32(d),
+                             ctypes.c_int32(bs), ctypes.c_int32(nb), ctypes.c_float(scale),
+                             ctypes.c_int32(split), ctypes.c_int32(ms), po, pl, out, None)
+
+    assert decode(q=None) == -1
+    assert decode(hq=7, hkv=2) == -1           # heads do not group
+    assert decode(hq=32, hkv=2) == -2          # group of 16: not built
+    assert decode(d=96) == -2                  # head_dim
+    assert decode(bs=12) == -2                 # block size not a power of two
+    assert decode(q=odd) == -1                 # alignment
+    assert decode(split=24, ms=4, po=fake, pl=fake) == -1   # split not a multiple of 16
+    assert decode(split=32, ms=4) == -4        # split without partial buffers
+    assert decode(split=32, ms=0, po=fake, pl=fake) == -1
+    assert decode(nb=1 << 27, bs=32) == -1     # pool rows overflow int32
+    assert decode(scale=float("nan")) == -1
+    assert decode(B=0) == 0                    # nothing to do
+
+    T = ctypes.c_int32
+    assert lib.pa_kv_append(fake, fake, fake, T(4), None, fake, T(8), T(16), T(2), T(64), None) == -1
+    assert lib.pa_kv_append(fake, fake, fake, T(4), fake, fake, T(8), T(16), T(2), T(60), None) == -2
+    assert lib.pa_kv_append(odd, fake, fake, T(4), fake, fake, T(8), T(16), T(2), T(64), None) == -1
+    assert lib.pa_kv_append(fake, fake, fake, T(0), fake, fake, T(8), T(16), T(2), T(64), None) == 0
+
+    assert lib.pa_decode_splitk_reduce(fake, fake, fake, T(2), T(8), T(128), T(0), T(4), fake,
+                                       None) == -1
+    assert lib.pa_decode_splitk_reduce(fake, fake, fake, T(2), T(8), T(80), T(16), T(4), fake,
+                                       None) == -2

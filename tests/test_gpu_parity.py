@@ -1,0 +1,271 @@
+"""GPU parity: the sm_103a kernels, called through the C ABI, against the fp64
+oracle on the same seeded inputs.
+
+* pa_kv_append and all block indexing: bit-exact.
+* pa_decode (+ pa_decode_splitk_reduce): max abs error <= 2e-2 and per-row
+  relative L2 <= 5e-3 against the oracle (tests/parity.py).
+Sizes span several 16-token tiles, every block size, ragged tails, empty
+contexts and empty splits.
+"""
+
+import math
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import paged_attention as pa
+from paged_kv_cache_45_gb300 import workloads as wl
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+def run_step(b, case, split=0, max_context=None):
+    """Append (if any) then decode on the GPU; returns (out, k_cache, v_cache)."""
+    d = P.dev(case)
+    if case.k_new is not None:
+        b.pa_kv_append(d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"], d["v_cache"])
+    out = b.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                   case.scale, split_tokens=split, max_context=max_context)
+    torch.cuda.synchronize()
+    return out, d["k_cache"], d["v_cache"]
+
+
+# ---------------------------------------------------------------------------
+# append: bit-exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("maker", [lambda: wl.tiny_case(0),
+                                   lambda: wl.make_case("s", 1, [0, 1, 15, 16, 31, 32, 33, 200],
+                                                        8, 2, 64, 8),
+                                   lambda: wl.llama8b_case(0, batch=64)],
+                         ids=["tiny", "ragged_bs8", "8b_full"])
+def test_append_bit_exact(cuda_lib, maker):
+    case = maker()
+    d = P.dev(case)
+    cuda_lib.pa_kv_append(d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"], d["v_cache"])
+    torch.cuda.synchronize()
+    kc, vc = P.oracle_caches(case)
+    assert np.array_equal(wl.bits(d["k_cache"].cpu()), kc)
+    assert np.array_equal(wl.bits(d["v_cache"].cpu()), vc)
+
+
+def test_append_skips_negative_and_out_of_pool_slots(cuda_lib):
+    case = wl.make_case("s", 2, [3, 4, 5, 6], 2, 1, 64, 16)
+    d = P.dev(case)
+    before_k = d["k_cache"].clone()
+    nslots = case.num_blocks * case.block_size
+    slots = torch.tensor([-1, nslots, nslots + 100, -7], dtype=torch.int64, device="cuda")
+    cuda_lib.pa_kv_append(d["k_new"], d["v_new"], slots, d["k_cache"], d["v_cache"])
+    torch.cuda.synchronize()
+    assert torch.equal(before_k.view(torch.int16), d["k_cache"].view(torch.int16))
+
+
+def test_append_many_rows_prefill_style(cuda_lib):
+    # a joiner's whole prompt written through the same entry point
+    case = wl.make_case("p", 3, [0, 0], 8, 8, 128, 16, append=False, num_blocks=40)
+    g = torch.Generator().manual_seed(5)
+    T = 300
+    rows = torch.randn((T, 8, 128), generator=g).to(torch.bfloat16)
+    rows_v = torch.randn((T, 8, 128), generator=g).to(torch.bfloat16)
+    slots = torch.from_numpy(np.random.default_rng(1).permutation(40 * 16)[:T].astype(np.int64))
+    d = P.dev(case)
+    cuda_lib.pa_kv_append(rows.cuda(), rows_v.cuda(), slots.cuda(), d["k_cache"], d["v_cache"])
+    torch.cuda.synchronize()
+    kc, vc = pa.kv_append(wl.bits(case.k_cache), wl.bits(case.v_cache), wl.bits(rows),
+                          wl.bits(rows_v), slots.numpy())
+    assert np.array_equal(wl.bits(d["k_cache"].cpu()), kc)
+    assert np.array_equal(wl.bits(d["v_cache"].cpu()), vc)
+
+
+# ---------------------------------------------------------------------------
+# decode: against the oracle
+# ---------------------------------------------------------------------------
+
+def test_tiny_case(cuda_lib):
+    case = wl.tiny_case(0)
+    out, _, _ = run_step(cuda_lib, case)
+    P.assert_close(P.to_f64(out), P.oracle_out(case), "tiny")
+    out16, _, _ = run_step(cuda_lib, case, split=16)
+    P.assert_close(P.to_f64(out16), P.oracle_out(case), "tiny split16")
+
+
+LENS = [0, 1, 2, 15, 16, 17, 31, 33, 64, 100, 257, 1000]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (8, 1), (6, 2), (16, 2)])
+def test_group_and_head_dim_sweep(cuda_lib, d, hq, hkv):
+    case = wl.make_case("sweep", 100 + d + hq * 3 + hkv, LENS, hq, hkv, d, 16)
+    out, _, _ = run_step(cuda_lib, case)
+    P.assert_close(P.to_f64(out), P.oracle_out(case), f"G={hq // hkv} D={d}")
+
+
+@pytest.mark.parametrize("bs", [1, 2, 4, 8, 16, 32, 64, 256])
+def test_every_block_size(cuda_lib, bs):
+    case = wl.make_case("bs", 200 + bs, LENS, 8, 2, 128, bs)
+    out, _, _ = run_step(cuda_lib, case)
+    P.assert_close(P.to_f64(out), P.oracle_out(case), f"bs={bs}")
+
+
+@pytest.mark.parametrize("split", [16, 32, 256, 4096])
+def test_context_splits_and_reduce(cuda_lib, split):
+    case = wl.make_case("split", 300, LENS + [2049, 4000], 8, 2, 128, 16)
+    out, _, _ = run_step(cuda_lib, case, split=split)
+    P.assert_close(P.to_f64(out), P.oracle_out(case), f"split={split}")
+
+
+def test_split_partials_match_oracle_partials(cuda_lib):
+    case = wl.make_case("part", 301, [0, 5, 40, 300], 8, 2, 64, 16, append=False)
+    split, S = 32, 12
+    d = P.dev(case)
+    po = torch.full((4, 8, S, 64), float("nan"), device="cuda")
+    pl = torch.full((4, 8, S), float("nan"), device="cuda")
+    out = torch.empty((4, 8, 64), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.pa_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                       case.scale, out, split, S, po, pl)
+    torch.cuda.synchronize()
+    ref_o, ref_l = pa.decode_split_partials(wl.bits(case.q), wl.bits(case.k_cache),
+                                            wl.bits(case.v_cache), case.block_tables.numpy(),
+                                            case.context_lens.numpy(), case.scale, split, S)
+    po, pl = po.cpu().numpy(), pl.cpu().numpy()
+    for b, ctx in enumerate(case.context_lens.tolist()):
+        n = -(-ctx // split)
+        if n:
+            np.testing.assert_allclose(pl[b, :, :n], ref_l[b, :, :n], rtol=0, atol=2e-3)
+            np.testing.assert_allclose(po[b, :, :n], ref_o[b, :, :n], rtol=0, atol=1e-2)
+        assert np.isnan(pl[b, :, n:]).all()      # splits past the context are not written
+
+
+def test_context_of_one_returns_v_exactly(cuda_lib):
+    case = wl.make_case("one", 400, [0, 0, 0], 8, 1, 128, 16)   # append 1 -> ctx 1
+    out, _, _ = run_step(cuda_lib, case)
+    v = case.v_new.float()                                          # [B, 1, D]
+    assert torch.equal(out.float().cpu(), v.expand(-1, 8, -1))
+
+
+def test_identical_keys_give_mean_of_v(cuda_lib):
+    case = wl.make_case("same", 401, [300, 47], 4, 1, 128, 16, append=False)
+    kf = case.k_cache.view(-1, 1, 128)
+    for b, blocks in enumerate(case.seq_blocks):
+        rows = torch.from_numpy(wl.token_rows(blocks, int(case.context_lens[b]), 16))
+        kf[rows] = kf[rows[0]].clone()
+    out, _, _ = run_step(cuda_lib, case)
+    ref = P.oracle_out(case)
+    for b, blocks in enumerate(case.seq_blocks):
+        V = pa.bf16_bits_to_f64(pa.gather_sequence(wl.bits(case.v_cache), case.block_tables[b].numpy(),
+                                                   int(case.context_lens[b])))
+        np.testing.assert_allclose(ref[b, 0], V[:, 0].mean(0), atol=1e-12)
+    P.assert_close(P.to_f64(out), ref, "identical keys")
+
+
+def test_empty_contexts_give_zero_rows(cuda_lib):
+    case = wl.make_case("empty", 402, [0, 0, 50], 8, 2, 128, 16, append=False)
+    for split in (0, 32):
+        out, _, _ = run_step(cuda_lib, case, split=split, max_context=64)
+        o = out.float().cpu()
+        assert torch.all(o[:2] == 0) and torch.isfinite(o).all()
+        P.assert_close(P.to_f64(out), P.oracle_out(case), f"empty split={split}")
+
+
+# ---------------------------------------------------------------------------
+# invariances on the GPU (block ids are names only)
+# ---------------------------------------------------------------------------
+
+def test_gpu_block_permutation_is_bit_invisible(cuda_lib):
+    case = wl.make_case("perm", 500, LENS, 8, 2, 128, 16)
+    out1, _, _ = run_step(cuda_lib, case)
+    rng = np.random.default_rng(3)
+    pi = np.concatenate([[0], 1 + rng.permutation(case.num_blocks - 1)])
+    pit = torch.from_numpy(pi)
+    perm = wl.DecodeCase(**{**case.__dict__})
+    perm.k_cache = torch.empty_like(case.k_cache); perm.k_cache[pit] = case.k_cache
+    perm.v_cache = torch.empty_like(case.v_cache); perm.v_cache[pit] = case.v_cache
+    perm.block_tables = torch.from_numpy(pi[case.block_tables.numpy()].astype(np.int32))
+    s = case.slot_mapping.numpy()
+    perm.slot_mapping = torch.from_numpy(pi[s // 16] * 16 + s % 16)
+    out2, _, _ = run_step(cuda_lib, perm)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_gpu_block_size_1_vs_16_bit_identical(cuda_lib):
+    lens = [5, 16, 40, 129]
+    c16 = wl.make_case("b16", 501, lens, 8, 2, 128, 16, append=False)
+    kc, vc = wl.bits(c16.k_cache), wl.bits(c16.v_cache)
+    bt, cl = c16.block_tables.numpy(), c16.context_lens.numpy()
+    nb1 = int(cl.sum()) + 1
+    k1 = np.full((nb1, 1, 2, 128), wl.BF16_NAN_BITS, np.uint16)
+    v1 = k1.copy()
+    tab1 = np.zeros((4, int(cl.max())), np.int32)
+    nxt = 1
+    for b in range(4):
+        K = pa.gather_sequence(kc, bt[b], int(cl[b]))
+        V = pa.gather_sequence(vc, bt[b], int(cl[b]))
+        for t in range(int(cl[b])):
+            tab1[b, t] = nxt
+            k1[nxt, 0], v1[nxt, 0] = K[t], V[t]
+            nxt += 1
+    c1 = wl.DecodeCase(**{**c16.__dict__})
+    c1.block_size, c1.num_blocks = 1, nb1
+    c1.k_cache = torch.from_numpy(k1.view(np.int16)).view(torch.bfloat16)
+    c1.v_cache = torch.from_numpy(v1.view(np.int16)).view(torch.bfloat16)
+    c1.block_tables = torch.from_numpy(tab1)
+    o16, _, _ = run_step(cuda_lib, c16)
+    o1, _, _ = run_step(cuda_lib, c1)
+    assert torch.equal(o16.view(torch.int16), o1.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# the full-size 8B and prefix-sharing workloads
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_8b_workload_full(cuda_lib, seed):
+    case = wl.llama8b_case(seed)
+    split = cuda_lib.plan_split(case.context_lens.numpy(), 8, cuda_lib.num_sms())
+    out, _, _ = run_step(cuda_lib, case, split=split,
+                         max_context=int(case.context_lens.max()))
+    P.assert_close(P.to_f64(out), P.oracle_out(case), f"8b seed={seed} split={split}")
+    out0, _, _ = run_step(cuda_lib, case, split=0)
+    P.assert_close(P.to_f64(out0), P.oracle_out(case), f"8b seed={seed} unsplit")
+
+
+def test_prefix_sharing_full(cuda_lib):
+    case = wl.prefix_sharing_case(0)
+    split = cuda_lib.plan_split(case.context_lens.numpy(), 8, cuda_lib.num_sms())
+    out, _, _ = run_step(cuda_lib, case, split=split, max_context=int(case.context_lens.max()))
+    ref = P.oracle_out(case)
+    P.assert_close(P.to_f64(out), ref, f"prefix split={split}")
+
+
+def test_device_error_word_is_clear(cuda_lib):
+    run_step(cuda_lib, wl.tiny_case(0))
+    assert cuda_lib.pa_last_device_error() == 0
+
+
+def test_validating_mode_rejects_bad_tables(cuda_lib):
+    code = r"""
+import torch, sys
+sys.path.insert(0, %r)
+from paged_kv_cache_45_gb300 import binding as b, workloads as wl
+c = wl.tiny_case(0)
+q, kc, vc = c.q.cuda(), c.k_cache.cuda(), c.v_cache.cuda()
+bt, cl = c.block_tables.clone(), c.context_lens.cuda()
+out = torch.empty_like(q)
+b.pa_decode(q, kc, vc, bt.cuda(), cl, c.scale, out)
+bad = bt.clone(); bad[3, 1] = c.num_blocks
+try:
+    b.pa_decode(q, kc, vc, bad.cuda(), cl, c.scale, out)
+    print("accepted")
+except b.PagedKVError as e:
+    print("rejected", e.status)
+""" % os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PA_VALIDATE="1")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert "rejected -1" in r.stdout
