@@ -9,17 +9,20 @@ The 32-iteration schedule is drawn once and replayed cyclically (replays
 re-write the same slots, so every step has the shape of its iteration).
 
 A step is one pass of the hot path over the batch: pa_kv_append of one new
-token per sequence, pa_decode over every sequence's paged context and, when
-the context is split, pa_decode_splitk_reduce. Joiners' prompt rows are
-written with pa_kv_append before their step, outside the step's timing (a
-prefill stand-in). Inputs are resident in HBM; each step streams ~2 GB of KV,
-far more than the 129 MB L2, so no L2 flush is needed between steps.
+token per sequence, then the decode over every sequence's paged context:
+pa_decode_balanced (default, one launch) or pa_decode + pa_decode_splitk_reduce
+(--schedule split). Joiners' prompt rows (a prefill stand-in) are written with
+pa_kv_append once before the warm-up and timed apart: they set block contents,
+which the step's cost does not depend on. Inputs are resident in HBM; each
+step streams ~1.7 GB of KV, far more than the 129 MB L2, so no L2 flush is
+needed between steps.
 
   value   = algorithmic bytes (each attended token's K and V rows once, plus
             q in and out) / device time of the step (append + decode + reduce)
   e2e     = the same with the step's inputs copied from pinned host memory and
             the output copied back inside the timed region
-  roofline: the decode kernel alone, timed with CUDA events on its stream.
+  roofline: the decode kernel alone, timed with CUDA events around each of
+            its launches on its stream (a separate instrumented pass).
 
 --impl reference times the fp64 CPU oracle on the host cores instead (the
 reference arm): each step is the oracle's append + decode of one sequence of
@@ -53,8 +56,15 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["cb70b", "8b", "long", "prefix"], default="cb70b")
-    ap.add_argument("--split", type=int, default=-1, help="split_tokens (-1: planned)")
+    ap.add_argument("--schedule", choices=["balanced", "split"], default="balanced",
+                    help="balanced: pa_decode_balanced (one persistent launch); split: pa_decode "
+                         "over fixed context splits + pa_decode_splitk_reduce")
+    ap.add_argument("--split", type=int, default=-1,
+                    help="split_tokens for --schedule split (-1: planned; 0: no split)")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=256,
+                    help="sequences of the continuous batch (256 is the workload; smaller "
+                         "values are for profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=256)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle's CPU baseline sample")
@@ -67,9 +77,9 @@ def parse_args():
 # workloads as step lists (host side)
 # ---------------------------------------------------------------------------
 
-def describe(workload: str) -> str:
+def describe(workload: str, batch: int = 256) -> str:
     return {
-        "cb70b": "70B-shape continuous batching: B=256, 64 q heads / 8 KV heads, head_dim 128, "
+        "cb70b": "70B-shape continuous batching: B={batch}, 64 q heads / 8 KV heads, head_dim 128, "
                  "bf16, block_size 16, ctx log-uniform [128, 8192], p_finish 0.02, joiner "
                  "prompts log-uniform [128, 2048], 32-iteration schedule replayed",
         "8b": "8B-shape decode layer: B=64, 32 q heads / 8 KV heads, head_dim 128, bf16, "
@@ -78,19 +88,19 @@ def describe(workload: str) -> str:
                 "128, bf16, block_size 16, 1% of K rows x8, no append",
         "prefix": "radix prefix sharing: B=128, 2048-token prefix in the same 128 blocks, "
                   "private suffix uniform [64, 1024] + 1 appended, 8B heads",
-    }[workload]
+    }[workload].replace("{batch}", str(batch))
 
 
 class Steps:
     """Device-resident inputs of a workload's steps, cycled by index."""
 
-    def __init__(self, workload: str, seed: int, device):
+    def __init__(self, workload: str, seed: int, device, batch: int = 256):
         import torch
         from paged_kv_cache_45_gb300 import workloads as wl
         self.workload = workload
         self.items = []
         if workload == "cb70b":
-            cb = wl.ContinuousBatching(seed=seed)
+            cb = wl.ContinuousBatching(seed=seed, batch=batch)
             self.k_cache, self.v_cache = cb.initial_caches(device)
             self.scale, self.hkv, self.hq, self.d = cb.scale, cb.Hkv, cb.Hq, cb.D
             self.max_context = cb.max_blocks * cb.bs
@@ -198,26 +208,36 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_source_hash() -> str:
+KERNEL_SOURCES = {
+    "balanced_decode_kernel": ("pa_decode_balanced.cu", "pa_tile.cuh", "pa_device.cuh"),
+    "paged_decode_kernel": ("pa_decode.cu", "pa_tile.cuh", "pa_device.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for name in ("pa_decode.cu", "pa_device.cuh"):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "paged_kv_cache_45_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def traffic_per_launch(kv_tokens_per_launch: float):
-    """dram read+write bytes of one decode launch, scaled from the committed
-    ncu capture if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+def traffic_per_launch(kernel: str, kv_tokens_per_launch: float):
+    """DRAM read+write bytes of one decode launch, scaled by KV tokens from the
+    ncu capture recorded in profiles/dram_traffic.txt, if that capture was
+    taken on the current source of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     try:
         with open(path) as fh:
-            rec = json.load(fh)
-    except Exception:
-        return None
-    if rec.get("source_sha") != decode_source_hash():
-        return None
-    return rec["dram_bytes_per_kv_token"] * kv_tokens_per_launch
+            for line in fh:
+                f = line.split()
+                if len(f) >= 3 and not line.startswith("#") and f[0] == kernel:
+                    if f[1] != kernel_source_hash(kernel):
+                        return None
+                    return float(f[2]) * kv_tokens_per_launch
+    except OSError:
+        pass
+    return None
 
 
 def run_gpu(args):
@@ -245,15 +265,18 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline_subprocess(args)
 
-    steps = Steps(args.workload, args.seed + rank, device)
+    steps = Steps(args.workload, args.seed + rank, device, args.batch)
     sms = b.num_sms(local)
-    if args.split >= 0:
+    if args.schedule == "balanced":
+        split = b.BALANCED
+    elif args.split >= 0:
         split = args.split
+    elif args.workload == "long":
+        split = 4096
     else:
         split = max(b.plan_split(it["lens"].numpy(), steps.hkv, sms) for it in steps.items)
-    if args.workload == "long" and args.split < 0:
-        split = 4096
-    ws = b.DecodeWorkspace(steps.batch, steps.hq, steps.d, split, steps.max_context, device)
+    ws = b.DecodeWorkspace(steps.batch, steps.hq, steps.d, split, steps.max_context, device,
+                           num_kv_heads=steps.hkv)
     stream = torch.cuda.current_stream(device)
 
     def fill(it):
@@ -268,8 +291,13 @@ def run_gpu(args):
             b.pa_kv_append(dv["k_new"], dv["v_new"], dv["slots"], steps.k_cache, steps.v_cache)
         if ev is not None:
             ev[1].record(stream)
-        b.pa_decode(dv["q"], steps.k_cache, steps.v_cache, dv["tables"], dv["lens"], steps.scale,
-                    ws.out, ws.split_tokens, ws.max_splits, ws.part_out, ws.part_lse)
+        if ws.balanced:
+            b.pa_decode_balanced(dv["q"], steps.k_cache, steps.v_cache, dv["tables"], dv["lens"],
+                                 steps.scale, ws.scratch, ws.out)
+        else:
+            b.pa_decode(dv["q"], steps.k_cache, steps.v_cache, dv["tables"], dv["lens"],
+                        steps.scale, ws.out, ws.split_tokens, ws.max_splits, ws.part_out,
+                        ws.part_lse)
         if ev is not None:
             ev[2].record(stream)
         if ws.split_tokens:
@@ -278,15 +306,28 @@ def run_gpu(args):
             ev[3].record(stream)
 
     n = len(steps)
+    # Joiners' prompt rows (the prefill stand-in) are written once, before the
+    # warm-up: they only set block contents, which the decode step's cost does
+    # not depend on; their time is reported apart from the step.
+    fill_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    fill_ev[0].record(stream)
+    n_fills = 0
+    for it in steps.items:
+        if it["fill"] is not None:
+            fill(it)
+            n_fills += 1
+    fill_ev[1].record(stream)
     for w in range(args.warmup):
-        it = steps.items[w % n]
-        fill(it)
-        step(it["dev"])
+        step(steps.items[w % n]["dev"])
     torch.cuda.synchronize()
+    fill_ms = fill_ev[0].elapsed_time(fill_ev[1])
 
+    # ------------------------------------------------ the timed region: K steps
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    launches = 0
+    idx = [(args.warmup + k) % n for k in range(K)]
+    per_step_launches = (1 if steps.items[0]["dev"].get("k_new") is not None else 0) + 1 + \
+        (1 if ws.split_tokens else 0)
+    t_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
     if sampler:
         sampler.__enter__()
@@ -294,55 +335,58 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
+    t_ev[0].record(stream)
     for k in range(K):
-        it = steps.items[(args.warmup + k) % n]
-        if it["fill"] is not None:
-            fill(it)
-            launches += 1
-        step(it["dev"], evs[k])
-        launches += (1 if it["dev"].get("k_new") is not None else 0) + 1 + (1 if ws.split_tokens else 0)
+        step(steps.items[idx[k]]["dev"])
+    t_ev[1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     t_wall = time.perf_counter() - t_wall0
     if sampler:
         sampler.__exit__(None, None, None)
+    launches = K * per_step_launches
+    total_s = t_ev[0].elapsed_time(t_ev[1]) / 1e3
+    alg_bytes = sum(steps.items[i]["kv_bytes"] + steps.items[i]["qo_bytes"] for i in idx)
 
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    # ---------- an instrumented pass: events around every launch of the step
+    # (the per-kernel breakdown and the decode kernel's own duration; an event
+    # pair costs ~2 us of device time, so these steps are not the headline)
+    KI = min(K, 512)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KI)]
+    for k in range(KI):
+        step(steps.items[idx[k]]["dev"], evs[k])
+    torch.cuda.synchronize()
     dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
     app_ms = [e[0].elapsed_time(e[1]) for e in evs]
     red_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    idx = [(args.warmup + k) % n for k in range(K)]
-    alg_bytes = sum(steps.items[i]["kv_bytes"] + steps.items[i]["qo_bytes"] for i in idx)
-    kv_tokens = sum(int(steps.items[i]["lens"].sum()) for i in idx)
-    total_s = sum(step_ms) / 1e3
+    dec_bytes = sum(steps.items[idx[k]]["kv_bytes"] + steps.items[idx[k]]["qo_bytes"]
+                    for k in range(KI))
+    kv_tokens = sum(int(steps.items[idx[k]]["lens"].sum()) for k in range(KI))
     dec_s = sum(dec_ms) / 1e3
 
     # ------------------------------------------------------------ end to end
     E = min(args.e2e_steps, K)
-    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(E)]
     out_host = torch.empty(ws.out.shape, dtype=ws.out.dtype, pin_memory=True)
-    bi = bo = 0
-    e2e_bytes = 0
+    first = steps.items[0]["host"]
+    bi = sum(t.numel() * t.element_size() for t in first.values())
+    bo = out_host.numel() * out_host.element_size()
+    e2e_bytes = sum(steps.items[k % n]["kv_bytes"] + steps.items[k % n]["qo_bytes"]
+                    for k in range(E))
+    e2e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     torch.cuda.synchronize()
+    e2e_ev[0].record(stream)
     for k in range(E):
-        it = steps.items[k % n]
-        fill(it)
-        e2e_ev[k][0].record(stream)
-        dv = {key: t.to(device, non_blocking=True) for key, t in it["host"].items()}
+        dv = {key: t.to(device, non_blocking=True) for key, t in steps.items[k % n]["host"].items()}
         step(dv)
         out_host.copy_(ws.out, non_blocking=True)
-        e2e_ev[k][1].record(stream)
-        if k == 0:
-            bi = sum(t.numel() * t.element_size() for t in it["host"].values())
-            bo = out_host.numel() * out_host.element_size()
-        e2e_bytes += it["kv_bytes"] + it["qo_bytes"]
+    e2e_ev[1].record(stream)
     torch.cuda.synchronize()
-    e2e_s = sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / 1e3
+    e2e_s = e2e_ev[0].elapsed_time(e2e_ev[1]) / 1e3
 
     # ------------------------------------------------------------ across ranks
-    stats = torch.tensor([total_s, alg_bytes, e2e_s, e2e_bytes, dec_s, t_wall], dtype=torch.float64,
-                         device=device)
+    stats = torch.tensor([total_s, alg_bytes, e2e_s, e2e_bytes, dec_s, dec_bytes],
+                         dtype=torch.float64, device=device)
     if world > 1:
         mx = stats.clone()
         sm = stats.clone()
@@ -357,9 +401,10 @@ def run_gpu(args):
 
     peak, peak_kind = measured_hbm_peak()
     gbs = alg_bytes / total_s / 1e9
-    dec_gbs_rank0 = float(stats[1]) / dec_s / 1e9 if world > 1 else alg_bytes / dec_s / 1e9
-    kv_tokens_per_launch = kv_tokens / K
-    traffic = traffic_per_launch(kv_tokens_per_launch)
+    dec_gbs_rank0 = dec_bytes / dec_s / 1e9
+    kv_tokens_per_launch = kv_tokens / KI
+    kernel = "balanced_decode_kernel" if ws.balanced else "paged_decode_kernel"
+    traffic = traffic_per_launch(kernel, kv_tokens_per_launch)
     clocks = sampler.summary() if sampler else None
     line = {
         "metric": METRIC,
@@ -374,26 +419,36 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 q/K/V; seeded lengths and block placement)",
-        "config": {"workload": describe(args.workload), "split_tokens": ws.split_tokens,
-                   "max_splits": ws.max_splits, "batch": steps.batch,
+        "config": {"workload": describe(args.workload, args.batch),
+                   "schedule": "balanced (pa_decode_balanced, one launch)" if ws.balanced else
+                   f"split (pa_decode split_tokens={ws.split_tokens} + pa_decode_splitk_reduce)",
+                   "split_tokens": ws.split_tokens, "max_splits": ws.max_splits,
+                   "batch": steps.batch,
                    "l2": "no flush: each step reads ~2 GB of KV, inputs far larger than the 129 MB L2"
                    if args.workload == "cb70b" else "inputs larger than L2",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "pct_of_hbm_peak": round(100 * gbs / peak, 2),
         "steps_per_s": round(K / total_s, 1),
         "kv_bytes_per_step": int(alg_bytes / K / world),
+        "pct_of_datasheet_8tbs": round(100 * gbs / 8000.0, 2),
         "ms_breakdown": {"append": round(statistics.mean(app_ms), 5),
                          "decode": round(statistics.mean(dec_ms), 5),
-                         "reduce": round(statistics.mean(red_ms), 5)},
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel",
+                         "reduce_or_event_gap": round(statistics.mean(red_ms), 5),
+                         "steps": KI, "note": "instrumented pass, an event pair around each "
+                                             "launch"},
+        "fill_ms_before_warmup": round(fill_ms, 4), "fills": n_fills,
+        "roofline": {"bound": "hbm", "kernel": kernel,
                      "achieved": round(dec_gbs_rank0, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(dec_gbs_rank0 / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
                      "traffic": None if traffic is None else int(traffic),
-                     "algorithmic_bytes_per_launch": int(float(stats[1]) / K)},
+                     "algorithmic_bytes_per_launch": int(dec_bytes / KI),
+                     "measured": f"CUDA events around each decode launch, {KI} steps"},
         "e2e": {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo), "steps": E},
         "gpu_launches": launches,
         "wall_s_timed_region": round(t_wall, 4),
+        "timing": "CUDA events bracketing the K steps on the launching stream, "
+                  "barrier + synchronize on both sides",
     }
     if clocks is not None:
         line["clocks"] = clocks

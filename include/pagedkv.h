@@ -137,6 +137,39 @@ pa_status pa_decode_splitk_reduce(const float* part_out, const float* part_lse,
                                   int32_t split_tokens, int32_t max_splits,
                                   void* out, void* stream);
 
+/*
+ * pa_decode_balanced -- the same attention as pa_decode, in one launch,
+ * scheduled for a continuously batched mix of lengths: the 16-token tiles of
+ * all (sequence, KV head) pairs are divided into equal contiguous ranges, one
+ * per warp of a persistent grid (two thread blocks per SM, four warps each),
+ * so every warp streams the same number of KV bytes whatever the lengths. A
+ * (sequence, KV head) pair cut by a range boundary is merged by log-sum-exp
+ * (the running-max rescale of [TGI-FA]) by the last warp to finish its part;
+ * no separate reduce call is needed. Layouts, supported shapes and error
+ * behaviour are those of pa_decode; context_lens stay on the device (the
+ * schedule is computed there).
+ *
+ *   workspace        device memory of at least
+ *                    pa_decode_balanced_workspace_bytes(num_seqs, num_kv_heads,
+ *                    head_dim) bytes, 256-byte aligned, ZERO-FILLED before its
+ *                    first use; every call leaves it reusable (its counters are
+ *                    back at zero). Calls that share a workspace must not run
+ *                    concurrently.
+ *   workspace_bytes  its size; too small gives PA_ERR_WORKSPACE.
+ */
+pa_status pa_decode_balanced(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* context_lens, int32_t num_seqs,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int32_t num_blocks, float scale,
+                             void* workspace, size_t workspace_bytes,
+                             void* out, void* stream);
+
+/* Workspace bytes pa_decode_balanced needs on the current device (its size
+ * depends on the device's SM count); 0 for invalid sizes. */
+size_t pa_decode_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads,
+                                          int32_t head_dim);
+
 /* Splits needed for contexts up to max_context tokens (0 if split_tokens <= 0). */
 int32_t pa_decode_num_splits(int32_t max_context, int32_t split_tokens);
 

@@ -33,6 +33,9 @@ _SIGS = {
     "pa_decode": (_i32, [_p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32, _f32,
                          _i32, _i32, _p, _p, _p, _p]),
     "pa_decode_splitk_reduce": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _p, _p]),
+    "pa_decode_balanced": (_i32, [_p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32,
+                                  _f32, _p, _sz, _p, _p]),
+    "pa_decode_balanced_workspace_bytes": (_sz, [_i32, _i32, _i32]),
     "pa_decode_num_splits": (_i32, [_i32, _i32]),
     "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "pa_kv_bytes_per_token": (_i64, [_i32, _i32, _i32, _i32]),
@@ -143,9 +146,34 @@ def pa_decode_splitk_reduce(part_out, part_lse, context_lens, split_tokens: int,
         _t(out, torch.bfloat16, "out"), _stream(stream)))
 
 
+def pa_decode_balanced(q, k_cache, v_cache, block_tables, context_lens, scale: float, workspace,
+                       out, stream=None) -> None:
+    """Work-balanced persistent decode into ``out`` [B, Hq, D] bf16 in one launch.
+    ``workspace``: a zero-filled uint8 CUDA tensor of at least
+    ``pa_decode_balanced_workspace_bytes(B, Hkv, D)`` bytes (left reusable)."""
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shapes do not match q")
+    if tuple(out.shape) != (B, hq, d) or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("out / block_tables shape mismatch")
+    if context_lens.numel() != B:
+        raise ValueError("context_lens must have one entry per sequence")
+    _check("pa_decode_balanced", _lib.pa_decode_balanced(
+        _t(q, torch.bfloat16, "q"), _t(k_cache, torch.bfloat16, "k_cache"),
+        _t(v_cache, torch.bfloat16, "v_cache"), _t(block_tables, torch.int32, "block_tables"),
+        int(block_tables.shape[1]), _t(context_lens, torch.int32, "context_lens"), B, hq, hkv, d,
+        bs, nb, float(scale), _t(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _t(out, torch.bfloat16, "out"), _stream(stream)))
+
+
 # ---------------------------------------------------------------------------
 # sizes and diagnostics
 # ---------------------------------------------------------------------------
+
+def pa_decode_balanced_workspace_bytes(num_seqs: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(_lib.pa_decode_balanced_workspace_bytes(num_seqs, num_kv_heads, head_dim))
+
 
 def pa_decode_num_splits(max_context: int, split_tokens: int) -> int:
     return int(_lib.pa_decode_num_splits(int(max_context), int(split_tokens)))
@@ -174,11 +202,25 @@ def pa_last_device_error() -> int:
 # convenience: one decode call with library-sized buffers
 # ---------------------------------------------------------------------------
 
+BALANCED = -1  # schedule selector: work-balanced persistent decode (pa_decode_balanced)
+
+
 class DecodeWorkspace:
-    """Output and split partial buffers for repeated decode calls of one shape."""
+    """Output plus split partial buffers (``split_tokens > 0``) or the zero-filled
+    balanced-schedule workspace (``split_tokens == BALANCED``) for repeated decode
+    calls of one shape."""
 
     def __init__(self, num_seqs: int, num_q_heads: int, head_dim: int, split_tokens: int = 0,
-                 max_context: int = 0, device="cuda"):
+                 max_context: int = 0, device="cuda", num_kv_heads: int | None = None):
+        self.balanced = split_tokens == BALANCED
+        self.scratch = None
+        if self.balanced:
+            if num_kv_heads is None:
+                raise ValueError("the balanced schedule needs num_kv_heads")
+            with torch.cuda.device(torch.device(device)):
+                n = pa_decode_balanced_workspace_bytes(num_seqs, num_kv_heads, head_dim)
+            self.scratch = torch.zeros(n, dtype=torch.uint8, device=device)
+            split_tokens = 0
         self.split_tokens = int(split_tokens)
         self.max_splits = pa_decode_num_splits(max_context, split_tokens) if split_tokens else 0
         self.out = torch.empty((num_seqs, num_q_heads, head_dim), dtype=torch.bfloat16,
@@ -195,13 +237,19 @@ class DecodeWorkspace:
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
            ws: DecodeWorkspace | None = None, split_tokens: int = 0, max_context: int | None = None,
            stream=None) -> torch.Tensor:
-    """``pa_decode`` (+ ``pa_decode_splitk_reduce`` when split) into a workspace;
+    """``pa_decode`` (+ ``pa_decode_splitk_reduce`` when split), or
+    ``pa_decode_balanced`` when ``split_tokens == BALANCED``, into a workspace;
     returns the bf16 output [B, Hq, D]."""
     B, hq, d = q.shape
     if ws is None:
-        if split_tokens and max_context is None:
+        if split_tokens > 0 and max_context is None:
             max_context = int(block_tables.shape[1]) * int(k_cache.shape[1])
-        ws = DecodeWorkspace(B, hq, d, split_tokens, max_context or 0, q.device)
+        ws = DecodeWorkspace(B, hq, d, split_tokens, max_context or 0, q.device,
+                             num_kv_heads=int(k_cache.shape[2]))
+    if ws.balanced:
+        pa_decode_balanced(q, k_cache, v_cache, block_tables, context_lens, scale, ws.scratch,
+                           ws.out, stream)
+        return ws.out
     pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, ws.out, ws.split_tokens,
               ws.max_splits, ws.part_out, ws.part_lse, stream)
     if ws.split_tokens:

@@ -1,10 +1,13 @@
 // pa_api.cu -- status strings, sizes and shared host helpers of the C ABI.
 
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "pa_host.h"
 #include "pagedkv.h"
@@ -21,6 +24,81 @@ bool validating() {
 
 pa_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+}  // namespace
+
+bool make_cache_map(CUtensorMap* map, const void* base, int hkv, int d, long long rows,
+                    int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)hkv * d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)hkv * d * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+pa_status check_tables(const int32_t* block_tables, int mb, const int32_t* context_lens, int B,
+                       int num_blocks, int bs, int split_tokens, int max_splits,
+                       cudaStream_t stream) {
+  std::vector<int32_t> lens(B), tab((size_t)B * mb);
+  if (cudaMemcpyAsync(lens.data(), context_lens, sizeof(int32_t) * B, cudaMemcpyDeviceToHost,
+                      stream) != cudaSuccess ||
+      cudaMemcpyAsync(tab.data(), block_tables, sizeof(int32_t) * tab.size(),
+                      cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return PA_ERR_CUDA;
+  for (int b = 0; b < B; ++b) {
+    const long long ctx = lens[b];
+    if (ctx < 0 || ctx > (long long)mb * bs) return PA_ERR_INVALID_ARG;
+    if (split_tokens > 0 && ctx > (long long)max_splits * split_tokens) return PA_ERR_INVALID_ARG;
+    const long long nblk = (ctx + bs - 1) / bs;
+    for (long long i = 0; i < nblk; ++i) {
+      const int32_t v = tab[(size_t)b * mb + i];
+      if (v < 0 || v >= num_blocks) return PA_ERR_INVALID_ARG;
+    }
+  }
+  return PA_OK;
+}
+
+pa_status check_decode_args(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int32_t num_blocks, float scale, const void* out) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
+      max_blocks_per_seq <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return PA_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+  if (num_q_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (!is_pow2(block_size) || block_size > 256) return PA_ERR_UNSUPPORTED;
+  if ((long long)num_blocks * block_size >= (1ll << 31)) return PA_ERR_INVALID_ARG;
+  if ((long long)max_blocks_per_seq * block_size >= (1ll << 31)) return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_INVALID_ARG;
+  if (!(scale == scale)) return PA_ERR_INVALID_ARG;
+  return PA_OK;
 }
 
 }  // namespace pa
@@ -41,6 +119,14 @@ extern "C" size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_head
 extern "C" int64_t pa_kv_bytes_per_token(int32_t num_layers, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t bytes_per_value) {
   return 2ll * num_layers * num_kv_heads * head_dim * bytes_per_value;
+}
+
+extern "C" pa_status pa_last_device_error(int32_t* code) {
+  if (!code) return PA_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+  const unsigned int v = pa::take_decode_errors() | pa::take_balanced_errors();
+  *code = (int32_t)v;
+  return v ? PA_ERR_DEVICE : PA_OK;
 }
 
 extern "C" const char* pa_status_str(pa_status status) {

@@ -1,0 +1,504 @@
+// pa_decode_balanced.cu -- paged decode attention with a work-balanced,
+// persistent schedule (sm_103a).
+//
+// Same result as pa_decode (softmax(scale * q K^T) V per query head over each
+// sequence's paged context, "Text Generation Inference: Hugging Face's
+// production-grade LLM inference server", sections "Under the Hood:
+// PagedAttention" and "Under the Hood: Flash Attention"), scheduled for a
+// continuously batched set of sequences whose lengths differ by 60x:
+//
+//   * the work is the list of 16-token tiles of every (sequence, KV head)
+//     unit, sequence-major; its length N = Hkv * sum_b ceil(ctx_b / 16) is
+//     computed on the device by every block from context_lens (a prefix sum
+//     in shared memory), so the host needs neither the lengths nor a sync;
+//   * each block of a persistent grid (kBlocksPerSM per SM) owns the
+//     contiguous tile range [c N / C, (c + 1) N / C): every block streams the
+//     same number of tiles (to one) whatever the length mix, and no block is
+//     launched for an empty context split;
+//   * inside a block, the structure of pa_decode: a loader warp streams the
+//     range's K/V tiles through a ring of stages (TMA, or a cp.async gather
+//     below block size 8), crossing unit boundaries without a pause, and four
+//     consumer warps fold tiles round-robin, each serving the whole GQA group;
+//   * at the end of each unit the four warps' states are merged through
+//     shared memory. A unit inside one block's range is written as bf16. A
+//     unit cut by a range boundary leaves one normalised fp32 partial + base-2
+//     log-sum-exp per block; the block that arrives last on the unit's
+//     counter (an atomic ticket, no waiting) merges them by log-sum-exp and
+//     resets the counter to zero.
+// The workspace (counters + partials) must be zero-filled before its first
+// use; every call leaves the counters at zero again.
+
+#include <math.h>
+
+#include <cstring>
+
+#include "pa_device.cuh"
+#include "pa_host.h"
+#include "pa_tile.cuh"
+#include "pagedkv.h"
+
+namespace pa {
+namespace {
+
+__device__ unsigned int g_balanced_error;
+
+__device__ __forceinline__ void report(unsigned int bits) { atomicOr(&g_balanced_error, bits); }
+
+constexpr int kConsumers = 4;   // consumer warps per block
+constexpr int kStages = 4;      // ring stages per block
+constexpr int kBlocksPerSM = 4;
+constexpr int kThreads = (kConsumers + 1) * 32;
+
+struct BalParams {
+  const __nv_bfloat16* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  __nv_bfloat16* out;
+  int* counters;   // [num_seqs * Hkv]
+  float* rec_lse;  // [blocks][2][8]     base-2 LSE of each partial
+  float* rec_o;    // [blocks][2][8][D]  normalised partial outputs
+  TileSrc src;
+  int max_blocks;
+  int num_seqs;
+  int num_q_heads;
+  int group;
+  float scale_log2;
+};
+
+template <int D>
+struct BalSmem {
+  static constexpr int kStageBytes = TileGeom<D>::kStageBytes;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kMergeOff = kRingBytes;                            // [NC][8][D] fp32
+  static constexpr int kStatsOff = kMergeOff + kConsumers * kMaxGroup * D * 4;  // m, l [NC][8]
+  static constexpr int kBarOff = kStatsOff + 2 * kConsumers * kMaxGroup * 4;    // full, empty
+  static constexpr int kMiscOff = kBarOff + 2 * kStages * 8;  // abort, ticket, warp totals
+  static constexpr int kScanOff = kMiscOff + 16 + 8 * 4;      // S[B + 1]
+  static constexpr int bytes(int B) { return kScanOff + (B + 1) * 4 + 1024; }
+};
+
+__device__ __forceinline__ int tiles_of(int ctx, int cap) {
+  ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
+  return (ctx + kTile - 1) / kTile;
+}
+
+// Largest worker whose range [w N / W, (w + 1) N / W) starts at or before tile g.
+__device__ __forceinline__ int owner_of(long long g, long long N, long long W) {
+  return (int)(((g + 1) * W - 1) / N);
+}
+
+// Position (sequence, KV head, tile) in the unit list.
+struct Cursor {
+  int b, kvh, t, n;
+
+  // Place the cursor on global tile g (g < N).
+  __device__ __forceinline__ void seek(long long g, const int* S, int B, int hkv) {
+    int lo = 0, hi = B - 1;  // largest b with hkv * S[b] <= g
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((long long)hkv * S[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    n = S[b + 1] - S[b];
+    const long long r = g - (long long)hkv * S[b];
+    kvh = (int)(r / n);
+    t = (int)(r - (long long)kvh * n);
+  }
+
+  // Move to the first tile of the next unit.
+  __device__ __forceinline__ void next_unit(const int* S, int B, int hkv) {
+    t = 0;
+    if (++kvh == hkv) {
+      kvh = 0;
+      do { ++b; } while (b < B && S[b + 1] == S[b]);
+      n = b < B ? S[b + 1] - S[b] : 0;
+    }
+  }
+};
+
+template <int D, bool kTma>
+__global__ void __launch_bounds__(kThreads, kBlocksPerSM)
+    balanced_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                           const __grid_constant__ CUtensorMap tmap_v, const BalParams p) {
+  using Gm = TileGeom<D>;
+  using L = BalSmem<D>;
+  constexpr int NC = kConsumers;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* merge = reinterpret_cast<float*>(smem + L::kMergeOff);
+  float* stat_m = reinterpret_cast<float*>(smem + L::kStatsOff);
+  float* stat_l = stat_m + NC * kMaxGroup;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* empty = full + kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
+  volatile int* ticket_s = abort_flag + 1;
+  volatile int* stop_s = abort_flag + 2;
+  int* warp_tot = reinterpret_cast<int*>(smem + L::kMiscOff + 16);
+  int* S = reinterpret_cast<int*>(smem + L::kScanOff);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int B = p.num_seqs;
+  const int hkv = p.src.num_kv_heads;
+  const int G = p.group;
+  const int cap = p.max_blocks << p.src.log2_bs;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], kTma ? 1 : 32);
+      mbar_init(&empty[s], 1);
+    }
+    *abort_flag = 0;
+  }
+
+  // ---- S[b] = tiles of the sequences before b (exclusive prefix sum) -------
+  {
+    const int tid = threadIdx.x;
+    const int seg = (B + kThreads - 1) / kThreads;
+    const int lo = min(tid * seg, B), hi = min(lo + seg, B);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += tiles_of(p.context_lens[i], cap);
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += warp_tot[w];
+    int run = base + incl - sum;
+    for (int i = lo; i < hi; ++i) {
+      S[i] = run;
+      run += tiles_of(p.context_lens[i], cap);
+    }
+    if (tid == kThreads - 1) S[B] = base + incl;
+  }
+  fence_mbar_init();
+  __syncthreads();
+
+  // ---- sequences with no tokens get zero rows ------------------------------
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    if (S[b + 1] != S[b]) continue;
+    uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)b * p.num_q_heads * D);
+    for (int i = threadIdx.x; i < p.num_q_heads * D / 8; i += kThreads)
+      dst[i] = make_uint4(0, 0, 0, 0);
+  }
+
+  // ---- this block's tile range -----------------------------------------------
+  const long long N = (long long)S[B] * hkv;
+  const long long W = min((long long)gridDim.x, N);
+  const int c = blockIdx.x;
+  if (c >= W) return;
+  const long long g0 = (long long)c * N / W, g1 = (long long)(c + 1) * N / W;
+  const int count = (int)(g1 - g0);
+  const uint32_t ring = smem_u32(smem);
+
+  if (warp == NC) {
+    // ------------------------------------------------------------ loader warp
+    if (kTma && lane == 0) {
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+    }
+    Cursor ic;
+    ic.seek(g0, S, B, hkv);
+    int ic_ctx = min(max(p.context_lens[ic.b], 0), cap);
+    int ic_nblk = (ic_ctx + p.src.block_size - 1) >> p.src.log2_bs;
+    int tc_b = -1, tc_base = 0, tc_val = -1;
+    int issued = 0;
+    for (int j = 0; j < count; ++j) {
+      if (__any_sync(0xffffffffu, *abort_flag)) break;
+      const int stage = j % kStages;
+      if (j >= kStages &&
+          !__all_sync(0xffffffffu, mbar_wait(&empty[stage], ((j / kStages) - 1) & 1))) {
+        if (lane == 0) report(kErrWaitEmpty);
+        *abort_flag = 1;
+        break;
+      }
+      const int t0 = ic.t * kTile;
+      const int blk_first = t0 >> p.src.log2_bs;
+      const int blk_last = (t0 + kTile - 1) >> p.src.log2_bs;
+      if (tc_b != ic.b || blk_first < tc_base || blk_last >= tc_base + 32) {  // warp-uniform
+        tc_b = ic.b;
+        tc_base = blk_first;
+        const int idx = tc_base + lane;
+        tc_val = idx < ic_nblk ? p.block_tables[(size_t)ic.b * p.max_blocks + idx] : -1;
+      }
+      issue_tile<D, kTma>(ring + stage * Gm::kStageBytes, &full[stage], &tmap_k, &tmap_v, p.src,
+                          ic.kvh, t0, ic_ctx, ic_nblk, tc_base, tc_val, lane);
+      ++issued;
+      if (++ic.t == ic.n) {
+        const int prev_b = ic.b;
+        ic.next_unit(S, B, hkv);
+        if (ic.b != prev_b && ic.b < B) {
+          ic_ctx = min(max(p.context_lens[ic.b], 0), cap);
+          ic_nblk = (ic_ctx + p.src.block_size - 1) >> p.src.log2_bs;
+        }
+      }
+    }
+    // Drain: the last copy issued into each stage must have landed before the
+    // block may exit (its shared memory must outlive the copies).
+    const int first = issued > kStages ? issued - kStages : 0;
+    for (int j = first; j < issued; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[j % kStages], (j / kStages) & 1))) {
+        if (lane == 0) report(kErrDrain);
+        break;
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int tid = threadIdx.x;  // 0 .. NC*32-1
+  const int r0 = lane >> 2;
+  const int tk = 2 * (lane & 3);
+  Cursor uc;
+  uc.seek(g0, S, B, hkv);
+  uint32_t qf[D / 16][2];
+  AttnState<D> st;
+  int j0 = 0;  // block-local index of the current unit's first tile
+  while (j0 < count) {
+    const int b = uc.b, kvh = uc.kvh;
+    const int m = min(uc.n - uc.t, count - j0);  // this block's tiles of the unit
+    const int ctx = min(max(p.context_lens[b], 0), cap);
+    load_q_frags<D>(qf, p.q + ((size_t)b * p.num_q_heads + kvh * G) * D, G, lane);
+    st.reset();
+    // tiles j0 .. j0+m-1, round-robin: tile j -> warp j % NC
+    for (int j = j0 + ((warp - j0) % NC + NC) % NC; j < j0 + m; j += NC) {
+      if (__any_sync(0xffffffffu, *abort_flag)) break;
+      const int stage = j % kStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], (j / kStages) & 1))) {
+        if (lane == 0) report(kErrWaitFull);
+        *abort_flag = 1;
+        break;
+      }
+      const uint32_t sK = ring + stage * Gm::kStageBytes;
+      const int t = uc.t + (j - j0);
+      attend_tile<D>(st, sK, sK + Gm::kKVBytes, qf, min(kTile, ctx - t * kTile), p.scale_log2,
+                     lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+
+    // ---- merge the NC warps' states of this unit --------------------------
+    st.reduce_l();
+    if (lane < 4) {
+      stat_m[warp * kMaxGroup + tk] = st.m0;
+      stat_m[warp * kMaxGroup + tk + 1] = st.m1;
+      stat_l[warp * kMaxGroup + tk] = st.l0;
+      stat_l[warp * kMaxGroup + tk + 1] = st.l1;
+    }
+    {
+      float* base = merge + (size_t)warp * kMaxGroup * D;
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        const int d0 = mt * 16 + r0;
+        base[tk * D + d0] = st.o[mt][0];
+        base[(tk + 1) * D + d0] = st.o[mt][1];
+        base[tk * D + d0 + 8] = st.o[mt][2];
+        base[(tk + 1) * D + d0 + 8] = st.o[mt][3];
+      }
+    }
+    named_barrier_sync(1, NC * 32);
+    // one snapshot of the abort flag decides, for every consumer warp alike,
+    // whether to stop after this unit (the loader may set it at any time)
+    if (tid == 0) *stop_s = *abort_flag;
+
+    const long long U = (long long)hkv * S[b] + (long long)kvh * uc.n;
+    const int c0 = owner_of(U, N, W), c1 = owner_of(U + uc.n - 1, N, W);
+    const bool cut = c0 != c1;
+    const int rec = 2 * c + (c == c0 ? 1 : 0);
+    __nv_bfloat16* orow = p.out + ((size_t)b * p.num_q_heads + kvh * G) * D;
+    constexpr int kC8 = D / 8;
+    for (int idx = tid; idx < G * kC8; idx += NC * 32) {
+      const int g = idx / kC8, c8 = idx % kC8;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NC; ++w) M = fmaxf(M, stat_m[w * kMaxGroup + g]);
+      float Lsum = 0.f, acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int w = 0; w < NC; ++w) {
+        const float wt = exp2f(stat_m[w * kMaxGroup + g] - M);
+        Lsum += wt * stat_l[w * kMaxGroup + g];
+        const float4* src =
+            reinterpret_cast<const float4*>(merge + ((size_t)w * kMaxGroup + g) * D + c8 * 8);
+        const float4 u = src[0], v = src[1];
+        acc[0] += wt * u.x; acc[1] += wt * u.y; acc[2] += wt * u.z; acc[3] += wt * u.w;
+        acc[4] += wt * v.x; acc[5] += wt * v.y; acc[6] += wt * v.z; acc[7] += wt * v.w;
+      }
+      if (!cut) {
+        uint4 pk;
+        pk.x = pack_bf16x2(acc[0] / Lsum, acc[1] / Lsum);
+        pk.y = pack_bf16x2(acc[2] / Lsum, acc[3] / Lsum);
+        pk.z = pack_bf16x2(acc[4] / Lsum, acc[5] / Lsum);
+        pk.w = pack_bf16x2(acc[6] / Lsum, acc[7] / Lsum);
+        *reinterpret_cast<uint4*>(orow + (size_t)g * D + c8 * 8) = pk;
+      } else {
+        float4* dst = reinterpret_cast<float4*>(p.rec_o + ((size_t)rec * kMaxGroup + g) * D + c8 * 8);
+        dst[0] = make_float4(acc[0] / Lsum, acc[1] / Lsum, acc[2] / Lsum, acc[3] / Lsum);
+        dst[1] = make_float4(acc[4] / Lsum, acc[5] / Lsum, acc[6] / Lsum, acc[7] / Lsum);
+        if (c8 == 0) p.rec_lse[rec * kMaxGroup + g] = M + log2f(Lsum);
+      }
+    }
+    if (cut) {
+      __threadfence();
+      named_barrier_sync(1, NC * 32);
+      if (tid == 0) *ticket_s = atomicAdd(&p.counters[b * hkv + kvh], 1);
+      named_barrier_sync(1, NC * 32);
+      if (*ticket_s == c1 - c0) {
+        // last block on this unit: merge every block's partial by log-sum-exp
+        __threadfence();
+        for (int idx = tid; idx < G * (D / 4); idx += NC * 32) {
+          const int g = idx / (D / 4), c4 = idx % (D / 4);
+          float M = -INFINITY;
+          for (int cc = c0; cc <= c1; ++cc)
+            M = fmaxf(M, __ldcg(p.rec_lse + (2 * cc + (cc == c0 ? 1 : 0)) * kMaxGroup + g));
+          float Wsum = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int cc = c0; cc <= c1; ++cc) {
+            const int r = 2 * cc + (cc == c0 ? 1 : 0);
+            const float wt = exp2f(__ldcg(p.rec_lse + r * kMaxGroup + g) - M);
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                p.rec_o + ((size_t)r * kMaxGroup + g) * D + c4 * 4));
+            Wsum += wt;
+            acc.x += wt * v.x; acc.y += wt * v.y; acc.z += wt * v.z; acc.w += wt * v.w;
+          }
+          uint2 pk;
+          pk.x = pack_bf16x2(acc.x / Wsum, acc.y / Wsum);
+          pk.y = pack_bf16x2(acc.z / Wsum, acc.w / Wsum);
+          *reinterpret_cast<uint2*>(orow + (size_t)g * D + c4 * 4) = pk;
+        }
+        if (tid == 0) p.counters[b * hkv + kvh] = 0;
+      }
+    }
+    named_barrier_sync(1, NC * 32);  // the merge buffer is free again
+    if (*stop_s) break;
+    j0 += m;
+    uc.next_unit(S, B, hkv);
+  }
+}
+
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return sms;
+}
+
+struct WsLayout {
+  size_t counters, rec_lse, rec_o, total;
+};
+
+WsLayout ws_layout(int num_seqs, int num_kv_heads, int head_dim, int blocks) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  WsLayout l;
+  l.counters = 0;
+  l.rec_lse = up((size_t)num_seqs * num_kv_heads * sizeof(int));
+  l.rec_o = l.rec_lse + up((size_t)blocks * 2 * kMaxGroup * sizeof(float));
+  l.total = l.rec_o + (size_t)blocks * 2 * kMaxGroup * head_dim * sizeof(float);
+  return l;
+}
+
+template <int D, bool kTma>
+pa_status launch_balanced(const CUtensorMap& mk, const CUtensorMap& mv, const BalParams& prm,
+                          int sms, cudaStream_t stream) {
+  auto kern = balanced_decode_kernel<D, kTma>;
+  const int smem = BalSmem<D>::bytes(prm.num_seqs);
+  if (smem > 227 * 1024) return PA_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return PA_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
+    return PA_ERR_CUDA;
+  per_sm = per_sm < 1 ? 1 : (per_sm > kBlocksPerSM ? kBlocksPerSM : per_sm);
+  kern<<<sms * per_sm, kThreads, smem, stream>>>(mk, mv, prm);
+  return launch_status();
+}
+
+}  // namespace
+
+unsigned int take_balanced_errors() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_balanced_error, sizeof(v)) != cudaSuccess) return 0x80000000u;
+  if (v) cudaMemcpyToSymbol(g_balanced_error, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace pa
+
+extern "C" size_t pa_decode_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads,
+                                                     int32_t head_dim) {
+  using namespace pa;
+  const int sms = sm_count();
+  if (num_seqs <= 0 || num_kv_heads <= 0 || head_dim <= 0 || sms <= 0) return 0;
+  return ws_layout(num_seqs, num_kv_heads, head_dim, sms * kBlocksPerSM).total;
+}
+
+extern "C" pa_status pa_decode_balanced(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t num_seqs,
+                                        int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                        float scale, void* workspace, size_t workspace_bytes,
+                                        void* out, void* stream) {
+  using namespace pa;
+  if (num_seqs == 0) return PA_OK;
+  pa_status s = check_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                  context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                  block_size, num_blocks, scale, out);
+  if (s != PA_OK) return s;
+  const int sms = sm_count();
+  if (sms <= 0) return PA_ERR_CUDA;
+  const WsLayout lay = ws_layout(num_seqs, num_kv_heads, head_dim, sms * kBlocksPerSM);
+  if (!workspace || workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  if (validating()) {
+    s = check_tables(block_tables, max_blocks_per_seq, context_lens, num_seqs, num_blocks,
+                     block_size, 0, 0, st);
+    if (s != PA_OK) return s;
+  }
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  BalParams prm;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.block_tables = block_tables;
+  prm.context_lens = context_lens;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.counters = reinterpret_cast<int*>(ws + lay.counters);
+  prm.rec_lse = reinterpret_cast<float*>(ws + lay.rec_lse);
+  prm.rec_o = reinterpret_cast<float*>(ws + lay.rec_o);
+  prm.src.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  prm.src.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  prm.src.num_kv_heads = num_kv_heads;
+  prm.src.block_size = block_size;
+  prm.src.log2_bs = ilog2(block_size);
+  prm.src.num_blocks = num_blocks;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.num_seqs = num_seqs;
+  prm.num_q_heads = num_q_heads;
+  prm.group = num_q_heads / num_kv_heads;
+  prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+
+  CUtensorMap mk, mv;
+  std::memset(&mk, 0, sizeof(mk));
+  std::memset(&mv, 0, sizeof(mv));
+  const bool tma = block_size >= 8;
+  if (tma) {
+    const long long rows = (long long)num_blocks * block_size;
+    const int box_rows = block_size < kTile ? block_size : kTile;
+    if (!make_cache_map(&mk, k_cache, num_kv_heads, head_dim, rows, box_rows) ||
+        !make_cache_map(&mv, v_cache, num_kv_heads, head_dim, rows, box_rows))
+      return PA_ERR_CUDA;
+  }
+  if (head_dim == 128)
+    return tma ? launch_balanced<128, true>(mk, mv, prm, sms, st)
+               : launch_balanced<128, false>(mk, mv, prm, sms, st);
+  return tma ? launch_balanced<64, true>(mk, mv, prm, sms, st)
+             : launch_balanced<64, false>(mk, mv, prm, sms, st);
+}

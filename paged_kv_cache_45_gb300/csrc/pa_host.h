@@ -1,6 +1,7 @@
 // pa_host.h -- host-side helpers shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -25,5 +26,29 @@ bool validating();
 
 // Maps the last launch error to a status, clearing it.
 pa_status launch_status();
+
+// 2-D tensor map over a cache viewed as [rows = num_blocks*block_size,
+// cols = num_kv_heads*head_dim] bf16, box {64 columns, box_rows rows},
+// 128-byte swizzle, zero fill out of bounds.
+bool make_cache_map(CUtensorMap* map, const void* base, int num_kv_heads, int head_dim,
+                    long long rows, int box_rows);
+
+// Validating mode: copies context_lens / block_tables to the host (stream
+// synchronised) and range-checks them. split_tokens > 0 also bounds contexts
+// by max_splits * split_tokens.
+pa_status check_tables(const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                       int num_seqs, int num_blocks, int block_size, int split_tokens,
+                       int max_splits, cudaStream_t stream);
+
+// The shape checks every decode entry point shares; PA_OK when supported.
+pa_status check_decode_args(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int32_t num_blocks, float scale, const void* out);
+
+// Reads and clears a translation unit's device error word (synchronous).
+unsigned int take_decode_errors();
+unsigned int take_balanced_errors();
 
 }  // namespace pa

@@ -1,0 +1,232 @@
+// pa_tile.cuh -- the 16-token K/V tile shared by both decode kernels: how a
+// tile is fetched into shared memory and how one warp folds it into its
+// running attention state for the GQA group of one KV head.
+//
+// The tile math is the streaming softmax of "Text Generation Inference:
+// Hugging Face's production-grade LLM inference server" (section "Under the
+// Hood: Flash Attention"): per tile, the new running max m' per query head,
+// P = exp(S - m'), l = exp(m - m') l + sum P, O = exp(m - m') O + P V. It runs
+// in base 2 (scale * log2(e) folded into one multiply) and in transposed MMA
+// form so that the GQA group (up to 8 query heads) is the n = 8 side:
+//   S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]    (m16n8k16, bf16 -> fp32)
+//   O^T[D x 8 heads]     += V^T[D x 16] . P^T[16 x 8]
+// The score accumulator becomes the B operand of the second product through a
+// movmatrix transpose of each 8x8 half.
+//
+// Shared-memory tile layout: K then V; each is D/64 column halves of 16 rows x
+// 128 bytes with the 128-byte swizzle (16-byte chunk c of row r stored at
+// chunk c ^ (r & 7)), the layout a TMA box {64 columns, 16 rows} with
+// CU_TENSOR_MAP_SWIZZLE_128B writes. ldmatrix reads of 8 rows then hit 8
+// distinct bank groups.
+#pragma once
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+constexpr int kTile = 16;                // tokens per tile (the m of S^T)
+constexpr int kMaxGroup = 8;             // query heads per KV head (the n of the MMA)
+constexpr int kHalfBytes = kTile * 128;  // one 64-column half of a tile
+
+template <int D>
+struct TileGeom {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kKVBytes = kHalves * kHalfBytes;  // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kKVBytes;       // K then V
+};
+
+// Running state of one warp for the GQA group of one KV head.
+template <int D>
+struct AttnState {
+  float o[D / 16][4];  // O^T fragments: dims (mt*16 + lane/4 [+8]) x heads (2*(lane%4) [+1])
+  float m0, m1;        // running max (base 2) of heads 2*(lane%4), 2*(lane%4)+1
+  float l0, l1;        // this lane's part of the running sums of those heads
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+  }
+
+  // Sum the running sums over the 8 lanes that share a head pair.
+  __device__ __forceinline__ void reduce_l() {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+  }
+};
+
+// B-operand fragments of Q^T for query heads [0, G) of a group; `qg` points
+// at head 0 of the group. Heads >= G are zero.
+template <int D>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[D / 16][2], const __nv_bfloat16* qg,
+                                             int G, int lane) {
+  const int g = lane >> 2;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) qf[ks][0] = qf[ks][1] = 0u;
+  if (g < G) {
+    const unsigned int* row =
+        reinterpret_cast<const unsigned int*>(qg + (size_t)g * D + 2 * (lane & 3));
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      qf[ks][0] = __ldg(row + ks * 8);
+      qf[ks][1] = __ldg(row + ks * 8 + 4);
+    }
+  }
+}
+
+// Fold one tile (shared-memory K at sK, V at sV) into `st`. Rows >= valid are
+// masked: their scores become -inf and their V rows are zeroed in registers,
+// so stale or NaN slots past the end of a sequence cannot leak into O.
+template <int D>
+__device__ __forceinline__ void attend_tile(AttnState<D>& st, uint32_t sK, uint32_t sV,
+                                            const uint32_t (&qf)[D / 16][2], int valid,
+                                            float scale_log2, int lane) {
+  // S^T = K . Q^T  (16 tokens x 8 heads)
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    const int r = lane & 15;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int cg = 2 * ks + (lane >> 4);
+      uint32_t a[4];
+      ldsm_x4(sK + (cg >> 3) * kHalfBytes + r * 128 + (((cg & 7) ^ (r & 7)) << 4), a);
+      mma_bf16_16816(s, a, qf[ks][0], qf[ks][1]);
+    }
+  }
+  const int r0 = lane >> 2;
+  const int tk = 2 * (lane & 3);
+  const float y0 = r0 < valid ? s[0] * scale_log2 : -INFINITY;
+  const float y1 = r0 < valid ? s[1] * scale_log2 : -INFINITY;
+  const float y2 = r0 + 8 < valid ? s[2] * scale_log2 : -INFINITY;
+  const float y3 = r0 + 8 < valid ? s[3] * scale_log2 : -INFINITY;
+  float mx0 = fmaxf(y0, y2), mx1 = fmaxf(y1, y3);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+  }
+  const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
+  const float a0 = exp2f(st.m0 - mn0), a1 = exp2f(st.m1 - mn1);
+  const uint32_t p01 = pack_bf16x2(exp2f(y0 - mn0), exp2f(y1 - mn1));
+  const uint32_t p23 = pack_bf16x2(exp2f(y2 - mn0), exp2f(y3 - mn1));
+  // the running sum adds the same bf16-rounded weights the PV product uses
+  st.l0 = st.l0 * a0 + (bf16_lo(p01) + bf16_lo(p23));
+  st.l1 = st.l1 * a1 + (bf16_hi(p01) + bf16_hi(p23));
+  st.m0 = mn0;
+  st.m1 = mn1;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    st.o[mt][0] *= a0;
+    st.o[mt][1] *= a1;
+    st.o[mt][2] *= a0;
+    st.o[mt][3] *= a1;
+  }
+  const uint32_t pb0 = movmatrix_trans(p01);  // P^T tokens 0-7 as the MMA's B operand
+  const uint32_t pb1 = movmatrix_trans(p23);  // tokens 8-15
+
+  // O^T += V^T . P^T
+  uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
+  if (valid < kTile) {
+    vm01 = (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
+    vm23 = (tk + 8 < valid ? 0x0000ffffu : 0u) | (tk + 9 < valid ? 0xffff0000u : 0u);
+  }
+  const int mi = lane >> 3;
+  const int r = ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    const int cg = 2 * mt + (mi & 1);
+    uint32_t a[4];
+    ldsm_x4_trans(sV + (cg >> 3) * kHalfBytes + r * 128 + (((cg & 7) ^ (r & 7)) << 4), a);
+    a[0] &= vm01;
+    a[1] &= vm01;
+    a[2] &= vm23;
+    a[3] &= vm23;
+    mma_bf16_16816(st.o[mt], a, pb0, pb1);
+  }
+}
+
+// Where a tile's K/V rows come from.
+struct TileSrc {
+  const __nv_bfloat16* k_cache;  // for the cp.async gather (block sizes < 8)
+  const __nv_bfloat16* v_cache;
+  int num_kv_heads;
+  int block_size;
+  int log2_bs;
+  int num_blocks;
+};
+
+// Issue the copies of the tile starting at logical token t0 of one sequence
+// (KV head kvh) into the stage at sK (V follows at sK + kKVBytes), completing
+// on `full`. Warp-collective. The sequence's block-table entries
+// [tc_base, tc_base + 32) are held one per lane in tc_val (-1 past the
+// sequence's n_seq_blocks blocks); the tile's blocks must lie in that window.
+// TMA path (block_size >= 8): lane 0 issues min(bs,16)-row boxes per column
+// half; rows of blocks past the sequence or of out-of-range ids are fetched
+// from a coordinate past the pool, which TMA fills with zeros. Gather path:
+// every lane copies 16-byte chunks; tokens >= t_end and invalid blocks are
+// zero-filled without a read.
+template <int D, bool kTma>
+__device__ __forceinline__ void issue_tile(uint32_t sK, uint64_t* full, const CUtensorMap* tmap_k,
+                                           const CUtensorMap* tmap_v, const TileSrc& src, int kvh,
+                                           int t0, int t_end, int n_seq_blocks, int tc_base,
+                                           int tc_val, int lane) {
+  using Gm = TileGeom<D>;
+  const int bs = src.block_size;
+  const int blk_first = t0 >> src.log2_bs;
+  const uint32_t sV = sK + Gm::kKVBytes;
+  if constexpr (kTma) {
+    const int box_rows = bs < kTile ? bs : kTile;
+    const int oob_row = src.num_blocks * bs;  // < 2^31 (checked on the host)
+    const int phys0 = __shfl_sync(0xffffffffu, tc_val, (blk_first - tc_base) & 31);
+    const int phys1 = __shfl_sync(0xffffffffu, tc_val, (blk_first + 1 - tc_base) & 31);
+    const bool ok0 = blk_first < n_seq_blocks && phys0 >= 0 && phys0 < src.num_blocks;
+    const bool ok1 = blk_first + 1 < n_seq_blocks && phys1 >= 0 && phys1 < src.num_blocks;
+    const int row0 = ok0 ? (int)((unsigned)phys0 * (unsigned)bs +
+                                 (bs > kTile ? (unsigned)(t0 & (bs - 1)) : 0u))
+                         : oob_row;
+    const int row1 = ok1 ? (int)((unsigned)phys1 * (unsigned)bs) : oob_row;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(full, Gm::kStageBytes);
+#pragma unroll
+      for (int h = 0; h < Gm::kHalves; ++h) {
+        const int x = kvh * D + h * 64;
+        const uint32_t off = h * kHalfBytes;
+        tma_load_2d(sK + off, tmap_k, x, row0, full);
+        tma_load_2d(sV + off, tmap_v, x, row0, full);
+        if (box_rows < kTile) {  // block_size 8: the tile's second block
+          tma_load_2d(sK + off + box_rows * 128, tmap_k, x, row1, full);
+          tma_load_2d(sV + off + box_rows * 128, tmap_v, x, row1, full);
+        }
+      }
+    }
+  } else {
+    constexpr int kChunks = D / 8;  // 16-byte chunks per row
+    const size_t row_elems = (size_t)src.num_kv_heads * D;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const __nv_bfloat16* cache = which == 0 ? src.k_cache : src.v_cache;
+      const uint32_t dst_tile = which == 0 ? sK : sV;
+#pragma unroll
+      for (int k = 0; k < kTile * kChunks / 32; ++k) {
+        const int idx = k * 32 + lane;
+        const int r = idx / kChunks, c = idx % kChunks;
+        const int t = t0 + r;
+        const int blk = t >> src.log2_bs;
+        const int phys = __shfl_sync(0xffffffffu, tc_val, (blk - tc_base) & 31);
+        const bool ok = t < t_end && blk < n_seq_blocks && phys >= 0 && phys < src.num_blocks;
+        const __nv_bfloat16* p =
+            ok ? cache + ((size_t)phys * bs + (t & (bs - 1))) * row_elems + (size_t)kvh * D + c * 8
+               : cache;
+        const uint32_t dst = dst_tile + (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+        cp_async_16_zfill(dst, p, ok);
+      }
+    }
+    cp_async_arrive_noinc(full);
+  }
+}
+
+}  // namespace pa

@@ -94,6 +94,21 @@ def test_bad_arguments_are_rejected_before_any_launch(lib):
     assert decode(scale=float("nan")) == -1
     assert decode(B=0) == 0                    # nothing to do
 
+    lib.pa_decode_balanced.restype = ctypes.c_int32
+
+    def balanced(q=fake, B=2, hq=8, hkv=2, d=128, bs=16, ws=fake, ws_bytes=1 << 20):
+        return lib.pa_decode_balanced(q, fake, fake, fake, ctypes.c_int32(4), fake,
+                                      ctypes.c_int32(B), ctypes.c_int32(hq), ctypes.c_int32(hkv),
+                                      ctypes.c_int32(d), ctypes.c_int32(bs), ctypes.c_int32(16),
+                                      ctypes.c_float(0.1), ws, ctypes.c_size_t(ws_bytes), fake,
+                                      None)
+
+    assert balanced(q=None) == -1
+    assert balanced(hq=7) == -1
+    assert balanced(d=80) == -2
+    assert balanced(bs=3) == -2
+    assert balanced(B=0) == 0
+
     T = ctypes.c_int32
     assert lib.pa_kv_append(fake, fake, fake, T(4), None, fake, T(8), T(16), T(2), T(64), None) == -1
     assert lib.pa_kv_append(fake, fake, fake, T(4), fake, fake, T(8), T(16), T(2), T(60), None) == -2

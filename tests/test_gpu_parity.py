@@ -88,28 +88,73 @@ def test_append_many_rows_prefill_style(cuda_lib):
 
 def test_tiny_case(cuda_lib):
     case = wl.tiny_case(0)
-    out, _, _ = run_step(cuda_lib, case)
-    P.assert_close(P.to_f64(out), P.oracle_out(case), "tiny")
-    out16, _, _ = run_step(cuda_lib, case, split=16)
-    P.assert_close(P.to_f64(out16), P.oracle_out(case), "tiny split16")
+    for split in (0, 16, BAL):
+        out, _, _ = run_step(cuda_lib, case, split=split)
+        P.assert_close(P.to_f64(out), P.oracle_out(case), f"tiny split={split}")
 
 
 LENS = [0, 1, 2, 15, 16, 17, 31, 33, 64, 100, 257, 1000]
+BAL = -1  # binding.BALANCED: the work-balanced persistent schedule
 
 
+@pytest.mark.parametrize("sched", [0, BAL], ids=["per_split", "balanced"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (8, 2), (8, 1), (6, 2), (16, 2)])
-def test_group_and_head_dim_sweep(cuda_lib, d, hq, hkv):
+def test_group_and_head_dim_sweep(cuda_lib, d, hq, hkv, sched):
     case = wl.make_case("sweep", 100 + d + hq * 3 + hkv, LENS, hq, hkv, d, 16)
-    out, _, _ = run_step(cuda_lib, case)
-    P.assert_close(P.to_f64(out), P.oracle_out(case), f"G={hq // hkv} D={d}")
+    out, _, _ = run_step(cuda_lib, case, split=sched)
+    P.assert_close(P.to_f64(out), P.oracle_out(case), f"G={hq // hkv} D={d} sched={sched}")
 
 
+@pytest.mark.parametrize("sched", [0, BAL], ids=["per_split", "balanced"])
 @pytest.mark.parametrize("bs", [1, 2, 4, 8, 16, 32, 64, 256])
-def test_every_block_size(cuda_lib, bs):
+def test_every_block_size(cuda_lib, bs, sched):
     case = wl.make_case("bs", 200 + bs, LENS, 8, 2, 128, bs)
-    out, _, _ = run_step(cuda_lib, case)
-    P.assert_close(P.to_f64(out), P.oracle_out(case), f"bs={bs}")
+    out, _, _ = run_step(cuda_lib, case, split=sched)
+    P.assert_close(P.to_f64(out), P.oracle_out(case), f"bs={bs} sched={sched}")
+
+
+@pytest.mark.parametrize("lens", [[5], [0, 0, 3], [1] * 7, [2000, 1, 0, 17, 4096, 33] * 20,
+                                  list(range(0, 700, 7))],
+                         ids=["one_seq", "mostly_empty", "fewer_tiles_than_workers", "mixed_120",
+                              "ramp_100"])
+def test_balanced_partitions(cuda_lib, lens):
+    # fewer tiles than workers, units cut by many workers, empty sequences
+    case = wl.make_case("bal", 600 + len(lens), lens, 8, 2, 128, 16)
+    out, _, _ = run_step(cuda_lib, case, split=BAL)
+    P.assert_close(P.to_f64(out), P.oracle_out(case), f"balanced {len(lens)} seqs")
+
+
+def test_balanced_workspace_is_reusable_and_deterministic(cuda_lib):
+    b = cuda_lib
+    case = wl.make_case("bal_ws", 610, [3000, 5, 800, 0, 1234, 64] * 8, 8, 2, 128, 16,
+                        append=False)
+    d = P.dev(case)
+    ws = b.DecodeWorkspace(case.batch, 8, 128, b.BALANCED, device="cuda", num_kv_heads=2)
+    outs = []
+    for _ in range(3):
+        b.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                 case.scale, ws=ws)
+        outs.append(ws.out.clone())
+    torch.cuda.synchronize()
+    counters = ws.scratch[: case.batch * 2 * 4].view(torch.int32)
+    assert torch.all(counters == 0), "counters not left at zero"
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.equal(outs[0].view(torch.int16), outs[2].view(torch.int16))
+    P.assert_close(P.to_f64(outs[0]), P.oracle_out(case), "balanced reuse")
+
+
+def test_balanced_rejects_small_workspace(cuda_lib):
+    b = cuda_lib
+    case = wl.tiny_case(0)
+    d = P.dev(case)
+    need = b.pa_decode_balanced_workspace_bytes(case.batch, 1, 64)
+    small = torch.zeros(need - 256, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(d["q"])
+    with pytest.raises(b.PagedKVError) as e:
+        b.pa_decode_balanced(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                             d["context_lens"], case.scale, small, out)
+    assert e.value.status == -4
 
 
 @pytest.mark.parametrize("split", [16, 32, 256, 4096])
@@ -141,9 +186,10 @@ def test_split_partials_match_oracle_partials(cuda_lib):
         assert np.isnan(pl[b, :, n:]).all()      # splits past the context are not written
 
 
-def test_context_of_one_returns_v_exactly(cuda_lib):
+@pytest.mark.parametrize("sched", [0, BAL], ids=["per_split", "balanced"])
+def test_context_of_one_returns_v_exactly(cuda_lib, sched):
     case = wl.make_case("one", 400, [0, 0, 0], 8, 1, 128, 16)   # append 1 -> ctx 1
-    out, _, _ = run_step(cuda_lib, case)
+    out, _, _ = run_step(cuda_lib, case, split=sched)
     v = case.v_new.float()                                          # [B, 1, D]
     assert torch.equal(out.float().cpu(), v.expand(-1, 8, -1))
 
@@ -165,7 +211,7 @@ def test_identical_keys_give_mean_of_v(cuda_lib):
 
 def test_empty_contexts_give_zero_rows(cuda_lib):
     case = wl.make_case("empty", 402, [0, 0, 50], 8, 2, 128, 16, append=False)
-    for split in (0, 32):
+    for split in (0, 32, BAL):
         out, _, _ = run_step(cuda_lib, case, split=split, max_context=64)
         o = out.float().cpu()
         assert torch.all(o[:2] == 0) and torch.isfinite(o).all()
@@ -176,9 +222,10 @@ def test_empty_contexts_give_zero_rows(cuda_lib):
 # invariances on the GPU (block ids are names only)
 # ---------------------------------------------------------------------------
 
-def test_gpu_block_permutation_is_bit_invisible(cuda_lib):
+@pytest.mark.parametrize("sched", [0, BAL], ids=["per_split", "balanced"])
+def test_gpu_block_permutation_is_bit_invisible(cuda_lib, sched):
     case = wl.make_case("perm", 500, LENS, 8, 2, 128, 16)
-    out1, _, _ = run_step(cuda_lib, case)
+    out1, _, _ = run_step(cuda_lib, case, split=sched)
     rng = np.random.default_rng(3)
     pi = np.concatenate([[0], 1 + rng.permutation(case.num_blocks - 1)])
     pit = torch.from_numpy(pi)
@@ -188,11 +235,12 @@ def test_gpu_block_permutation_is_bit_invisible(cuda_lib):
     perm.block_tables = torch.from_numpy(pi[case.block_tables.numpy()].astype(np.int32))
     s = case.slot_mapping.numpy()
     perm.slot_mapping = torch.from_numpy(pi[s // 16] * 16 + s % 16)
-    out2, _, _ = run_step(cuda_lib, perm)
+    out2, _, _ = run_step(cuda_lib, perm, split=sched)
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
-def test_gpu_block_size_1_vs_16_bit_identical(cuda_lib):
+@pytest.mark.parametrize("sched", [0, BAL], ids=["per_split", "balanced"])
+def test_gpu_block_size_1_vs_16_bit_identical(cuda_lib, sched):
     lens = [5, 16, 40, 129]
     c16 = wl.make_case("b16", 501, lens, 8, 2, 128, 16, append=False)
     kc, vc = wl.bits(c16.k_cache), wl.bits(c16.v_cache)
@@ -214,8 +262,8 @@ def test_gpu_block_size_1_vs_16_bit_identical(cuda_lib):
     c1.k_cache = torch.from_numpy(k1.view(np.int16)).view(torch.bfloat16)
     c1.v_cache = torch.from_numpy(v1.view(np.int16)).view(torch.bfloat16)
     c1.block_tables = torch.from_numpy(tab1)
-    o16, _, _ = run_step(cuda_lib, c16)
-    o1, _, _ = run_step(cuda_lib, c1)
+    o16, _, _ = run_step(cuda_lib, c16, split=sched)
+    o1, _, _ = run_step(cuda_lib, c1, split=sched)
     assert torch.equal(o16.view(torch.int16), o1.view(torch.int16))
 
 
@@ -230,8 +278,10 @@ def test_8b_workload_full(cuda_lib, seed):
     out, _, _ = run_step(cuda_lib, case, split=split,
                          max_context=int(case.context_lens.max()))
     P.assert_close(P.to_f64(out), P.oracle_out(case), f"8b seed={seed} split={split}")
-    out0, _, _ = run_step(cuda_lib, case, split=0)
-    P.assert_close(P.to_f64(out0), P.oracle_out(case), f"8b seed={seed} unsplit")
+    ref = P.oracle_out(case)
+    for sched in (0, BAL):
+        o, _, _ = run_step(cuda_lib, case, split=sched)
+        P.assert_close(P.to_f64(o), ref, f"8b seed={seed} sched={sched}")
 
 
 def test_prefix_sharing_full(cuda_lib):
@@ -240,6 +290,8 @@ def test_prefix_sharing_full(cuda_lib):
     out, _, _ = run_step(cuda_lib, case, split=split, max_context=int(case.context_lens.max()))
     ref = P.oracle_out(case)
     P.assert_close(P.to_f64(out), ref, f"prefix split={split}")
+    out, _, _ = run_step(cuda_lib, case, split=BAL)
+    P.assert_close(P.to_f64(out), ref, "prefix balanced")
 
 
 def test_device_error_word_is_clear(cuda_lib):

@@ -22,6 +22,7 @@ def test_continuous_batching_70b_shape(cuda_lib):
     ko, vo = wl.bits(kc_cpu), wl.bits(vc_cpu)          # oracle state (CPU, updated in place)
     rng = np.random.default_rng(0)
     max_ctx = cb.max_blocks * cb.bs
+    ws_bal = b.DecodeWorkspace(cb.B, cb.Hq, cb.D, b.BALANCED, device="cuda", num_kv_heads=cb.Hkv)
     for it in range(cb.iterations):
         st = cb.step(it)
         wl.poison_blocks(kc, st.freed)
@@ -36,11 +37,15 @@ def test_continuous_batching_70b_shape(cuda_lib):
         b.pa_kv_append(st.k_new.cuda(), st.v_new.cuda(), st.slot_mapping.cuda(), kc, vc)
         pa.kv_append_inplace(ko, vo, wl.bits(st.k_new), wl.bits(st.v_new),
                              st.slot_mapping.numpy())
+        qd, btd, cld = st.q.cuda(), st.block_tables.cuda(), st.context_lens.cuda()
+        b.decode(qd, kc, vc, btd, cld, cb.scale, ws=ws_bal)            # the bench's schedule
+        got = P.to_f64(ws_bal.out)
         split = b.plan_split(st.context_lens.numpy(), cb.Hkv, b.num_sms())
-        out = b.decode(st.q.cuda(), kc, vc, st.block_tables.cuda(), st.context_lens.cuda(),
-                       cb.scale, split_tokens=split, max_context=max_ctx)
-        got = P.to_f64(out)
+        out_split = b.decode(qd, kc, vc, btd, cld, cb.scale, split_tokens=split,
+                             max_context=max_ctx)
+        got_split = P.to_f64(out_split)
         assert np.isfinite(got).all(), f"iteration {it}: NaN leaked from a poisoned block"
+        assert np.isfinite(got_split).all(), f"iteration {it}: NaN leaked (split {split})"
         if it in (0, cb.iterations - 1):
             seqs = np.arange(cb.B)
         else:
@@ -50,7 +55,8 @@ def test_continuous_batching_70b_shape(cuda_lib):
                                              longest]).astype(int))
         ref = pa.decode(wl.bits(st.q), ko, vo, st.block_tables.numpy(), st.context_lens.numpy(),
                         cb.scale, seqs=seqs)
-        P.assert_close(got[seqs], ref, f"iteration {it} split={split}")
+        P.assert_close(got[seqs], ref, f"iteration {it} balanced")
+        P.assert_close(got_split[seqs], ref, f"iteration {it} split={split}")
     torch.cuda.synchronize()
     # the whole pool after 32 iterations of appends, fills and poisoning: bit-exact
     assert np.array_equal(wl.bits(kc.cpu()), ko)
@@ -58,7 +64,7 @@ def test_continuous_batching_70b_shape(cuda_lib):
     assert b.pa_last_device_error() == 0
 
 
-@pytest.mark.parametrize("split", [4096, "planned"])
+@pytest.mark.parametrize("split", [4096, "planned", -1])
 def test_long_context_split_reduce(cuda_lib, split):
     case = wl.long_context_case(0)
     if split == "planned":
