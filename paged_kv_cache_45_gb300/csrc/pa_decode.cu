@@ -71,6 +71,10 @@ template <int D, int NCW, int STAGES, bool kTma>
 __global__ void __launch_bounds__((NCW + 1) * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+  // Every stage must belong to one consumer warp (tile i -> warp i % NCW,
+  // stage i % STAGES): a warp then polls a stage's "full" barrier only after
+  // consuming that stage's previous tile, never one phase early.
+  static_assert(STAGES % NCW == 0, "each ring stage must belong to one consumer warp");
   using L = Smem<D, NCW, STAGES>;
   using Gm = TileGeom<D>;
   extern __shared__ unsigned char smem_raw[];

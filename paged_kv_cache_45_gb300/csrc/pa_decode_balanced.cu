@@ -30,6 +30,7 @@
 
 #include <math.h>
 
+#include <cstdlib>
 #include <cstring>
 
 #include "pa_device.cuh"
@@ -44,10 +45,19 @@ __device__ unsigned int g_balanced_error;
 
 __device__ __forceinline__ void report(unsigned int bits) { atomicOr(&g_balanced_error, bits); }
 
-constexpr int kConsumers = 4;   // consumer warps per block
-constexpr int kStages = 4;      // ring stages per block
-constexpr int kBlocksPerSM = 4;
-constexpr int kThreads = (kConsumers + 1) * 32;
+// Block shapes: consumer warps, ring stages, blocks per SM. The default
+// was chosen by measurement on the 70B-shape continuous batch; the others
+// stay selectable (PA_BALANCED_SHAPE = 1, 2) for tuning on other length mixes.
+// The ring depth must be a multiple of the consumer count: then every stage
+// is always read by the same warp, which polls a stage's "full" barrier only
+// after consuming that stage's previous tile, so the barrier is never more
+// than one phase ahead of the parity the warp waits for.
+struct Shape {
+  int consumers, stages, blocks_per_sm;
+};
+constexpr Shape kShapes[] = {{4, 4, 4}, {4, 8, 2}, {8, 8, 2}};
+constexpr int kNumShapes = sizeof(kShapes) / sizeof(kShapes[0]);
+constexpr int kMaxBlocksPerSM = 4;
 
 struct BalParams {
   const __nv_bfloat16* q;
@@ -65,15 +75,18 @@ struct BalParams {
   float scale_log2;
 };
 
-template <int D>
+template <int D, int NC, int STAGES>
 struct BalSmem {
   static constexpr int kStageBytes = TileGeom<D>::kStageBytes;
-  static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kMergeOff = kRingBytes;                            // [NC][8][D] fp32
-  static constexpr int kStatsOff = kMergeOff + kConsumers * kMaxGroup * D * 4;  // m, l [NC][8]
-  static constexpr int kBarOff = kStatsOff + 2 * kConsumers * kMaxGroup * 4;    // full, empty
-  static constexpr int kMiscOff = kBarOff + 2 * kStages * 8;  // abort, ticket, warp totals
-  static constexpr int kScanOff = kMiscOff + 16 + 8 * 4;      // S[B + 1]
+  static constexpr int kRingBytes = STAGES * kStageBytes;
+  static constexpr int kMergeOff = kRingBytes;                                  // [NC][8][D] fp32
+  static constexpr int kQOff = kMergeOff + NC * kMaxGroup * D * 4;             // [2][8][D] bf16
+  static constexpr int kStatsOff = kQOff + 2 * kMaxGroup * D * 2;              // m, l [NC][8]
+  static constexpr int kBarOff = kStatsOff + 2 * NC * kMaxGroup * 4;           // barriers
+  static constexpr int kNumBars = 2 * STAGES + 4;  // full, empty, q_full[2], q_empty[2]
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // abort, ticket, stop, ctx[2]
+  static constexpr int kTotOff = kMiscOff + 32;            // warp totals [NC + 1]
+  static constexpr int kScanOff = kTotOff + (NC + 1) * 4;  // S[B + 1]
   static constexpr int bytes(int B) { return kScanOff + (B + 1) * 4 + 1024; }
 };
 
@@ -86,6 +99,11 @@ __device__ __forceinline__ int tiles_of(int ctx, int cap) {
 __device__ __forceinline__ int owner_of(long long g, long long N, long long W) {
   return (int)(((g + 1) * W - 1) / N);
 }
+
+// Column of element d of head row h in the merge buffer: XOR-swizzled in
+// groups of 8 floats so the 4 head rows one store instruction touches fall
+// in 4 different bank groups (8-float groups stay contiguous for float4).
+__device__ __forceinline__ int merge_col(int h, int d) { return d ^ ((h >> 1) << 3); }
 
 // Position (sequence, KV head, tile) in the unit list.
 struct Cursor {
@@ -116,25 +134,31 @@ struct Cursor {
   }
 };
 
-template <int D, bool kTma>
-__global__ void __launch_bounds__(kThreads, kBlocksPerSM)
+template <int D, bool kTma, int NC, int STAGES, int BPS>
+__global__ void __launch_bounds__((NC + 1) * 32, BPS)
     balanced_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const BalParams p) {
+  static_assert(STAGES % NC == 0, "each ring stage must belong to one consumer warp");
+  static_assert(BPS <= kMaxBlocksPerSM, "workspace is sized for kMaxBlocksPerSM blocks per SM");
   using Gm = TileGeom<D>;
-  using L = BalSmem<D>;
-  constexpr int NC = kConsumers;
+  using L = BalSmem<D, NC, STAGES>;
+  constexpr int kThreads = (NC + 1) * 32;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* merge = reinterpret_cast<float*>(smem + L::kMergeOff);
+  __nv_bfloat16* sq = reinterpret_cast<__nv_bfloat16*>(smem + L::kQOff);
   float* stat_m = reinterpret_cast<float*>(smem + L::kStatsOff);
   float* stat_l = stat_m + NC * kMaxGroup;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* empty = full + kStages;
+  uint64_t* empty = full + STAGES;
+  uint64_t* q_full = empty + STAGES;
+  uint64_t* q_empty = q_full + 2;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
   volatile int* ticket_s = abort_flag + 1;
   volatile int* stop_s = abort_flag + 2;
-  int* warp_tot = reinterpret_cast<int*>(smem + L::kMiscOff + 16);
+  volatile int* q_ctx = abort_flag + 3;  // [2]
+  int* warp_tot = reinterpret_cast<int*>(smem + L::kTotOff);
   int* S = reinterpret_cast<int*>(smem + L::kScanOff);
 
   const int warp = threadIdx.x >> 5;
@@ -145,9 +169,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   const int cap = p.max_blocks << p.src.log2_bs;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], kTma ? 1 : 32);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], NC);
     }
     *abort_flag = 0;
   }
@@ -195,24 +223,50 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   const long long g0 = (long long)c * N / W, g1 = (long long)(c + 1) * N / W;
   const int count = (int)(g1 - g0);
   const uint32_t ring = smem_u32(smem);
+  const uint32_t q_bytes = (uint32_t)(G * D * 2);
 
   if (warp == NC) {
     // ------------------------------------------------------------ loader warp
+    // Streams the range's K/V tiles and, ahead of each unit's first tile,
+    // the unit's q rows and context length (double-buffered q slots).
     if (kTma && lane == 0) {
       prefetch_tensormap(&tmap_k);
       prefetch_tensormap(&tmap_v);
     }
     Cursor ic;
     ic.seek(g0, S, B, hkv);
-    int ic_ctx = min(max(p.context_lens[ic.b], 0), cap);
-    int ic_nblk = (ic_ctx + p.src.block_size - 1) >> p.src.log2_bs;
+    int ic_ctx = 0, ic_nblk = 0;
     int tc_b = -1, tc_base = 0, tc_val = -1;
-    int issued = 0;
+    int issued = 0, units = 0, q_issued = 0;
+    bool unit_start = true;
     for (int j = 0; j < count; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag)) break;
-      const int stage = j % kStages;
-      if (j >= kStages &&
-          !__all_sync(0xffffffffu, mbar_wait(&empty[stage], ((j / kStages) - 1) & 1))) {
+      if (unit_start) {
+        if (ic_ctx == 0 || tc_b != ic.b) {
+          ic_ctx = min(max(p.context_lens[ic.b], 0), cap);
+          ic_nblk = (ic_ctx + p.src.block_size - 1) >> p.src.log2_bs;
+        }
+        const int slot = units & 1;
+        if (units >= 2 &&
+            !__all_sync(0xffffffffu, mbar_wait(&q_empty[slot], ((units >> 1) - 1) & 1))) {
+          if (lane == 0) report(kErrWaitEmpty);
+          *abort_flag = 1;
+          break;
+        }
+        if (lane == 0) {
+          q_ctx[slot] = ic_ctx;
+          mbar_arrive_expect_tx(&q_full[slot], q_bytes);
+          bulk_load(smem_u32(sq + slot * kMaxGroup * D),
+                    p.q + ((size_t)ic.b * p.num_q_heads + ic.kvh * G) * D, q_bytes,
+                    &q_full[slot]);
+        }
+        ++units;
+        q_issued = units;
+        unit_start = false;
+      }
+      const int stage = j % STAGES;
+      if (j >= STAGES &&
+          !__all_sync(0xffffffffu, mbar_wait(&empty[stage], ((j / STAGES) - 1) & 1))) {
         if (lane == 0) report(kErrWaitEmpty);
         *abort_flag = 1;
         break;
@@ -232,17 +286,20 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       if (++ic.t == ic.n) {
         const int prev_b = ic.b;
         ic.next_unit(S, B, hkv);
-        if (ic.b != prev_b && ic.b < B) {
-          ic_ctx = min(max(p.context_lens[ic.b], 0), cap);
-          ic_nblk = (ic_ctx + p.src.block_size - 1) >> p.src.log2_bs;
-        }
+        unit_start = true;
+        if (ic.b != prev_b) ic_ctx = 0;  // reload for the new sequence
       }
     }
-    // Drain: the last copy issued into each stage must have landed before the
-    // block may exit (its shared memory must outlive the copies).
-    const int first = issued > kStages ? issued - kStages : 0;
+    // Drain: copies still in flight must land before the block may exit.
+    const int first = issued > STAGES ? issued - STAGES : 0;
     for (int j = first; j < issued; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[j % kStages], (j / kStages) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[j % STAGES], (j / STAGES) & 1))) {
+        if (lane == 0) report(kErrDrain);
+        break;
+      }
+    }
+    for (int u = q_issued > 2 ? q_issued - 2 : 0; u < q_issued; ++u) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&q_full[u & 1], (u >> 1) & 1))) {
         if (lane == 0) report(kErrDrain);
         break;
       }
@@ -258,18 +315,29 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   uc.seek(g0, S, B, hkv);
   uint32_t qf[D / 16][2];
   AttnState<D> st;
-  int j0 = 0;  // block-local index of the current unit's first tile
+  int j0 = 0;     // block-local index of the current unit's first tile
+  int units = 0;  // units started (selects the q slot)
   while (j0 < count) {
     const int b = uc.b, kvh = uc.kvh;
     const int m = min(uc.n - uc.t, count - j0);  // this block's tiles of the unit
-    const int ctx = min(max(p.context_lens[b], 0), cap);
-    load_q_frags<D>(qf, p.q + ((size_t)b * p.num_q_heads + kvh * G) * D, G, lane);
+    const int slot = units & 1;
+    int ctx = 0;
+    if (__all_sync(0xffffffffu, mbar_wait(&q_full[slot], (units >> 1) & 1))) {
+      ctx = q_ctx[slot];
+      load_q_frags_smem<D>(qf, sq + slot * kMaxGroup * D, G, lane);
+    } else {
+      if (lane == 0) report(kErrWaitFull);
+      *abort_flag = 1;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&q_empty[slot]);
+    ++units;
     st.reset();
     // tiles j0 .. j0+m-1, round-robin: tile j -> warp j % NC
     for (int j = j0 + ((warp - j0) % NC + NC) % NC; j < j0 + m; j += NC) {
       if (__any_sync(0xffffffffu, *abort_flag)) break;
-      const int stage = j % kStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], (j / kStages) & 1))) {
+      const int stage = j % STAGES;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], (j / STAGES) & 1))) {
         if (lane == 0) report(kErrWaitFull);
         *abort_flag = 1;
         break;
@@ -295,10 +363,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) {
         const int d0 = mt * 16 + r0;
-        base[tk * D + d0] = st.o[mt][0];
-        base[(tk + 1) * D + d0] = st.o[mt][1];
-        base[tk * D + d0 + 8] = st.o[mt][2];
-        base[(tk + 1) * D + d0 + 8] = st.o[mt][3];
+        base[tk * D + merge_col(tk, d0)] = st.o[mt][0];
+        base[(tk + 1) * D + merge_col(tk + 1, d0)] = st.o[mt][1];
+        base[tk * D + merge_col(tk, d0 + 8)] = st.o[mt][2];
+        base[(tk + 1) * D + merge_col(tk + 1, d0 + 8)] = st.o[mt][3];
       }
     }
     named_barrier_sync(1, NC * 32);
@@ -324,8 +392,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       for (int w = 0; w < NC; ++w) {
         const float wt = exp2f(stat_m[w * kMaxGroup + g] - M);
         Lsum += wt * stat_l[w * kMaxGroup + g];
-        const float4* src =
-            reinterpret_cast<const float4*>(merge + ((size_t)w * kMaxGroup + g) * D + c8 * 8);
+        const float4* src = reinterpret_cast<const float4*>(
+            merge + ((size_t)w * kMaxGroup + g) * D + merge_col(g, c8 * 8));
         const float4 u = src[0], v = src[1];
         acc[0] += wt * u.x; acc[1] += wt * u.y; acc[2] += wt * u.z; acc[3] += wt * u.w;
         acc[4] += wt * v.x; acc[5] += wt * v.y; acc[6] += wt * v.z; acc[7] += wt * v.w;
@@ -345,13 +413,17 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       }
     }
     if (cut) {
-      __threadfence();
+      // Publish this block's partial: block barrier, then one thread's GPU-scope
+      // fence + ticket (the fence is cumulative over the block's stores).
       named_barrier_sync(1, NC * 32);
-      if (tid == 0) *ticket_s = atomicAdd(&p.counters[b * hkv + kvh], 1);
+      if (tid == 0) {
+        fence_acq_rel_gpu();
+        *ticket_s = atomicAdd(&p.counters[b * hkv + kvh], 1);
+        fence_acq_rel_gpu();
+      }
       named_barrier_sync(1, NC * 32);
       if (*ticket_s == c1 - c0) {
         // last block on this unit: merge every block's partial by log-sum-exp
-        __threadfence();
         for (int idx = tid; idx < G * (D / 4); idx += NC * 32) {
           const int g = idx / (D / 4), c4 = idx % (D / 4);
           float M = -INFINITY;
@@ -404,20 +476,41 @@ WsLayout ws_layout(int num_seqs, int num_kv_heads, int head_dim, int blocks) {
   return l;
 }
 
-template <int D, bool kTma>
-pa_status launch_balanced(const CUtensorMap& mk, const CUtensorMap& mv, const BalParams& prm,
-                          int sms, cudaStream_t stream) {
-  auto kern = balanced_decode_kernel<D, kTma>;
-  const int smem = BalSmem<D>::bytes(prm.num_seqs);
+template <int D, bool kTma, int NC, int STAGES, int BPS>
+pa_status launch_shape(const CUtensorMap& mk, const CUtensorMap& mv, const BalParams& prm, int sms,
+                       cudaStream_t stream) {
+  auto kern = balanced_decode_kernel<D, kTma, NC, STAGES, BPS>;
+  const int smem = BalSmem<D, NC, STAGES>::bytes(prm.num_seqs);
   if (smem > 227 * 1024) return PA_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return PA_ERR_CUDA;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, (NC + 1) * 32, smem) !=
+      cudaSuccess)
     return PA_ERR_CUDA;
-  per_sm = per_sm < 1 ? 1 : (per_sm > kBlocksPerSM ? kBlocksPerSM : per_sm);
-  kern<<<sms * per_sm, kThreads, smem, stream>>>(mk, mv, prm);
+  per_sm = per_sm < 1 ? 1 : (per_sm > BPS ? BPS : per_sm);
+  kern<<<sms * per_sm, (NC + 1) * 32, smem, stream>>>(mk, mv, prm);
   return launch_status();
+}
+
+int shape_index() {
+  static const int idx = [] {
+    const char* v = std::getenv("PA_BALANCED_SHAPE");
+    if (!v) return 0;
+    const int i = std::atoi(v);
+    return (i >= 0 && i < kNumShapes) ? i : 0;
+  }();
+  return idx;
+}
+
+template <int D, bool kTma>
+pa_status launch_balanced(const CUtensorMap& mk, const CUtensorMap& mv, const BalParams& prm,
+                          int sms, cudaStream_t stream) {
+  switch (shape_index()) {
+    case 1: return launch_shape<D, kTma, 4, 8, 2>(mk, mv, prm, sms, stream);
+    case 2: return launch_shape<D, kTma, 8, 8, 2>(mk, mv, prm, sms, stream);
+    default: return launch_shape<D, kTma, 4, 4, 4>(mk, mv, prm, sms, stream);
+  }
 }
 
 }  // namespace
@@ -436,7 +529,7 @@ extern "C" size_t pa_decode_balanced_workspace_bytes(int32_t num_seqs, int32_t n
   using namespace pa;
   const int sms = sm_count();
   if (num_seqs <= 0 || num_kv_heads <= 0 || head_dim <= 0 || sms <= 0) return 0;
-  return ws_layout(num_seqs, num_kv_heads, head_dim, sms * kBlocksPerSM).total;
+  return ws_layout(num_seqs, num_kv_heads, head_dim, sms * kMaxBlocksPerSM).total;
 }
 
 extern "C" pa_status pa_decode_balanced(const void* q, const void* k_cache, const void* v_cache,
@@ -454,7 +547,7 @@ extern "C" pa_status pa_decode_balanced(const void* q, const void* k_cache, cons
   if (s != PA_OK) return s;
   const int sms = sm_count();
   if (sms <= 0) return PA_ERR_CUDA;
-  const WsLayout lay = ws_layout(num_seqs, num_kv_heads, head_dim, sms * kBlocksPerSM);
+  const WsLayout lay = ws_layout(num_seqs, num_kv_heads, head_dim, sms * kMaxBlocksPerSM);
   if (!workspace || workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
   cudaStream_t st = as_stream(stream);

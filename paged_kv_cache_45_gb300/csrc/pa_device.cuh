@@ -99,6 +99,22 @@ __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src,
                : "memory");
 }
 
+// 1-D bulk copy global -> shared (`dst` a shared-space address); both
+// addresses 16-byte aligned, `bytes` a multiple of 16; completes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// GPU-scope acquire-release fence (orders this thread's view, cumulatively,
+// against other blocks).
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 // Arrive on `bar` once this thread's earlier cp.async copies have landed
 // (no increment of the pending count: the barrier's init count includes it).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {

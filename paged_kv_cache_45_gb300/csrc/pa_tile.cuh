@@ -78,6 +78,24 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[D / 16][2], const __
   }
 }
 
+// The same fragments from a shared-memory copy of the group's q rows
+// (bf16 [G][D]).
+template <int D>
+__device__ __forceinline__ void load_q_frags_smem(uint32_t (&qf)[D / 16][2],
+                                                  const __nv_bfloat16* sq, int G, int lane) {
+  const int g = lane >> 2;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) qf[ks][0] = qf[ks][1] = 0u;
+  if (g < G) {
+    const unsigned int* row = reinterpret_cast<const unsigned int*>(sq + g * D + 2 * (lane & 3));
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      qf[ks][0] = row[ks * 8];
+      qf[ks][1] = row[ks * 8 + 4];
+    }
+  }
+}
+
 // Fold one tile (shared-memory K at sK, V at sV) into `st`. Rows >= valid are
 // masked: their scores become -inf and their V rows are zeroed in registers,
 // so stale or NaN slots past the end of a sequence cannot leak into O.
