@@ -170,6 +170,42 @@ pa_status pa_decode_balanced(const void* q, const void* k_cache, const void* v_c
 size_t pa_decode_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads,
                                           int32_t head_dim);
 
+/*
+ * pa_decode_balanced_static -- pa_decode_balanced without a workspace argument:
+ * it allocates nothing and takes no scratch from the caller. (The source pages
+ * have no counterpart to this entry point; it exists for callers of this
+ * library.)
+ *
+ * Who needs it: callers that cannot allocate device memory at the call site.
+ * A serving engine typically reserves nearly all free HBM for its KV block
+ * pool at start-up, so a per-call cudaMalloc has nothing left to take (and
+ * cudaMalloc may synchronise the device, which a per-token decode loop cannot
+ * afford); a plug-in called from a host framework that owns all device memory
+ * may have no allocator to ask at all.
+ *
+ * Instead, the library keeps one 6 MiB scratch array in device memory
+ * (a file-scope __device__ array: every GPU that loads the library holds it
+ * until the process exits). Inputs, output, layouts and supported shapes are
+ * those of pa_decode_balanced; the output is the same.
+ *
+ *   - Shapes whose scratch (pa_decode_balanced_workspace_bytes) exceeds
+ *     6 MiB return PA_ERR_WORKSPACE without launching. On a 152-SM GB300 at
+ *     head_dim 128 that limit is about 310,000 (sequence, KV head) pairs.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture on the device.
+ *   - Every call on a device shares the one array: calls whose kernels may
+ *     overlap on the GPU (different streams without ordering between them)
+ *     race on it and must not be issued. Each call clears the part that must
+ *     start at zero (a memset on `stream`) before its kernel.
+ */
+pa_status pa_decode_balanced_static(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t* context_lens, int32_t num_seqs,
+                                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t block_size, int32_t num_blocks, float scale,
+                                    void* out, void* stream);
+
 /* Splits needed for contexts up to max_context tokens (0 if split_tokens <= 0). */
 int32_t pa_decode_num_splits(int32_t max_context, int32_t split_tokens);
 

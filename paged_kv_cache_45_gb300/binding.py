@@ -36,6 +36,8 @@ _SIGS = {
     "pa_decode_balanced": (_i32, [_p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32,
                                   _f32, _p, _sz, _p, _p]),
     "pa_decode_balanced_workspace_bytes": (_sz, [_i32, _i32, _i32]),
+    "pa_decode_balanced_static": (_i32, [_p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32,
+                                         _i32, _f32, _p, _p]),
     "pa_decode_num_splits": (_i32, [_i32, _i32]),
     "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "pa_kv_bytes_per_token": (_i64, [_i32, _i32, _i32, _i32]),
@@ -165,6 +167,28 @@ def pa_decode_balanced(q, k_cache, v_cache, block_tables, context_lens, scale: f
         int(block_tables.shape[1]), _t(context_lens, torch.int32, "context_lens"), B, hq, hkv, d,
         bs, nb, float(scale), _t(workspace, torch.uint8, "workspace"), workspace.numel(),
         _t(out, torch.bfloat16, "out"), _stream(stream)))
+
+
+def pa_decode_balanced_static(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                              out, stream=None) -> None:
+    """``pa_decode_balanced`` for callers that cannot allocate device memory:
+    no workspace argument, the library's built-in 6 MiB device array serves as
+    scratch. Calls on one device share that array, so calls whose kernels may
+    overlap on the GPU must not be issued; the first call on a device should
+    come before any stream capture (it looks the array's address up)."""
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shapes do not match q")
+    if tuple(out.shape) != (B, hq, d) or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("out / block_tables shape mismatch")
+    if context_lens.numel() != B:
+        raise ValueError("context_lens must have one entry per sequence")
+    _check("pa_decode_balanced_static", _lib.pa_decode_balanced_static(
+        _t(q, torch.bfloat16, "q"), _t(k_cache, torch.bfloat16, "k_cache"),
+        _t(v_cache, torch.bfloat16, "v_cache"), _t(block_tables, torch.int32, "block_tables"),
+        int(block_tables.shape[1]), _t(context_lens, torch.int32, "context_lens"), B, hq, hkv, d,
+        bs, nb, float(scale), _t(out, torch.bfloat16, "out"), _stream(stream)))
 
 
 # ---------------------------------------------------------------------------

@@ -32,6 +32,7 @@
 
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "pa_device.cuh"
 #include "pa_host.h"
@@ -513,6 +514,30 @@ pa_status launch_balanced(const CUtensorMap& mk, const CUtensorMap& mv, const Ba
   }
 }
 
+// ---- built-in scratch for callers that cannot allocate device memory ------
+// A fixed 6 MiB array that every device loading this library keeps until the
+// process exits. In host code `g_static_scratch` names a host-side stand-in,
+// not the device array, so its device address is looked up once per device
+// (with that device current) and cached.
+constexpr size_t kStaticScratchBytes = size_t(6) << 20;
+constexpr int kMaxDevices = 64;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device, or nullptr.
+void* static_scratch(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess) return nullptr;
+    g_static_ptr[dev] = ptr;
+  }
+  return g_static_ptr[dev];
+}
+
 }  // namespace
 
 unsigned int take_balanced_errors() {
@@ -594,4 +619,36 @@ extern "C" pa_status pa_decode_balanced(const void* q, const void* k_cache, cons
                : launch_balanced<128, false>(mk, mv, prm, sms, st);
   return tma ? launch_balanced<64, true>(mk, mv, prm, sms, st)
              : launch_balanced<64, false>(mk, mv, prm, sms, st);
+}
+
+extern "C" pa_status pa_decode_balanced_static(const void* q, const void* k_cache,
+                                               const void* v_cache, const int32_t* block_tables,
+                                               int32_t max_blocks_per_seq,
+                                               const int32_t* context_lens, int32_t num_seqs,
+                                               int32_t num_q_heads, int32_t num_kv_heads,
+                                               int32_t head_dim, int32_t block_size,
+                                               int32_t num_blocks, float scale, void* out,
+                                               void* stream) {
+  using namespace pa;
+  if (num_seqs == 0) return PA_OK;
+  pa_status s = check_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                  context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                  block_size, num_blocks, scale, out);
+  if (s != PA_OK) return s;
+  const int sms = sm_count();
+  if (sms <= 0) return PA_ERR_CUDA;
+  const WsLayout lay = ws_layout(num_seqs, num_kv_heads, head_dim, sms * kMaxBlocksPerSM);
+  if (lay.total > kStaticScratchBytes) return PA_ERR_WORKSPACE;  // beyond the built-in 6 MiB
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  unsigned char* scratch = static_cast<unsigned char*>(static_scratch(dev));
+  if (!scratch) return PA_ERR_CUDA;
+  // The array keeps whatever the previous call left; the per-unit counters
+  // must start at zero, so clear them on this call's stream first.
+  if (cudaMemsetAsync(scratch + lay.counters, 0, (size_t)num_seqs * num_kv_heads * sizeof(int),
+                      as_stream(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return pa_decode_balanced(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                            num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                            scale, scratch, kStaticScratchBytes, out, stream);
 }
