@@ -224,6 +224,15 @@ int64_t pa_kv_bytes_per_token(int32_t num_layers, int32_t num_kv_heads,
  * last call, else a nonzero bit set. Returns PA_ERR_DEVICE when nonzero. */
 pa_status pa_last_device_error(int32_t* code);
 
+/* Failure-detection self-test. Launches one warp that waits, for at most
+ * limit_us microseconds (1..2,000,000), on an mbarrier whose phase nothing
+ * completes -- the same bounded wait every decode kernel uses for its K/V
+ * tiles. The wait runs out, the kernel sets bit 8 of the device error word and
+ * returns; pa_last_device_error then reports PA_ERR_DEVICE with that bit and
+ * the context stays usable. No counterpart on the pages (they describe the
+ * serving system's failure handling, not kernels'). */
+pa_status pa_selftest_wait_timeout(int32_t limit_us, void* stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char* pa_status_str(pa_status status);
 

@@ -42,6 +42,7 @@ _SIGS = {
     "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "pa_kv_bytes_per_token": (_i64, [_i32, _i32, _i32, _i32]),
     "pa_last_device_error": (_i32, [ctypes.POINTER(_i32)]),
+    "pa_selftest_wait_timeout": (_i32, [_i32, _p]),
     "pa_status_str": (ctypes.c_char_p, [_i32]),
     "pa_version": (ctypes.c_char_p, []),
 }
@@ -211,6 +212,12 @@ def pa_decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int,
 def pa_kv_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int,
                           bytes_per_value: int) -> int:
     return int(_lib.pa_kv_bytes_per_token(num_layers, num_kv_heads, head_dim, bytes_per_value))
+
+
+def pa_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launch the bounded-wait self-test (a wait nobody completes runs out
+    after ``limit_us``); pa_last_device_error() then returns bit 8."""
+    _check("pa_selftest_wait_timeout", _lib.pa_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def pa_last_device_error() -> int:

@@ -264,6 +264,19 @@ pa_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParam
   return launch_status();
 }
 
+// One warp waits, bounded by limit_ns, on an mbarrier that expects one
+// arrival nobody makes; the wait runs out and the warp records kErrSelfTest.
+__global__ void __launch_bounds__(32) selftest_wait_kernel(unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool done = __all_sync(0xffffffffu, mbar_wait(&bar, 0, limit_ns));
+  if (!done && threadIdx.x == 0) report(kErrSelfTest);
+}
+
 }  // namespace
 
 unsigned int take_decode_errors() {
@@ -340,4 +353,11 @@ extern "C" pa_status pa_decode(const void* q, const void* k_cache, const void* v
                : launch<128, NCW, 4, false>(mk, mv, prm, num_seqs, num_kv_heads, st);
   return tma ? launch<64, NCW, 4, true>(mk, mv, prm, num_seqs, num_kv_heads, st)
              : launch<64, NCW, 4, false>(mk, mv, prm, num_seqs, num_kv_heads, st);
+}
+
+extern "C" pa_status pa_selftest_wait_timeout(int32_t limit_us, void* stream) {
+  using namespace pa;
+  if (limit_us <= 0 || limit_us > 2000000) return PA_ERR_INVALID_ARG;
+  selftest_wait_kernel<<<1, 32, 0, as_stream(stream)>>>((unsigned long long)limit_us * 1000ull);
+  return launch_status();
 }

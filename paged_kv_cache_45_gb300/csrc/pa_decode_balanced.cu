@@ -46,19 +46,18 @@ __device__ unsigned int g_balanced_error;
 
 __device__ __forceinline__ void report(unsigned int bits) { atomicOr(&g_balanced_error, bits); }
 
-// Block shapes: consumer warps, ring stages, blocks per SM. The default
-// was chosen by measurement on the 70B-shape continuous batch; the others
-// stay selectable (PA_BALANCED_SHAPE = 1, 2) for tuning on other length mixes.
+// Block shape: 4 consumer warps + 1 loader warp, a 4-stage ring, 4 blocks per
+// SM (16 tiles in flight per SM). Chosen by measurement on the 70B-shape
+// continuous batch over {4 warps x 8 stages x 2 blocks, 8 x 8 x 2}, which
+// reached 71% and 66% of HBM peak against this shape's 93%.
 // The ring depth must be a multiple of the consumer count: then every stage
 // is always read by the same warp, which polls a stage's "full" barrier only
 // after consuming that stage's previous tile, so the barrier is never more
 // than one phase ahead of the parity the warp waits for.
-struct Shape {
-  int consumers, stages, blocks_per_sm;
-};
-constexpr Shape kShapes[] = {{4, 4, 4}, {4, 8, 2}, {8, 8, 2}};
-constexpr int kNumShapes = sizeof(kShapes) / sizeof(kShapes[0]);
-constexpr int kMaxBlocksPerSM = 4;
+constexpr int kConsumers = 4;
+constexpr int kStages = 4;
+constexpr int kBlocksPerSM = 4;
+constexpr int kMaxBlocksPerSM = kBlocksPerSM;
 
 struct BalParams {
   const __nv_bfloat16* q;
@@ -76,7 +75,7 @@ struct BalParams {
   float scale_log2;
 };
 
-template <int D, int NC, int STAGES>
+template <int D, int NC, int STAGES, bool kMma = true>
 struct BalSmem {
   static constexpr int kStageBytes = TileGeom<D>::kStageBytes;
   static constexpr int kRingBytes = STAGES * kStageBytes;
@@ -87,7 +86,10 @@ struct BalSmem {
   static constexpr int kNumBars = 2 * STAGES + 4;  // full, empty, q_full[2], q_empty[2]
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // abort, ticket, stop, ctx[2]
   static constexpr int kTotOff = kMiscOff + 32;            // warp totals [NC + 1]
-  static constexpr int kScanOff = kTotOff + (NC + 1) * 4;  // S[B + 1]
+  // FMA ablation only: fp32 q rows [8][D] and per-warp weights [NC][8][16]
+  static constexpr int kQf32Off = kTotOff + (NC + 1) * 4 + 12;
+  static constexpr int kWeightsOff = kQf32Off + (kMma ? 0 : kMaxGroup * D * 4);
+  static constexpr int kScanOff = kWeightsOff + (kMma ? 0 : NC * kMaxGroup * kTile * 4);  // S[B+1]
   static constexpr int bytes(int B) { return kScanOff + (B + 1) * 4 + 1024; }
 };
 
@@ -135,14 +137,14 @@ struct Cursor {
   }
 };
 
-template <int D, bool kTma, int NC, int STAGES, int BPS>
+template <int D, bool kTma, int NC, int STAGES, int BPS, bool kMma>
 __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     balanced_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const BalParams p) {
   static_assert(STAGES % NC == 0, "each ring stage must belong to one consumer warp");
   static_assert(BPS <= kMaxBlocksPerSM, "workspace is sized for kMaxBlocksPerSM blocks per SM");
   using Gm = TileGeom<D>;
-  using L = BalSmem<D, NC, STAGES>;
+  using L = BalSmem<D, NC, STAGES, kMma>;
   constexpr int kThreads = (NC + 1) * 32;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -161,6 +163,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
   volatile int* q_ctx = abort_flag + 3;  // [2]
   int* warp_tot = reinterpret_cast<int*>(smem + L::kTotOff);
   int* S = reinterpret_cast<int*>(smem + L::kScanOff);
+  float* qs32 = reinterpret_cast<float*>(smem + L::kQf32Off);     // FMA ablation only
+  float* weights = reinterpret_cast<float*>(smem + L::kWeightsOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -316,6 +320,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
   uc.seek(g0, S, B, hkv);
   uint32_t qf[D / 16][2];
   AttnState<D> st;
+  AttnStateFma<D> sf;  // the FMA ablation's state
   int j0 = 0;     // block-local index of the current unit's first tile
   int units = 0;  // units started (selects the q slot)
   while (j0 < count) {
@@ -325,15 +330,22 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     int ctx = 0;
     if (__all_sync(0xffffffffu, mbar_wait(&q_full[slot], (units >> 1) & 1))) {
       ctx = q_ctx[slot];
-      load_q_frags_smem<D>(qf, sq + slot * kMaxGroup * D, G, lane);
+      if constexpr (kMma) {
+        load_q_frags_smem<D>(qf, sq + slot * kMaxGroup * D, G, lane);
+      } else {
+        const __nv_bfloat16* src = sq + slot * kMaxGroup * D;
+        for (int i = tid; i < kMaxGroup * D; i += NC * 32)
+          qs32[i] = i < G * D ? __bfloat162float(src[i]) : 0.f;
+      }
     } else {
       if (lane == 0) report(kErrWaitFull);
       *abort_flag = 1;
     }
+    if constexpr (!kMma) named_barrier_sync(1, NC * 32);  // fp32 q rows ready
     __syncwarp();
     if (lane == 0) mbar_arrive(&q_empty[slot]);
     ++units;
-    st.reset();
+    if constexpr (kMma) st.reset(); else sf.reset();
     // tiles j0 .. j0+m-1, round-robin: tile j -> warp j % NC
     for (int j = j0 + ((warp - j0) % NC + NC) % NC; j < j0 + m; j += NC) {
       if (__any_sync(0xffffffffu, *abort_flag)) break;
@@ -345,21 +357,25 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
       }
       const uint32_t sK = ring + stage * Gm::kStageBytes;
       const int t = uc.t + (j - j0);
-      attend_tile<D>(st, sK, sK + Gm::kKVBytes, qf, min(kTile, ctx - t * kTile), p.scale_log2,
-                     lane);
+      if constexpr (kMma)
+        attend_tile<D>(st, sK, sK + Gm::kKVBytes, qf, min(kTile, ctx - t * kTile), p.scale_log2,
+                       lane);
+      else
+        attend_tile_fma<D>(sf, sK, sK + Gm::kKVBytes, qs32, weights + warp * kMaxGroup * kTile,
+                           min(kTile, ctx - t * kTile), p.scale_log2, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
     }
 
     // ---- merge the NC warps' states of this unit --------------------------
-    st.reduce_l();
-    if (lane < 4) {
-      stat_m[warp * kMaxGroup + tk] = st.m0;
-      stat_m[warp * kMaxGroup + tk + 1] = st.m1;
-      stat_l[warp * kMaxGroup + tk] = st.l0;
-      stat_l[warp * kMaxGroup + tk + 1] = st.l1;
-    }
-    {
+    if constexpr (kMma) {
+      st.reduce_l();
+      if (lane < 4) {
+        stat_m[warp * kMaxGroup + tk] = st.m0;
+        stat_m[warp * kMaxGroup + tk + 1] = st.m1;
+        stat_l[warp * kMaxGroup + tk] = st.l0;
+        stat_l[warp * kMaxGroup + tk + 1] = st.l1;
+      }
       float* base = merge + (size_t)warp * kMaxGroup * D;
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) {
@@ -369,6 +385,20 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
         base[tk * D + merge_col(tk, d0 + 8)] = st.o[mt][2];
         base[(tk + 1) * D + merge_col(tk + 1, d0 + 8)] = st.o[mt][3];
       }
+    } else {
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h)  // static indices keep sf in registers
+        if (lane == h) {
+          stat_m[warp * kMaxGroup + h] = sf.m[h];
+          stat_l[warp * kMaxGroup + h] = sf.l[h];
+        }
+      float* base = merge + (size_t)warp * kMaxGroup * D;
+      constexpr int kCols = D / 32;
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h)
+#pragma unroll
+        for (int jc = 0; jc < kCols; ++jc)
+          base[h * D + merge_col(h, kCols * lane + jc)] = sf.o[h][jc];
     }
     named_barrier_sync(1, NC * 32);
     // one snapshot of the abort flag decides, for every consumer warp alike,
@@ -477,11 +507,11 @@ WsLayout ws_layout(int num_seqs, int num_kv_heads, int head_dim, int blocks) {
   return l;
 }
 
-template <int D, bool kTma, int NC, int STAGES, int BPS>
+template <int D, bool kTma, int NC, int STAGES, int BPS, bool kMma>
 pa_status launch_shape(const CUtensorMap& mk, const CUtensorMap& mv, const BalParams& prm, int sms,
                        cudaStream_t stream) {
-  auto kern = balanced_decode_kernel<D, kTma, NC, STAGES, BPS>;
-  const int smem = BalSmem<D, NC, STAGES>::bytes(prm.num_seqs);
+  auto kern = balanced_decode_kernel<D, kTma, NC, STAGES, BPS, kMma>;
+  const int smem = BalSmem<D, NC, STAGES, kMma>::bytes(prm.num_seqs);
   if (smem > 227 * 1024) return PA_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return PA_ERR_CUDA;
@@ -494,24 +524,22 @@ pa_status launch_shape(const CUtensorMap& mk, const CUtensorMap& mv, const BalPa
   return launch_status();
 }
 
-int shape_index() {
-  static const int idx = [] {
-    const char* v = std::getenv("PA_BALANCED_SHAPE");
-    if (!v) return 0;
-    const int i = std::atoi(v);
-    return (i >= 0 && i < kNumShapes) ? i : 0;
+// PA_DECODE_MATH=fma selects the CUDA-core ablation of the tile math (kept
+// to measure what the tensor-core form buys); anything else, the default.
+bool fma_ablation() {
+  static const bool on = [] {
+    const char* v = std::getenv("PA_DECODE_MATH");
+    return v && std::strcmp(v, "fma") == 0;
   }();
-  return idx;
+  return on;
 }
 
 template <int D, bool kTma>
 pa_status launch_balanced(const CUtensorMap& mk, const CUtensorMap& mv, const BalParams& prm,
                           int sms, cudaStream_t stream) {
-  switch (shape_index()) {
-    case 1: return launch_shape<D, kTma, 4, 8, 2>(mk, mv, prm, sms, stream);
-    case 2: return launch_shape<D, kTma, 8, 8, 2>(mk, mv, prm, sms, stream);
-    default: return launch_shape<D, kTma, 4, 4, 4>(mk, mv, prm, sms, stream);
-  }
+  if (fma_ablation())  // its larger shared-memory footprint fits 3 blocks per SM
+    return launch_shape<D, kTma, kConsumers, kStages, 3, false>(mk, mv, prm, sms, stream);
+  return launch_shape<D, kTma, kConsumers, kStages, kBlocksPerSM, true>(mk, mv, prm, sms, stream);
 }
 
 // ---- built-in scratch for callers that cannot allocate device memory ------

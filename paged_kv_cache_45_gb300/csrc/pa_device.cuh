@@ -15,6 +15,7 @@ enum : unsigned int {
   kErrWaitFull = 1u,   // a consumer waited too long for a K/V tile
   kErrWaitEmpty = 2u,  // the loader waited too long for a free stage
   kErrDrain = 4u,      // the loader could not confirm its copies had landed
+  kErrSelfTest = 8u,   // pa_selftest_wait_timeout's wait ran out, as intended
 };
 
 // A wait that runs this long is treated as lost and reported (≈1 s).
@@ -63,15 +64,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with the given parity to complete. Gives up
-// after kWaitLimitNs and returns false; never spins forever.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// after limit_ns (default kWaitLimitNs) and returns false; never spins forever.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

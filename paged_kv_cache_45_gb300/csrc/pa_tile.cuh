@@ -167,6 +167,139 @@ __device__ __forceinline__ void attend_tile(AttnState<D>& st, uint32_t sK, uint3
   }
 }
 
+// ---------------------------------------------------------------------------
+// CUDA-core ablation of attend_tile: the same streaming-softmax math on FP32
+// FMAs, kept to measure what the tensor-core form buys. A lane computes the
+// 4 scores (token lane % 16, heads 4 * (lane / 16) ..+3) from shared memory
+// (K tile, the group's q rows converted to fp32 once per unit), the weights
+// go through a per-warp shared buffer, and a lane accumulates O for its D/32
+// columns of all 8 heads.
+template <int D>
+struct AttnStateFma {
+  static constexpr int kCols = D / 32;  // output columns per lane
+  float o[kMaxGroup][kCols];
+  float m[kMaxGroup];  // running max (base 2), the same in every lane
+  float l[kMaxGroup];  // running sum, the same in every lane
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int h = 0; h < kMaxGroup; ++h) {
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) o[h][j] = 0.f;
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+    }
+  }
+};
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// qs: fp32 [8][D] q rows of the group (rows >= G zero); sp: this warp's
+// fp32 [8][16] weight buffer.
+template <int D>
+__device__ __forceinline__ void attend_tile_fma(AttnStateFma<D>& st, uint32_t sK, uint32_t sV,
+                                                const float* qs, float* sp, int valid,
+                                                float scale_log2, int lane) {
+  constexpr int kCols = D / 32;
+  const int t = lane & 15;
+  const int hq = (lane >> 4) * 4;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int c = 0; c < D / 8; ++c) {
+    uint4 kv;
+    const uint32_t addr = sK + (c >> 3) * kHalfBytes + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(kv.x), "=r"(kv.y), "=r"(kv.z), "=r"(kv.w)
+                 : "r"(addr));
+    float k8[8];
+    bf16x8_to_f32(kv, k8);
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+      const float4 qa = *reinterpret_cast<const float4*>(qs + (hq + hh) * D + c * 8);
+      const float4 qb = *reinterpret_cast<const float4*>(qs + (hq + hh) * D + c * 8 + 4);
+      acc[hh] = fmaf(k8[0], qa.x, acc[hh]); acc[hh] = fmaf(k8[1], qa.y, acc[hh]);
+      acc[hh] = fmaf(k8[2], qa.z, acc[hh]); acc[hh] = fmaf(k8[3], qa.w, acc[hh]);
+      acc[hh] = fmaf(k8[4], qb.x, acc[hh]); acc[hh] = fmaf(k8[5], qb.y, acc[hh]);
+      acc[hh] = fmaf(k8[6], qb.z, acc[hh]); acc[hh] = fmaf(k8[7], qb.w, acc[hh]);
+    }
+  }
+  // per head: tile max over the 16 tokens (lanes with the same lane / 16)
+  float y[4], mx[4];
+#pragma unroll
+  for (int hh = 0; hh < 4; ++hh) {
+    y[hh] = t < valid ? acc[hh] * scale_log2 : -INFINITY;
+    mx[hh] = y[hh];
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1)
+      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], off));
+  }
+  // every lane needs the new max of all 8 heads (the other half via xor 16)
+  float mn[kMaxGroup], alpha[kMaxGroup];
+#pragma unroll
+  for (int hh = 0; hh < 4; ++hh) {
+    const float other = __shfl_xor_sync(0xffffffffu, mx[hh], 16);
+    const float lo = lane < 16 ? mx[hh] : other;   // heads 0..3
+    const float hi = lane < 16 ? other : mx[hh];   // heads 4..7
+    mn[hh] = fmaxf(st.m[hh], lo);
+    mn[hh + 4] = fmaxf(st.m[hh + 4], hi);
+  }
+  float psum[4];
+#pragma unroll
+  for (int hh = 0; hh < 4; ++hh) {
+    const float mine = lane < 16 ? mn[hh] : mn[hh + 4];  // the new max of head hq + hh
+    const float pv = exp2f(y[hh] - mine);
+    sp[(hq + hh) * kTile + t] = pv;
+    psum[hh] = pv;
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1)
+      psum[hh] += __shfl_xor_sync(0xffffffffu, psum[hh], off);
+  }
+#pragma unroll
+  for (int hh = 0; hh < 4; ++hh) {
+    const float other = __shfl_xor_sync(0xffffffffu, psum[hh], 16);
+    const float lo = lane < 16 ? psum[hh] : other;
+    const float hi = lane < 16 ? other : psum[hh];
+    alpha[hh] = exp2f(st.m[hh] - mn[hh]);
+    alpha[hh + 4] = exp2f(st.m[hh + 4] - mn[hh + 4]);
+    st.l[hh] = st.l[hh] * alpha[hh] + lo;
+    st.l[hh + 4] = st.l[hh + 4] * alpha[hh + 4] + hi;
+  }
+#pragma unroll
+  for (int h = 0; h < kMaxGroup; ++h) {
+    st.m[h] = mn[h];
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) st.o[h][j] *= alpha[h];
+  }
+  __syncwarp();
+  // O[h][cols] += sum_t p[h][t] V[t][cols]; this lane's columns kCols*lane..
+  const int col = kCols * lane;
+  const int c = col >> 3;  // 16-byte chunk holding the columns
+  for (int tt = 0; tt < valid; ++tt) {
+    const uint32_t addr =
+        sV + (c >> 3) * kHalfBytes + tt * 128 + (((c & 7) ^ (tt & 7)) << 4) + (col & 7) * 2;
+    float v[kCols];
+    if constexpr (kCols == 4) {
+      uint32_t a, b2;
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b2) : "r"(addr));
+      v[0] = bf16_lo(a); v[1] = bf16_hi(a); v[2] = bf16_lo(b2); v[3] = bf16_hi(b2);
+    } else {
+      uint32_t a;
+      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(a) : "r"(addr));
+      v[0] = bf16_lo(a); v[1] = bf16_hi(a);
+    }
+#pragma unroll
+    for (int h = 0; h < kMaxGroup; ++h) {
+      const float pw = sp[h * kTile + tt];
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) st.o[h][j] = fmaf(pw, v[j], st.o[h][j]);
+    }
+  }
+  __syncwarp();
+}
+
 // Where a tile's K/V rows come from.
 struct TileSrc {
   const __nv_bfloat16* k_cache;  // for the cp.async gather (block sizes < 8)

@@ -321,3 +321,35 @@ except b.PagedKVError as e:
                        timeout=300)
     assert r.returncode == 0, r.stderr
     assert "rejected -1" in r.stdout
+
+
+FMA_SCRIPT = r"""
+import sys, torch, numpy as np
+sys.path.insert(0, %r)
+from paged_kv_cache_45_gb300 import binding as b, workloads as wl
+from oracle import paged_attention as pa
+from tests import parity as P
+cases = [wl.tiny_case(0),
+         wl.make_case("fma", 800, [0, 1, 15, 16, 17, 33, 100, 1000, 3000], 8, 1, 128, 16),
+         wl.make_case("fma64", 801, [5, 40, 600], 8, 2, 64, 16),
+         wl.make_case("fma_bs1", 802, [20, 70], 4, 1, 128, 1)]
+for c in cases:
+    d = P.dev(c)
+    b.pa_kv_append(d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"], d["v_cache"])
+    out = b.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                   c.scale, split_tokens=b.BALANCED)
+    torch.cuda.synchronize()
+    P.assert_close(P.to_f64(out), P.oracle_out(c), c.name)
+print("fma ok")
+"""
+
+
+def test_fma_ablation_matches_oracle(cuda_lib):
+    # the CUDA-core ablation of the tile math (PA_DECODE_MATH=fma, read once
+    # per process) must compute the same attention
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PA_DECODE_MATH="fma")
+    r = subprocess.run([sys.executable, "-c", FMA_SCRIPT % root], env=env, capture_output=True,
+                       text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-3000:]
+    assert "fma ok" in r.stdout
