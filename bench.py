@@ -8,10 +8,11 @@ and a newcomer with a prompt log-uniform in [128, 2048] joins in its slot).
 The 32-iteration schedule is drawn once and replayed cyclically (replays
 re-write the same slots, so every step has the shape of its iteration).
 
-A step is one pass of the hot path over the batch: pa_kv_append of one new
-token per sequence, then the decode over every sequence's paged context:
-pa_decode_balanced (default, one launch) or pa_decode + pa_decode_splitk_reduce
-(--schedule split). Joiners' prompt rows (a prefill stand-in) are written with
+A step is one pass of the hot path over the batch: the append of one new
+token per sequence, then the decode over every sequence's paged context. By
+default both run in one launch (pa_append_decode: the append fused into the
+work-balanced decode); --step separate launches pa_kv_append and then
+pa_decode_balanced, or pa_decode + pa_decode_splitk_reduce (--schedule split). Joiners' prompt rows (a prefill stand-in) are written with
 pa_kv_append once before the warm-up and timed apart: they set block contents,
 which the step's cost does not depend on. Inputs are resident in HBM; each
 step streams ~1.7 GB of KV, far more than the 129 MB L2, so no L2 flush is
@@ -59,6 +60,9 @@ def parse_args():
     ap.add_argument("--schedule", choices=["balanced", "split"], default="balanced",
                     help="balanced: pa_decode_balanced (one persistent launch); split: pa_decode "
                          "over fixed context splits + pa_decode_splitk_reduce")
+    ap.add_argument("--step", choices=["fused", "separate"], default="fused",
+                    help="fused: pa_append_decode (append + balanced decode in one launch); "
+                         "separate: pa_kv_append, then the decode of --schedule")
     ap.add_argument("--split", type=int, default=-1,
                     help="split_tokens for --schedule split (-1: planned; 0: no split)")
     ap.add_argument("--seed", type=int, default=0)
@@ -240,6 +244,17 @@ def traffic_per_launch(kernel: str, kv_tokens_per_launch: float):
     return None
 
 
+def combine_ranks(stats):
+    """Whole-job figures from per-rank [time_s, bytes, e2e_time_s, e2e_bytes, ...]:
+    the slowest rank's times (max) and every rank's bytes (sum). Collective
+    over the default process group (NCCL on GPUs; gloo works on CPU)."""
+    import torch.distributed as dist
+    mx, sm = stats.clone(), stats.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(sm[1]), float(mx[2]), float(sm[3])
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -284,7 +299,20 @@ def run_gpu(args):
             fk, fv, fs = it["fill"]
             b.pa_kv_append(fk, fv, fs, steps.k_cache, steps.v_cache)
 
+    fused = args.step == "fused" and ws.balanced and steps.items[0]["dev"].get("k_new") is not None
+
     def step(dv, ev=None):
+        if fused:
+            if ev is not None:
+                ev[0].record(stream)
+                ev[1].record(stream)
+            b.pa_append_decode(dv["q"], dv["k_new"], dv["v_new"], dv["slots"], steps.k_cache,
+                               steps.v_cache, dv["tables"], dv["lens"], steps.scale, ws.scratch,
+                               ws.out)
+            if ev is not None:
+                ev[2].record(stream)
+                ev[3].record(stream)
+            return
         if ev is not None:
             ev[0].record(stream)
         if dv.get("k_new") is not None:
@@ -325,8 +353,8 @@ def run_gpu(args):
     # ------------------------------------------------ the timed region: K steps
     K = args.steps
     idx = [(args.warmup + k) % n for k in range(K)]
-    per_step_launches = (1 if steps.items[0]["dev"].get("k_new") is not None else 0) + 1 + \
-        (1 if ws.split_tokens else 0)
+    per_step_launches = 1 if fused else \
+        (1 if steps.items[0]["dev"].get("k_new") is not None else 0) + 1 + (1 if ws.split_tokens else 0)
     t_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
     if sampler:
@@ -388,12 +416,7 @@ def run_gpu(args):
     stats = torch.tensor([total_s, alg_bytes, e2e_s, e2e_bytes, dec_s, dec_bytes],
                          dtype=torch.float64, device=device)
     if world > 1:
-        mx = stats.clone()
-        sm = stats.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
-        total_s, e2e_s = float(mx[0]), float(mx[2])
-        alg_bytes, e2e_bytes = float(sm[1]), float(sm[3])
+        total_s, alg_bytes, e2e_s, e2e_bytes = combine_ranks(stats)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -420,8 +443,10 @@ def run_gpu(args):
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 q/K/V; seeded lengths and block placement)",
         "config": {"workload": describe(args.workload, args.batch),
-                   "schedule": "balanced (pa_decode_balanced, one launch)" if ws.balanced else
+                   "schedule": "balanced" if ws.balanced else
                    f"split (pa_decode split_tokens={ws.split_tokens} + pa_decode_splitk_reduce)",
+                   "step": "fused: pa_append_decode, one launch" if fused else
+                   "separate: pa_kv_append + decode launches",
                    "split_tokens": ws.split_tokens, "max_splits": ws.max_splits,
                    "batch": steps.batch,
                    "l2": "no flush: each step reads ~2 GB of KV, inputs far larger than the 129 MB L2"
@@ -431,7 +456,7 @@ def run_gpu(args):
         "steps_per_s": round(K / total_s, 1),
         "kv_bytes_per_step": int(alg_bytes / K / world),
         "pct_of_datasheet_8tbs": round(100 * gbs / 8000.0, 2),
-        "ms_breakdown": {"append": round(statistics.mean(app_ms), 5),
+        "ms_breakdown": {"append": None if fused else round(statistics.mean(app_ms), 5),
                          "decode": round(statistics.mean(dec_ms), 5),
                          "reduce_or_event_gap": round(statistics.mean(red_ms), 5),
                          "steps": KI, "note": "instrumented pass, an event pair around each "

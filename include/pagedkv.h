@@ -165,6 +165,33 @@ pa_status pa_decode_balanced(const void* q, const void* k_cache, const void* v_c
                              void* workspace, size_t workspace_bytes,
                              void* out, void* stream);
 
+/*
+ * pa_append_decode -- one decode step in one launch: pa_kv_append of one new
+ * token per sequence followed by pa_decode_balanced over the contexts that
+ * include it ([TGI-PA]: the new KV pair is appended to the current block, then
+ * attention runs over the block table; fusing the bookkeeping into the
+ * attention launch follows the kernel-fusion pattern of [TGI], section
+ * "Advanced Pattern: Kernel Fusion").
+ *
+ *   k_new, v_new  bf16 [num_seqs, num_kv_heads, head_dim]: the new token of
+ *                 each sequence.
+ *   slot_mapping  int64 [num_seqs]: its slot, which must be the slot of logical
+ *                 token context_lens[b] - 1 of sequence b in block_tables[b];
+ *                 slot < 0 skips the write (the step then reads whatever that
+ *                 slot holds, as append-then-decode would).
+ *   k_cache, v_cache  written at the slots, read for attention.
+ * Everything else as pa_decode_balanced (same workspace). The result equals
+ * pa_kv_append followed by pa_decode_balanced.
+ */
+pa_status pa_append_decode(const void* q, const void* k_new, const void* v_new,
+                           const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t num_blocks, float scale,
+                           void* workspace, size_t workspace_bytes,
+                           void* out, void* stream);
+
 /* Workspace bytes pa_decode_balanced needs on the current device (its size
  * depends on the device's SM count); 0 for invalid sizes. */
 size_t pa_decode_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads,

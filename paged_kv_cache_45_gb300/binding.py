@@ -36,6 +36,8 @@ _SIGS = {
     "pa_decode_balanced": (_i32, [_p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32,
                                   _f32, _p, _sz, _p, _p]),
     "pa_decode_balanced_workspace_bytes": (_sz, [_i32, _i32, _i32]),
+    "pa_append_decode": (_i32, [_p, _p, _p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32,
+                                _i32, _i32, _f32, _p, _sz, _p, _p]),
     "pa_decode_balanced_static": (_i32, [_p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32,
                                          _i32, _f32, _p, _p]),
     "pa_decode_num_splits": (_i32, [_i32, _i32]),
@@ -167,6 +169,31 @@ def pa_decode_balanced(q, k_cache, v_cache, block_tables, context_lens, scale: f
         _t(v_cache, torch.bfloat16, "v_cache"), _t(block_tables, torch.int32, "block_tables"),
         int(block_tables.shape[1]), _t(context_lens, torch.int32, "context_lens"), B, hq, hkv, d,
         bs, nb, float(scale), _t(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _t(out, torch.bfloat16, "out"), _stream(stream)))
+
+
+def pa_append_decode(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                     context_lens, scale: float, workspace, out, stream=None) -> None:
+    """One step in one launch: append each sequence's new K/V row at its slot
+    (the slot of its last logical token) and decode, as pa_kv_append followed
+    by pa_decode_balanced. ``workspace`` as for pa_decode_balanced."""
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shapes do not match q")
+    if tuple(k_new.shape) != (B, hkv, d) or tuple(v_new.shape) != (B, hkv, d):
+        raise ValueError("k_new/v_new must be [num_seqs, num_kv_heads, head_dim]")
+    if slot_mapping.numel() != B or context_lens.numel() != B:
+        raise ValueError("slot_mapping and context_lens need one entry per sequence")
+    if tuple(out.shape) != (B, hq, d) or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("out / block_tables shape mismatch")
+    _check("pa_append_decode", _lib.pa_append_decode(
+        _t(q, torch.bfloat16, "q"), _t(k_new, torch.bfloat16, "k_new"),
+        _t(v_new, torch.bfloat16, "v_new"), _t(slot_mapping, torch.int64, "slot_mapping"),
+        _t(k_cache, torch.bfloat16, "k_cache"), _t(v_cache, torch.bfloat16, "v_cache"),
+        _t(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]),
+        _t(context_lens, torch.int32, "context_lens"), B, hq, hkv, d, bs, nb, float(scale),
+        _t(workspace, torch.uint8, "workspace"), workspace.numel(),
         _t(out, torch.bfloat16, "out"), _stream(stream)))
 
 

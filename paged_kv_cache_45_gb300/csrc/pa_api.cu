@@ -6,7 +6,9 @@
 
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <vector>
 
 #include "pa_host.h"
@@ -41,6 +43,27 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 }  // namespace
+
+pa_status prepare_kernel(const void* func, int threads, int smem_bytes, int* blocks_per_sm) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, int>, int> cache;  // -> blocks per SM
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  const auto key = std::make_tuple(func, dev, threads, smem_bytes);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it == cache.end()) {
+    int per_sm = 0;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, threads, smem_bytes) !=
+            cudaSuccess)
+      return PA_ERR_CUDA;
+    it = cache.emplace(key, per_sm < 1 ? 1 : per_sm).first;
+  }
+  if (blocks_per_sm) *blocks_per_sm = it->second;
+  return PA_OK;
+}
 
 bool make_cache_map(CUtensorMap* map, const void* base, int hkv, int d, long long rows,
                     int box_rows) {

@@ -256,9 +256,9 @@ pa_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParam
                  int num_kv_heads, cudaStream_t stream) {
   using L = Smem<D, NCW, STAGES>;
   auto kern = paged_decode_kernel<D, NCW, STAGES, kTma>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
-      cudaSuccess)
-    return PA_ERR_CUDA;
+  const pa_status s =
+      prepare_kernel(reinterpret_cast<const void*>(kern), (NCW + 1) * 32, L::kAlloc, nullptr);
+  if (s != PA_OK) return s;
   dim3 grid(num_kv_heads, prm.split_tokens > 0 ? prm.max_splits : 1, B);
   kern<<<grid, (NCW + 1) * 32, L::kAlloc, stream>>>(mk, mv, prm);
   return launch_status();

@@ -73,6 +73,13 @@ struct BalParams {
   int num_q_heads;
   int group;
   float scale_log2;
+  // fused append (pa_append_decode): one new K/V row per sequence
+  const __nv_bfloat16* k_new;  // [num_seqs, Hkv, D]
+  const __nv_bfloat16* v_new;
+  const int64_t* slot_mapping;  // [num_seqs]
+  __nv_bfloat16* k_dst;         // the caches, written at the slots
+  __nv_bfloat16* v_dst;
+  long long num_slots;
 };
 
 template <int D, int NC, int STAGES, bool kMma = true>
@@ -81,7 +88,8 @@ struct BalSmem {
   static constexpr int kRingBytes = STAGES * kStageBytes;
   static constexpr int kMergeOff = kRingBytes;                                  // [NC][8][D] fp32
   static constexpr int kQOff = kMergeOff + NC * kMaxGroup * D * 4;             // [2][8][D] bf16
-  static constexpr int kStatsOff = kQOff + 2 * kMaxGroup * D * 2;              // m, l [NC][8]
+  static constexpr int kNewOff = kQOff + 2 * kMaxGroup * D * 2;  // [2][K,V][D] bf16 (fused append)
+  static constexpr int kStatsOff = kNewOff + 2 * 2 * D * 2;                    // m, l [NC][8]
   static constexpr int kBarOff = kStatsOff + 2 * NC * kMaxGroup * 4;           // barriers
   static constexpr int kNumBars = 2 * STAGES + 4;  // full, empty, q_full[2], q_empty[2]
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // abort, ticket, stop, ctx[2]
@@ -137,7 +145,7 @@ struct Cursor {
   }
 };
 
-template <int D, bool kTma, int NC, int STAGES, int BPS, bool kMma>
+template <int D, bool kTma, int NC, int STAGES, int BPS, bool kMma, bool kAppend>
 __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     balanced_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const BalParams p) {
@@ -161,6 +169,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
   volatile int* ticket_s = abort_flag + 1;
   volatile int* stop_s = abort_flag + 2;
   volatile int* q_ctx = abort_flag + 3;  // [2]
+  __nv_bfloat16* s_new = reinterpret_cast<__nv_bfloat16*>(smem + L::kNewOff);  // [2][2][D]
   int* warp_tot = reinterpret_cast<int*>(smem + L::kTotOff);
   int* S = reinterpret_cast<int*>(smem + L::kScanOff);
   float* qs32 = reinterpret_cast<float*>(smem + L::kQf32Off);     // FMA ablation only
@@ -212,12 +221,24 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
   fence_mbar_init();
   __syncthreads();
 
-  // ---- sequences with no tokens get zero rows ------------------------------
+  // ---- sequences with no tokens get zero rows (and, fused, their append) ---
   for (int b = blockIdx.x; b < B; b += gridDim.x) {
     if (S[b + 1] != S[b]) continue;
     uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)b * p.num_q_heads * D);
     for (int i = threadIdx.x; i < p.num_q_heads * D / 8; i += kThreads)
       dst[i] = make_uint4(0, 0, 0, 0);
+    if constexpr (kAppend) {
+      const long long slot = p.slot_mapping[b];
+      if (slot >= 0 && slot < p.num_slots) {
+        const size_t row = (size_t)hkv * D / 8;  // 16-byte chunks per pool row
+        const uint4* ks = reinterpret_cast<const uint4*>(p.k_new) + (size_t)b * row;
+        const uint4* vs = reinterpret_cast<const uint4*>(p.v_new) + (size_t)b * row;
+        for (size_t i = threadIdx.x; i < row; i += kThreads) {
+          reinterpret_cast<uint4*>(p.k_dst)[slot * row + i] = ks[i];
+          reinterpret_cast<uint4*>(p.v_dst)[slot * row + i] = vs[i];
+        }
+      }
+    }
   }
 
   // ---- this block's tile range -----------------------------------------------
@@ -260,7 +281,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
         }
         if (lane == 0) {
           q_ctx[slot] = ic_ctx;
-          mbar_arrive_expect_tx(&q_full[slot], q_bytes);
+          if constexpr (kAppend) {
+            // the unit's new K/V row, for the fused append
+            mbar_arrive_expect_tx(&q_full[slot], q_bytes + 4 * D);
+            const size_t row = ((size_t)ic.b * hkv + ic.kvh) * D;
+            bulk_load(smem_u32(s_new + slot * 2 * D), p.k_new + row, 2 * D, &q_full[slot]);
+            bulk_load(smem_u32(s_new + slot * 2 * D + D), p.v_new + row, 2 * D, &q_full[slot]);
+          } else {
+            mbar_arrive_expect_tx(&q_full[slot], q_bytes);
+          }
           bulk_load(smem_u32(sq + slot * kMaxGroup * D),
                     p.q + ((size_t)ic.b * p.num_q_heads + ic.kvh * G) * D, q_bytes,
                     &q_full[slot]);
@@ -328,8 +357,16 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     const int m = min(uc.n - uc.t, count - j0);  // this block's tiles of the unit
     const int slot = units & 1;
     int ctx = 0;
+    long long new_slot = -1;
+    uint2 k_piece = make_uint2(0, 0), v_piece = make_uint2(0, 0);
     if (__all_sync(0xffffffffu, mbar_wait(&q_full[slot], (units >> 1) & 1))) {
       ctx = q_ctx[slot];
+      if constexpr (kAppend) {
+        if (4 * lane < D) {
+          k_piece = *reinterpret_cast<const uint2*>(s_new + slot * 2 * D + 4 * lane);
+          v_piece = *reinterpret_cast<const uint2*>(s_new + slot * 2 * D + D + 4 * lane);
+        }
+      }
       if constexpr (kMma) {
         load_q_frags_smem<D>(qf, sq + slot * kMaxGroup * D, G, lane);
       } else {
@@ -346,6 +383,17 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     if (lane == 0) mbar_arrive(&q_empty[slot]);
     ++units;
     if constexpr (kMma) st.reset(); else sf.reset();
+    // Fused append: the warp that folds the unit's last tile (which holds the
+    // new token, logical position ctx - 1) writes the new K/V row of this KV
+    // head to the pool and patches it into that tile after the tile lands.
+    // No other block reads that row in this step.
+    bool owns_new = false;
+    if constexpr (kAppend) {
+      const int last = j0 + (uc.n - 1 - uc.t);  // block-local index of the unit's last tile
+      owns_new = uc.n - uc.t <= count - j0 && last % NC == warp;
+      // issued now, first used at the unit's last tile: the load overlaps the tiles
+      if (owns_new) new_slot = __ldg(p.slot_mapping + b);
+    }
     // tiles j0 .. j0+m-1, round-robin: tile j -> warp j % NC
     for (int j = j0 + ((warp - j0) % NC + NC) % NC; j < j0 + m; j += NC) {
       if (__any_sync(0xffffffffu, *abort_flag)) break;
@@ -357,6 +405,26 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
       }
       const uint32_t sK = ring + stage * Gm::kStageBytes;
       const int t = uc.t + (j - j0);
+      if constexpr (kAppend) {
+        if (owns_new && t == uc.n - 1 && new_slot >= 0 && new_slot < p.num_slots) {
+          if (4 * lane < D) {
+            const int r = (ctx - 1) & (kTile - 1);  // the new token's row in the tile
+            const int c = lane >> 1;                 // 16-byte chunk of this lane's 8 bytes
+            const uint32_t off = (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4) +
+                                 (lane & 1) * 8;
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(sK + off), "r"(k_piece.x),
+                         "r"(k_piece.y)
+                         : "memory");
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(sK + Gm::kKVBytes + off),
+                         "r"(v_piece.x), "r"(v_piece.y)
+                         : "memory");
+            const size_t g = ((size_t)new_slot * hkv + kvh) * D + 4 * lane;
+            *reinterpret_cast<uint2*>(p.k_dst + g) = k_piece;
+            *reinterpret_cast<uint2*>(p.v_dst + g) = v_piece;
+          }
+          __syncwarp();
+        }
+      }
       if constexpr (kMma)
         attend_tile<D>(st, sK, sK + Gm::kKVBytes, qf, min(kTile, ctx - t * kTile), p.scale_log2,
                        lane);
@@ -507,19 +575,17 @@ WsLayout ws_layout(int num_seqs, int num_kv_heads, int head_dim, int blocks) {
   return l;
 }
 
-template <int D, bool kTma, int NC, int STAGES, int BPS, bool kMma>
+template <int D, bool kTma, int NC, int STAGES, int BPS, bool kMma, bool kAppend>
 pa_status launch_shape(const CUtensorMap& mk, const CUtensorMap& mv, const BalParams& prm, int sms,
                        cudaStream_t stream) {
-  auto kern = balanced_decode_kernel<D, kTma, NC, STAGES, BPS, kMma>;
+  auto kern = balanced_decode_kernel<D, kTma, NC, STAGES, BPS, kMma, kAppend>;
   const int smem = BalSmem<D, NC, STAGES, kMma>::bytes(prm.num_seqs);
   if (smem > 227 * 1024) return PA_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return PA_ERR_CUDA;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, (NC + 1) * 32, smem) !=
-      cudaSuccess)
-    return PA_ERR_CUDA;
-  per_sm = per_sm < 1 ? 1 : (per_sm > BPS ? BPS : per_sm);
+  const pa_status s = prepare_kernel(reinterpret_cast<const void*>(kern), (NC + 1) * 32, smem,
+                                     &per_sm);
+  if (s != PA_OK) return s;
+  per_sm = per_sm > BPS ? BPS : per_sm;
   kern<<<sms * per_sm, (NC + 1) * 32, smem, stream>>>(mk, mv, prm);
   return launch_status();
 }
@@ -537,9 +603,13 @@ bool fma_ablation() {
 template <int D, bool kTma>
 pa_status launch_balanced(const CUtensorMap& mk, const CUtensorMap& mv, const BalParams& prm,
                           int sms, cudaStream_t stream) {
+  if (prm.slot_mapping)
+    return launch_shape<D, kTma, kConsumers, kStages, kBlocksPerSM, true, true>(mk, mv, prm, sms,
+                                                                              stream);
   if (fma_ablation())  // its larger shared-memory footprint fits 3 blocks per SM
-    return launch_shape<D, kTma, kConsumers, kStages, 3, false>(mk, mv, prm, sms, stream);
-  return launch_shape<D, kTma, kConsumers, kStages, kBlocksPerSM, true>(mk, mv, prm, sms, stream);
+    return launch_shape<D, kTma, kConsumers, kStages, 3, false, false>(mk, mv, prm, sms, stream);
+  return launch_shape<D, kTma, kConsumers, kStages, kBlocksPerSM, true, false>(mk, mv, prm, sms,
+                                                                             stream);
 }
 
 // ---- built-in scratch for callers that cannot allocate device memory ------
@@ -585,19 +655,26 @@ extern "C" size_t pa_decode_balanced_workspace_bytes(int32_t num_seqs, int32_t n
   return ws_layout(num_seqs, num_kv_heads, head_dim, sms * kMaxBlocksPerSM).total;
 }
 
-extern "C" pa_status pa_decode_balanced(const void* q, const void* k_cache, const void* v_cache,
-                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                        const int32_t* context_lens, int32_t num_seqs,
-                                        int32_t num_q_heads, int32_t num_kv_heads,
-                                        int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                                        float scale, void* workspace, size_t workspace_bytes,
-                                        void* out, void* stream) {
-  using namespace pa;
+namespace pa {
+namespace {
+
+// Shared body of pa_decode_balanced and pa_append_decode (k_new == nullptr:
+// no fused append).
+pa_status balanced_entry(const void* q, const void* k_new, const void* v_new,
+                         const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         int32_t num_blocks, float scale, void* workspace, size_t workspace_bytes,
+                         void* out, void* stream) {
   if (num_seqs == 0) return PA_OK;
   pa_status s = check_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                   context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                                   block_size, num_blocks, scale, out);
   if (s != PA_OK) return s;
+  const bool fused = k_new != nullptr;
+  if (fused && (!v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new)))
+    return PA_ERR_INVALID_ARG;
   const int sms = sm_count();
   if (sms <= 0) return PA_ERR_CUDA;
   const WsLayout lay = ws_layout(num_seqs, num_kv_heads, head_dim, sms * kMaxBlocksPerSM);
@@ -630,6 +707,12 @@ extern "C" pa_status pa_decode_balanced(const void* q, const void* k_cache, cons
   prm.num_q_heads = num_q_heads;
   prm.group = num_q_heads / num_kv_heads;
   prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  prm.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  prm.slot_mapping = fused ? slot_mapping : nullptr;
+  prm.k_dst = static_cast<__nv_bfloat16*>(k_cache);
+  prm.v_dst = static_cast<__nv_bfloat16*>(v_cache);
+  prm.num_slots = (long long)num_blocks * block_size;
 
   CUtensorMap mk, mv;
   std::memset(&mk, 0, sizeof(mk));
@@ -647,6 +730,37 @@ extern "C" pa_status pa_decode_balanced(const void* q, const void* k_cache, cons
                : launch_balanced<128, false>(mk, mv, prm, sms, st);
   return tma ? launch_balanced<64, true>(mk, mv, prm, sms, st)
              : launch_balanced<64, false>(mk, mv, prm, sms, st);
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_decode_balanced(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t num_seqs,
+                                        int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                        float scale, void* workspace, size_t workspace_bytes,
+                                        void* out, void* stream) {
+  return pa::balanced_entry(q, nullptr, nullptr, nullptr, const_cast<void*>(k_cache),
+                            const_cast<void*>(v_cache), block_tables, max_blocks_per_seq,
+                            context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                            block_size, num_blocks, scale, workspace, workspace_bytes, out, stream);
+}
+
+extern "C" pa_status pa_append_decode(const void* q, const void* k_new, const void* v_new,
+                                      const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                      float scale, void* workspace, size_t workspace_bytes,
+                                      void* out, void* stream) {
+  if (!k_new) return PA_ERR_INVALID_ARG;
+  return pa::balanced_entry(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                            max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                            head_dim, block_size, num_blocks, scale, workspace, workspace_bytes,
+                            out, stream);
 }
 
 extern "C" pa_status pa_decode_balanced_static(const void* q, const void* k_cache,

@@ -47,6 +47,14 @@ pa_status check_decode_args(const void* q, const void* k_cache, const void* v_ca
                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                             int32_t num_blocks, float scale, const void* out);
 
+// Prepares a kernel for a launch with `smem_bytes` of dynamic shared memory on
+// the current device and returns its resident blocks per SM (>= 1) in
+// *blocks_per_sm (may be null). The attribute call and the occupancy query
+// run once per (kernel, device, size); later calls only read a cache, so a
+// warmed-up entry point issues nothing but its launch (safe inside stream
+// capture).
+pa_status prepare_kernel(const void* func, int threads, int smem_bytes, int* blocks_per_sm);
+
 // Reads and clears a translation unit's device error word (synchronous).
 unsigned int take_decode_errors();
 unsigned int take_balanced_errors();

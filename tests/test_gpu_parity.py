@@ -353,3 +353,48 @@ def test_fma_ablation_matches_oracle(cuda_lib):
                        text=True, timeout=600, cwd=root)
     assert r.returncode == 0, r.stderr[-3000:]
     assert "fma ok" in r.stdout
+
+
+@pytest.mark.parametrize("lens,hq,hkv,d,bs", [
+    ([1, 7, 16, 33], 2, 1, 64, 16),                           # the tiny workload
+    (LENS, 8, 2, 128, 16),
+    ([0, 15, 16, 31, 47, 300, 1023, 2048], 8, 1, 128, 8),
+    ([3, 40, 600, 17], 4, 4, 64, 1),
+    ([5000, 2, 9, 128] * 12, 16, 2, 128, 32),
+], ids=["tiny", "edges", "bs8_g8", "bs1_mha", "mixed_bs32"])
+def test_fused_append_decode_matches_append_then_decode(cuda_lib, lens, hq, hkv, d, bs):
+    b = cuda_lib
+    case = wl.make_case("fused", 900 + len(lens) + bs, lens, hq, hkv, d, bs)
+    dv = P.dev(case)
+    ws = torch.zeros(b.pa_decode_balanced_workspace_bytes(case.batch, hkv, d), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.full_like(dv["q"], float("nan"))
+    b.pa_append_decode(dv["q"], dv["k_new"], dv["v_new"], dv["slot_mapping"], dv["k_cache"],
+                       dv["v_cache"], dv["block_tables"], dv["context_lens"], case.scale, ws, out)
+    torch.cuda.synchronize()
+    kc, vc = P.oracle_caches(case)
+    assert np.array_equal(wl.bits(dv["k_cache"].cpu()), kc)     # the append, bit-exact
+    assert np.array_equal(wl.bits(dv["v_cache"].cpu()), vc)
+    P.assert_close(P.to_f64(out), P.oracle_out(case, caches=(kc, vc)), "fused step")
+
+
+def test_fused_append_skips_negative_slots(cuda_lib):
+    b = cuda_lib
+    case = wl.make_case("fused_skip", 950, [20, 33, 7], 8, 2, 128, 16)
+    dv = P.dev(case)
+    slots = dv["slot_mapping"].clone()
+    slots[1] = -1
+    ws = torch.zeros(b.pa_decode_balanced_workspace_bytes(3, 2, 128), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty_like(dv["q"])
+    b.pa_append_decode(dv["q"], dv["k_new"], dv["v_new"], slots, dv["k_cache"], dv["v_cache"],
+                       dv["block_tables"], dv["context_lens"], case.scale, ws, out)
+    torch.cuda.synchronize()
+    kc, vc = pa.kv_append(wl.bits(case.k_cache), wl.bits(case.v_cache), wl.bits(case.k_new),
+                          wl.bits(case.v_new), slots.cpu().numpy())
+    assert np.array_equal(wl.bits(dv["k_cache"].cpu()), kc)
+    o = P.to_f64(out)
+    ref = P.oracle_out(case, caches=(kc, vc))
+    # sequence 1 attends over its (NaN-poisoned) unwritten slot, like append-then-decode
+    assert np.isnan(ref[1]).all()
+    P.assert_close(o[[0, 2]], ref[[0, 2]], "fused step with a skipped slot")
