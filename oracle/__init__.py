@@ -25,4 +25,11 @@ from .paged_attention import (  # noqa: F401
     decode_split_partials,
     lse_merge,
     decode_pseudocode_loops,
+    e4m3_value,
+    e4m3_encode,
+    e4m3_decode,
+    quantize_rows_e4m3,
+    kv_append_fp8_inplace,
+    dequantize_pool,
+    decode_fp8,
 )

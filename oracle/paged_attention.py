@@ -320,3 +320,107 @@ def decode_pseudocode_loops(q, k_cache, v_cache, block_tables, context_lens,
                              for e in range(d)])
         out.append(per_head)
     return out
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) KV cache
+# ---------------------------------------------------------------------------
+# "How to Speed Up LLM Inference: KV Cache to Production Serving" (section "The
+# KV cache: the memory problem that runs the show": quantizing the cache itself
+# to FP8 halves the bytes per token) and the FP8 row of "Text Generation
+# Inference ..." (section "Production Pattern: KV Cache Math", 163,840 B/token)
+# fix only the byte count. Readings taken: the OCP e4m3 format (1 sign bit,
+# 4 exponent bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 is
+# NaN, largest finite 448); one scale per KV head for K and one for V; a stored
+# code is the round-to-nearest-even e4m3 value of x / scale computed in
+# float32, saturated to +-448; a code reads back as value(code) * scale.
+
+def e4m3_value(code: int) -> float:
+    """The real number an e4m3 code stands for (NaN for the two NaN codes)."""
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    exp = (code >> 3) & 0xF
+    man = code & 0x7
+    if exp == 0xF and man == 0x7:
+        return math.nan
+    if exp == 0:                                   # subnormal: man/8 * 2^(1-7)
+        return sign * (man / 8.0) * 2.0 ** -6
+    return sign * (1.0 + man / 8.0) * 2.0 ** (exp - 7)
+
+
+E4M3_TABLE = np.array([e4m3_value(c) for c in range(256)], dtype=np.float64)
+E4M3_MAX = 448.0
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Round each float to the nearest e4m3 code, ties to the even code,
+    saturating finite values beyond +-448 to +-448; NaN -> 0x7F."""
+    x = np.asarray(x, dtype=np.float64)
+    pos = np.array([c for c in range(0x7F)], dtype=np.int64)      # 0x00 .. 0x7E, increasing
+    vals = E4M3_TABLE[pos]
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    hi = np.searchsorted(vals, a, side="left")                      # first value >= a
+    hi = np.clip(hi, 0, len(vals) - 1)
+    lo = np.clip(hi - 1, 0, len(vals) - 1)
+    d_lo, d_hi = a - vals[lo], vals[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (pos[hi] % 2 == 0) & (hi != lo))
+    code = np.where(pick_hi, pos[hi], pos[lo])
+    code = np.where(a == vals[hi], pos[hi], code)
+    code = code | np.where(np.signbit(x), 0x80, 0)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """float64 values of e4m3 codes (uint8)."""
+    c = np.asarray(codes)
+    if c.dtype != np.uint8:
+        raise TypeError("e4m3 codes must be uint8")
+    return E4M3_TABLE[c]
+
+
+def quantize_rows_e4m3(rows_bf16_bits: np.ndarray, scale_per_head) -> np.ndarray:
+    """e4m3 codes of bf16 rows [..., H_kv, D]: x / scale_h in float32, then
+    e4m3_encode."""
+    x = (np.asarray(rows_bf16_bits).astype(np.uint32) << np.uint32(16)).view(np.float32)
+    s = np.asarray(scale_per_head, dtype=np.float32)[:, None]
+    return e4m3_encode((x / s).astype(np.float32))
+
+
+def kv_append_fp8_inplace(k_codes, v_codes, k_new_bits, v_new_bits, slot_mapping,
+                          k_scale, v_scale) -> None:
+    """The append into an e4m3 pool: quantize each new row, write it at its slot
+    (slot < 0 skipped, a slot past the pool is an error)."""
+    kq = quantize_rows_e4m3(k_new_bits, k_scale)
+    vq = quantize_rows_e4m3(v_new_bits, v_scale)
+    kv_append_inplace(k_codes, v_codes, kq, vq, slot_mapping)
+
+
+def dequantize_pool(codes: np.ndarray, scale_per_head) -> np.ndarray:
+    """float64 [NB, bs, H_kv, D] values of an e4m3 pool."""
+    return e4m3_decode(codes) * np.asarray(scale_per_head, dtype=np.float64)[:, None]
+
+
+def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens,
+               scale: float, seqs=None) -> np.ndarray:
+    """:func:`decode` over an e4m3 pool: the K/V rows are read back as
+    value(code) * scale of their head, then the same softmax attention."""
+    G = _group(q, k_codes)
+    rows = _seq_list(q.shape[0], seqs)
+    hq, d = q.shape[1], q.shape[2]
+    ks = np.asarray(k_scale, dtype=np.float64)
+    vs = np.asarray(v_scale, dtype=np.float64)
+    out = np.zeros((len(rows), hq, d), dtype=np.float64)
+    for i, b in enumerate(rows):
+        ctx = int(context_lens[b])
+        if ctx == 0:
+            continue
+        K = e4m3_decode(gather_sequence(k_codes, block_tables[b], ctx)) * ks[:, None]
+        V = e4m3_decode(gather_sequence(v_codes, block_tables[b], ctx)) * vs[:, None]
+        qb = bf16_bits_to_f64(q[b])
+        for h in range(hq):
+            kvh = h // G
+            s = scale * (K[:, kvh, :] @ qb[h])
+            p = np.exp(s - s.max())
+            out[i, h] = (p @ V[:, kvh, :]) / p.sum()
+    return out

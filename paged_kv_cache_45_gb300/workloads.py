@@ -384,3 +384,20 @@ def kv_bytes_of_step(context_lens, num_kv_heads: int, head_dim: int,
     """Algorithmic KV bytes one decode step reads: each cached token's K and V
     row of every KV head exactly once (one layer)."""
     return int(np.asarray(context_lens, dtype=np.int64).sum()) * 2 * num_kv_heads * head_dim * bytes_per_value
+
+
+def fp8_pool(case: DecodeCase, seed: int = 0) -> dict:
+    """An e4m3 copy of a case's pool for the FP8 KV cache: per-KV-head scales
+    drawn in [1/32, 3/64) (N(0,1) values stay far inside the +-448 range), codes
+    by torch's float8_e4m3fn cast of value / scale (NaN-poisoned slots stay NaN)."""
+    rng = np.random.Generator(np.random.PCG64(seed + 11_000))
+    H = case.num_kv_heads
+    ks = (1.0 / 32.0 * (1.0 + 0.5 * rng.random(H))).astype(np.float32)
+    vs = (1.0 / 32.0 * (1.0 + 0.5 * rng.random(H))).astype(np.float32)
+
+    def codes(pool, s):
+        x = pool.float() / torch.from_numpy(s)[:, None]
+        return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+    return {"k_codes": codes(case.k_cache, ks), "v_codes": codes(case.v_cache, vs),
+            "k_scale": torch.from_numpy(ks), "v_scale": torch.from_numpy(vs)}
