@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["cb70b", "8b", "long", "prefix"], default="cb70b")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                    help="fp8: the same workload on an e4m3 KV pool with per-head scales "
+                         "(balanced schedule only)")
     ap.add_argument("--schedule", choices=["balanced", "split"], default="balanced",
                     help="balanced: pa_decode_balanced (one persistent launch); split: pa_decode "
                          "over fixed context splits + pa_decode_splitk_reduce")
@@ -98,11 +101,13 @@ def describe(workload: str, batch: int = 256) -> str:
 class Steps:
     """Device-resident inputs of a workload's steps, cycled by index."""
 
-    def __init__(self, workload: str, seed: int, device, batch: int = 256):
+    def __init__(self, workload: str, seed: int, device, batch: int = 256, kv_dtype="bf16"):
+        import numpy as np
         import torch
         from paged_kv_cache_45_gb300 import workloads as wl
         self.workload = workload
         self.items = []
+        self.fp8 = kv_dtype == "fp8"
         if workload == "cb70b":
             cb = wl.ContinuousBatching(seed=seed, batch=batch)
             self.k_cache, self.v_cache = cb.initial_caches(device)
@@ -130,9 +135,26 @@ class Steps:
             it["host"] = {k: it[k].pin_memory() for k in ("q", "k_new", "v_new", "slots", "tables",
                                                            "lens") if it[k] is not None}
             it["dev"] = {k: v.to(device) for k, v in it["host"].items()}
-            it["kv_bytes"] = int(it["lens"].to(torch.int64).sum()) * 2 * self.hkv * self.d * 2
+            it["kv_bytes"] = (int(it["lens"].to(torch.int64).sum()) * 2 * self.hkv * self.d *
+                              (1 if self.fp8 else 2))
             it["qo_bytes"] = 2 * it["q"].numel() * 2
         self.batch = int(self.items[0]["q"].shape[0])
+        if self.fp8:   # e4m3 copy of the pool (per-KV-head scales), made on the device
+            gen = np.random.Generator(np.random.PCG64(seed + 11_000))
+            ks = (1.0 / 32.0 * (1.0 + 0.5 * gen.random(self.hkv))).astype(np.float32)
+            vs = (1.0 / 32.0 * (1.0 + 0.5 * gen.random(self.hkv))).astype(np.float32)
+            self.k_scale = torch.from_numpy(ks).to(device)
+            self.v_scale = torch.from_numpy(vs).to(device)
+
+            def codes(pool, sc):
+                out = torch.empty(pool.shape, dtype=torch.uint8, device=device)
+                for i in range(0, pool.shape[0], 4096):   # chunks: bounded temporaries
+                    x = pool[i:i + 4096].float() / sc[:, None]
+                    out[i:i + 4096] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+                return out
+            self.k_cache = codes(self.k_cache, self.k_scale)
+            self.v_cache = codes(self.v_cache, self.v_scale)
+            torch.cuda.synchronize(device)
 
     def __len__(self):
         return len(self.items)
@@ -214,6 +236,7 @@ def measured_hbm_peak():
 
 KERNEL_SOURCES = {
     "balanced_decode_kernel": ("pa_decode_balanced.cu", "pa_tile.cuh", "pa_device.cuh"),
+    "balanced_decode_kernel[e4m3]": ("pa_decode_balanced.cu", "pa_tile.cuh", "pa_device.cuh"),
     "paged_decode_kernel": ("pa_decode.cu", "pa_tile.cuh", "pa_device.cuh"),
 }
 
@@ -280,7 +303,9 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline_subprocess(args)
 
-    steps = Steps(args.workload, args.seed + rank, device, args.batch)
+    steps = Steps(args.workload, args.seed + rank, device, args.batch, args.kv_dtype)
+    if steps.fp8 and args.schedule != "balanced":
+        raise SystemExit("--kv-dtype fp8 runs the balanced schedule only")
     sms = b.num_sms(local)
     if args.schedule == "balanced":
         split = b.BALANCED
@@ -297,7 +322,11 @@ def run_gpu(args):
     def fill(it):
         if it["fill"] is not None:
             fk, fv, fs = it["fill"]
-            b.pa_kv_append(fk, fv, fs, steps.k_cache, steps.v_cache)
+            if steps.fp8:
+                b.pa_kv_append_fp8(fk, fv, fs, steps.k_cache, steps.v_cache, steps.k_scale,
+                                   steps.v_scale)
+            else:
+                b.pa_kv_append(fk, fv, fs, steps.k_cache, steps.v_cache)
 
     fused = args.step == "fused" and ws.balanced and steps.items[0]["dev"].get("k_new") is not None
 
@@ -306,9 +335,15 @@ def run_gpu(args):
             if ev is not None:
                 ev[0].record(stream)
                 ev[1].record(stream)
-            b.pa_append_decode(dv["q"], dv["k_new"], dv["v_new"], dv["slots"], steps.k_cache,
-                               steps.v_cache, dv["tables"], dv["lens"], steps.scale, ws.scratch,
-                               ws.out)
+            if steps.fp8:
+                b.pa_append_decode_fp8(dv["q"], dv["k_new"], dv["v_new"], dv["slots"],
+                                       steps.k_cache, steps.v_cache, steps.k_scale,
+                                       steps.v_scale, dv["tables"], dv["lens"], steps.scale,
+                                       ws.scratch, ws.out)
+            else:
+                b.pa_append_decode(dv["q"], dv["k_new"], dv["v_new"], dv["slots"],
+                                   steps.k_cache, steps.v_cache, dv["tables"], dv["lens"],
+                                   steps.scale, ws.scratch, ws.out)
             if ev is not None:
                 ev[2].record(stream)
                 ev[3].record(stream)
@@ -316,12 +351,22 @@ def run_gpu(args):
         if ev is not None:
             ev[0].record(stream)
         if dv.get("k_new") is not None:
-            b.pa_kv_append(dv["k_new"], dv["v_new"], dv["slots"], steps.k_cache, steps.v_cache)
+            if steps.fp8:
+                b.pa_kv_append_fp8(dv["k_new"], dv["v_new"], dv["slots"], steps.k_cache,
+                                   steps.v_cache, steps.k_scale, steps.v_scale)
+            else:
+                b.pa_kv_append(dv["k_new"], dv["v_new"], dv["slots"], steps.k_cache,
+                               steps.v_cache)
         if ev is not None:
             ev[1].record(stream)
         if ws.balanced:
-            b.pa_decode_balanced(dv["q"], steps.k_cache, steps.v_cache, dv["tables"], dv["lens"],
-                                 steps.scale, ws.scratch, ws.out)
+            if steps.fp8:
+                b.pa_decode_balanced_fp8(dv["q"], steps.k_cache, steps.v_cache, steps.k_scale,
+                                         steps.v_scale, dv["tables"], dv["lens"], steps.scale,
+                                         ws.scratch, ws.out)
+            else:
+                b.pa_decode_balanced(dv["q"], steps.k_cache, steps.v_cache, dv["tables"],
+                                     dv["lens"], steps.scale, ws.scratch, ws.out)
         else:
             b.pa_decode(dv["q"], steps.k_cache, steps.v_cache, dv["tables"], dv["lens"],
                         steps.scale, ws.out, ws.split_tokens, ws.max_splits, ws.part_out,
@@ -426,7 +471,8 @@ def run_gpu(args):
     gbs = alg_bytes / total_s / 1e9
     dec_gbs_rank0 = dec_bytes / dec_s / 1e9
     kv_tokens_per_launch = kv_tokens / KI
-    kernel = "balanced_decode_kernel" if ws.balanced else "paged_decode_kernel"
+    kernel = ("balanced_decode_kernel" + ("[e4m3]" if steps.fp8 else "")) if ws.balanced \
+        else "paged_decode_kernel"
     traffic = traffic_per_launch(kernel, kv_tokens_per_launch)
     clocks = sampler.summary() if sampler else None
     line = {
@@ -440,9 +486,10 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "e4m3 KV, bf16 q/out" if steps.fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) bf16 q/K/V; seeded lengths and block placement)",
-        "config": {"workload": describe(args.workload, args.batch),
+        "config": {"workload": describe(args.workload, args.batch) +
+                   (" (e4m3 KV pool, per-KV-head scales)" if steps.fp8 else ""),
                    "schedule": "balanced" if ws.balanced else
                    f"split (pa_decode split_tokens={ws.split_tokens} + pa_decode_splitk_reduce)",
                    "step": "fused: pa_append_decode, one launch" if fused else

@@ -192,6 +192,53 @@ pa_status pa_append_decode(const void* q, const void* k_new, const void* v_new,
                            void* workspace, size_t workspace_bytes,
                            void* out, void* stream);
 
+/*
+ * FP8 KV cache. [SPEED] ("The KV cache: the memory problem that runs the
+ * show": quantizing the cache to FP8 halves the 320 KB/token) and the FP8 row
+ * of [TGI-KV] (163,840 B/token for the 70B class) fix the byte count; the
+ * format and scaling are this library's reading:
+ *   k_cache, v_cache  uint8 [num_blocks, block_size, num_kv_heads, head_dim],
+ *                     OCP e4m3 codes (bias 7, no infinities, largest 448).
+ *   k_scale, v_scale  fp32 [num_kv_heads], device: a code c of head h stands
+ *                     for value(c) * scale[h].
+ * Quantization (the appends): code = e4m3 round-to-nearest-even of
+ * x / scale[h] computed in fp32 (round to nearest), saturated to +-448.
+ * Supported: head_dim 128, at most 64 KV heads; otherwise PA_ERR_UNSUPPORTED.
+ */
+
+/* pa_kv_append for an FP8 pool: each new bf16 K/V row is quantized to codes. */
+pa_status pa_kv_append_fp8(const void* k_new, const void* v_new,
+                           const int64_t* slot_mapping, int32_t num_tokens,
+                           void* k_cache, void* v_cache,
+                           const float* k_scale, const float* v_scale,
+                           int32_t num_blocks, int32_t block_size,
+                           int32_t num_kv_heads, int32_t head_dim, void* stream);
+
+/* pa_decode_balanced over an FP8 pool: codes are read back as value * scale
+ * (the scales folded into the score factor and the output), the tile math runs
+ * on f16 MMAs (every e4m3 value is exact in f16). Same workspace. */
+pa_status pa_decode_balanced_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                 const float* k_scale, const float* v_scale,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens, int32_t num_seqs,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, int32_t num_blocks, float scale,
+                                 void* workspace, size_t workspace_bytes,
+                                 void* out, void* stream);
+
+/* pa_append_decode over an FP8 pool: the new rows are quantized at their slots
+ * and decoded in the same launch. Equals pa_kv_append_fp8 followed by
+ * pa_decode_balanced_fp8. */
+pa_status pa_append_decode_fp8(const void* q, const void* k_new, const void* v_new,
+                               const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, int32_t num_seqs,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int32_t num_blocks, float scale,
+                               void* workspace, size_t workspace_bytes,
+                               void* out, void* stream);
+
 /* Workspace bytes pa_decode_balanced needs on the current device (its size
  * depends on the device's SM count); 0 for invalid sizes. */
 size_t pa_decode_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads,

@@ -38,6 +38,11 @@ _SIGS = {
     "pa_decode_balanced_workspace_bytes": (_sz, [_i32, _i32, _i32]),
     "pa_append_decode": (_i32, [_p, _p, _p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32,
                                 _i32, _i32, _f32, _p, _sz, _p, _p]),
+    "pa_kv_append_fp8": (_i32, [_p, _p, _p, _i32, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _p]),
+    "pa_decode_balanced_fp8": (_i32, [_p, _p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32,
+                                      _i32, _i32, _f32, _p, _sz, _p, _p]),
+    "pa_append_decode_fp8": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i32, _p, _i32, _i32,
+                                    _i32, _i32, _i32, _i32, _f32, _p, _sz, _p, _p]),
     "pa_decode_balanced_static": (_i32, [_p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32,
                                          _i32, _f32, _p, _p]),
     "pa_decode_num_splits": (_i32, [_i32, _i32]),
@@ -191,6 +196,70 @@ def pa_append_decode(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tabl
         _t(q, torch.bfloat16, "q"), _t(k_new, torch.bfloat16, "k_new"),
         _t(v_new, torch.bfloat16, "v_new"), _t(slot_mapping, torch.int64, "slot_mapping"),
         _t(k_cache, torch.bfloat16, "k_cache"), _t(v_cache, torch.bfloat16, "v_cache"),
+        _t(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]),
+        _t(context_lens, torch.int32, "context_lens"), B, hq, hkv, d, bs, nb, float(scale),
+        _t(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _t(out, torch.bfloat16, "out"), _stream(stream)))
+
+
+def _fp8_shapes(k_cache, v_cache, k_scale, v_scale):
+    nb, bs, hkv, d = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache shapes differ")
+    if k_scale.numel() != hkv or v_scale.numel() != hkv:
+        raise ValueError("k_scale/v_scale need one entry per KV head")
+    return nb, bs, hkv, d
+
+
+def pa_kv_append_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                     stream=None) -> None:
+    """Quantize ``k_new``/``v_new`` [T, Hkv, D] bf16 to e4m3 codes (x / scale of
+    the head) at ``slot_mapping`` of the uint8 caches [NB, bs, Hkv, D]."""
+    nb, bs, hkv, d = _fp8_shapes(k_cache, v_cache, k_scale, v_scale)
+    T = k_new.shape[0]
+    if tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d):
+        raise ValueError("k_new/v_new must be [T, num_kv_heads, head_dim]")
+    if slot_mapping.numel() != T:
+        raise ValueError("slot_mapping needs one entry per token")
+    _check("pa_kv_append_fp8", _lib.pa_kv_append_fp8(
+        _t(k_new, torch.bfloat16, "k_new"), _t(v_new, torch.bfloat16, "v_new"),
+        _t(slot_mapping, torch.int64, "slot_mapping"), T, _t(k_cache, torch.uint8, "k_cache"),
+        _t(v_cache, torch.uint8, "v_cache"), _t(k_scale, torch.float32, "k_scale"),
+        _t(v_scale, torch.float32, "v_scale"), nb, bs, hkv, d, _stream(stream)))
+
+
+def pa_decode_balanced_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                           scale: float, workspace, out, stream=None) -> None:
+    """pa_decode_balanced over uint8 e4m3 caches with per-KV-head scales."""
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = _fp8_shapes(k_cache, v_cache, k_scale, v_scale)
+    if d2 != d or tuple(out.shape) != (B, hq, d) or block_tables.shape[0] != B:
+        raise ValueError("q / out / cache / block_tables shapes do not match")
+    _check("pa_decode_balanced_fp8", _lib.pa_decode_balanced_fp8(
+        _t(q, torch.bfloat16, "q"), _t(k_cache, torch.uint8, "k_cache"),
+        _t(v_cache, torch.uint8, "v_cache"), _t(k_scale, torch.float32, "k_scale"),
+        _t(v_scale, torch.float32, "v_scale"), _t(block_tables, torch.int32, "block_tables"),
+        int(block_tables.shape[1]), _t(context_lens, torch.int32, "context_lens"), B, hq, hkv, d,
+        bs, nb, float(scale), _t(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _t(out, torch.bfloat16, "out"), _stream(stream)))
+
+
+def pa_append_decode_fp8(q, k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                         block_tables, context_lens, scale: float, workspace, out,
+                         stream=None) -> None:
+    """pa_append_decode over uint8 e4m3 caches: quantize the new rows at their
+    slots and decode, one launch."""
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = _fp8_shapes(k_cache, v_cache, k_scale, v_scale)
+    if d2 != d or tuple(out.shape) != (B, hq, d) or block_tables.shape[0] != B:
+        raise ValueError("q / out / cache / block_tables shapes do not match")
+    if tuple(k_new.shape) != (B, hkv, d) or tuple(v_new.shape) != (B, hkv, d):
+        raise ValueError("k_new/v_new must be [num_seqs, num_kv_heads, head_dim]")
+    _check("pa_append_decode_fp8", _lib.pa_append_decode_fp8(
+        _t(q, torch.bfloat16, "q"), _t(k_new, torch.bfloat16, "k_new"),
+        _t(v_new, torch.bfloat16, "v_new"), _t(slot_mapping, torch.int64, "slot_mapping"),
+        _t(k_cache, torch.uint8, "k_cache"), _t(v_cache, torch.uint8, "v_cache"),
+        _t(k_scale, torch.float32, "k_scale"), _t(v_scale, torch.float32, "v_scale"),
         _t(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]),
         _t(context_lens, torch.int32, "context_lens"), B, hq, hkv, d, bs, nb, float(scale),
         _t(workspace, torch.uint8, "workspace"), workspace.numel(),

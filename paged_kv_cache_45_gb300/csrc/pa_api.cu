@@ -66,14 +66,16 @@ pa_status prepare_kernel(const void* func, int threads, int smem_bytes, int* blo
 }
 
 bool make_cache_map(CUtensorMap* map, const void* base, int hkv, int d, long long rows,
-                    int box_rows) {
+                    int box_rows, int elem_bytes) {
   auto enc = tensor_map_encoder();
-  if (!enc) return false;
+  if (!enc || (elem_bytes != 1 && elem_bytes != 2)) return false;
   cuuint64_t dims[2] = {(cuuint64_t)hkv * d, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)hkv * d * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)hkv * d * elem_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  const CUtensorMapDataType dt =
+      elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

@@ -323,8 +323,8 @@ extern "C" pa_status pa_decode(const void* q, const void* k_cache, const void* v
   prm.part_out = part_out;
   prm.part_lse = part_lse;
   prm.out = static_cast<__nv_bfloat16*>(out);
-  prm.src.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
-  prm.src.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  prm.src.k_cache = static_cast<const unsigned char*>(k_cache);
+  prm.src.v_cache = static_cast<const unsigned char*>(v_cache);
   prm.src.num_kv_heads = num_kv_heads;
   prm.src.block_size = block_size;
   prm.src.log2_bs = ilog2(block_size);

@@ -77,14 +77,24 @@ struct BalParams {
   const __nv_bfloat16* k_new;  // [num_seqs, Hkv, D]
   const __nv_bfloat16* v_new;
   const int64_t* slot_mapping;  // [num_seqs]
-  __nv_bfloat16* k_dst;         // the caches, written at the slots
-  __nv_bfloat16* v_dst;
+  unsigned char* k_dst;         // the caches, written at the slots
+  unsigned char* v_dst;
   long long num_slots;
+  // FP8 (e4m3) pools: per-KV-head scales, value = code * scale
+  const float* k_scale;  // [Hkv]
+  const float* v_scale;
 };
 
-template <int D, int NC, int STAGES, bool kMma = true>
+constexpr int kMaxFp8Heads = 64;  // KV heads whose scales an FP8 block keeps in shared memory
+
+// Tokens per K/V tile: e4m3 tiles hold 32 tokens so that a stage carries as
+// many bytes (8 KB at head_dim 128) as a 16-token bf16 tile.
+template <int EB>
+__host__ __device__ constexpr int tile_tokens() { return EB == 1 ? kFp8Tile : kTile; }
+
+template <int D, int NC, int STAGES, bool kMma = true, int EB = 2>
 struct BalSmem {
-  static constexpr int kStageBytes = TileGeom<D>::kStageBytes;
+  static constexpr int kStageBytes = TileGeom<D, EB, tile_tokens<EB>()>::kStageBytes;
   static constexpr int kRingBytes = STAGES * kStageBytes;
   static constexpr int kMergeOff = kRingBytes;                                  // [NC][8][D] fp32
   static constexpr int kQOff = kMergeOff + NC * kMaxGroup * D * 4;             // [2][8][D] bf16
@@ -97,13 +107,15 @@ struct BalSmem {
   // FMA ablation only: fp32 q rows [8][D] and per-warp weights [NC][8][16]
   static constexpr int kQf32Off = kTotOff + (NC + 1) * 4 + 12;
   static constexpr int kWeightsOff = kQf32Off + (kMma ? 0 : kMaxGroup * D * 4);
-  static constexpr int kScanOff = kWeightsOff + (kMma ? 0 : NC * kMaxGroup * kTile * 4);  // S[B+1]
+  static constexpr int kScaleOff = kWeightsOff + (kMma ? 0 : NC * kMaxGroup * kTile * 4);
+  static constexpr int kScanOff = kScaleOff + (EB == 1 ? 2 * kMaxFp8Heads * 4 : 0);  // S[B+1]
   static constexpr int bytes(int B) { return kScanOff + (B + 1) * 4 + 1024; }
 };
 
+template <int TT>
 __device__ __forceinline__ int tiles_of(int ctx, int cap) {
   ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-  return (ctx + kTile - 1) / kTile;
+  return (ctx + TT - 1) / TT;
 }
 
 // Largest worker whose range [w N / W, (w + 1) N / W) starts at or before tile g.
@@ -145,14 +157,24 @@ struct Cursor {
   }
 };
 
-template <int D, bool kTma, int NC, int STAGES, int BPS, bool kMma, bool kAppend>
+// Four e4m3 codes (one u32, low byte first) of four bf16 values / scale.
+__device__ __forceinline__ uint32_t quantize4_e4m3(uint2 v, float scale) {
+  const float f0 = __fdiv_rn(bf16_lo(v.x), scale), f1 = __fdiv_rn(bf16_hi(v.x), scale);
+  const float f2 = __fdiv_rn(bf16_lo(v.y), scale), f3 = __fdiv_rn(bf16_hi(v.y), scale);
+  return f32x2_to_e4m3x2(f0, f1) | (f32x2_to_e4m3x2(f2, f3) << 16);
+}
+
+template <int D, bool kTma, int NC, int STAGES, int BPS, bool kMma, bool kAppend, bool kFp8>
 __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     balanced_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const BalParams p) {
   static_assert(STAGES % NC == 0, "each ring stage must belong to one consumer warp");
   static_assert(BPS <= kMaxBlocksPerSM, "workspace is sized for kMaxBlocksPerSM blocks per SM");
-  using Gm = TileGeom<D>;
-  using L = BalSmem<D, NC, STAGES, kMma>;
+  static_assert(!kFp8 || (D == 128 && kMma), "FP8 tiles: head_dim 128, tensor-core math");
+  constexpr int EB = kFp8 ? 1 : 2;  // bytes per cache element
+  constexpr int TT = tile_tokens<EB>();
+  using Gm = TileGeom<D, EB, TT>;
+  using L = BalSmem<D, NC, STAGES, kMma, EB>;
   constexpr int kThreads = (NC + 1) * 32;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -174,6 +196,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
   int* S = reinterpret_cast<int*>(smem + L::kScanOff);
   float* qs32 = reinterpret_cast<float*>(smem + L::kQf32Off);     // FMA ablation only
   float* weights = reinterpret_cast<float*>(smem + L::kWeightsOff);
+  float* sc_k = reinterpret_cast<float*>(smem + L::kScaleOff);  // FP8 only: [kMaxFp8Heads] x 2
+  float* sc_v = sc_k + kMaxFp8Heads;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -193,6 +217,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     }
     *abort_flag = 0;
   }
+  if constexpr (kFp8) {
+    for (int i = threadIdx.x; i < hkv; i += kThreads) {
+      sc_k[i] = p.k_scale[i];
+      sc_v[i] = p.v_scale[i];
+    }
+  }
 
   // ---- S[b] = tiles of the sequences before b (exclusive prefix sum) -------
   {
@@ -200,7 +230,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     const int seg = (B + kThreads - 1) / kThreads;
     const int lo = min(tid * seg, B), hi = min(lo + seg, B);
     int sum = 0;
-    for (int i = lo; i < hi; ++i) sum += tiles_of(p.context_lens[i], cap);
+    for (int i = lo; i < hi; ++i) sum += tiles_of<TT>(p.context_lens[i], cap);
     int incl = sum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -214,7 +244,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     int run = base + incl - sum;
     for (int i = lo; i < hi; ++i) {
       S[i] = run;
-      run += tiles_of(p.context_lens[i], cap);
+      run += tiles_of<TT>(p.context_lens[i], cap);
     }
     if (tid == kThreads - 1) S[B] = base + incl;
   }
@@ -230,12 +260,23 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     if constexpr (kAppend) {
       const long long slot = p.slot_mapping[b];
       if (slot >= 0 && slot < p.num_slots) {
-        const size_t row = (size_t)hkv * D / 8;  // 16-byte chunks per pool row
-        const uint4* ks = reinterpret_cast<const uint4*>(p.k_new) + (size_t)b * row;
-        const uint4* vs = reinterpret_cast<const uint4*>(p.v_new) + (size_t)b * row;
-        for (size_t i = threadIdx.x; i < row; i += kThreads) {
-          reinterpret_cast<uint4*>(p.k_dst)[slot * row + i] = ks[i];
-          reinterpret_cast<uint4*>(p.v_dst)[slot * row + i] = vs[i];
+        if constexpr (kFp8) {  // quantize 4 values per thread
+          const size_t quads = (size_t)hkv * D / 4;
+          const uint2* ks = reinterpret_cast<const uint2*>(p.k_new) + (size_t)b * quads;
+          const uint2* vs = reinterpret_cast<const uint2*>(p.v_new) + (size_t)b * quads;
+          for (size_t i = threadIdx.x; i < quads; i += kThreads) {
+            const int h = (int)(i / (D / 4));
+            reinterpret_cast<uint32_t*>(p.k_dst)[slot * quads + i] = quantize4_e4m3(ks[i], sc_k[h]);
+            reinterpret_cast<uint32_t*>(p.v_dst)[slot * quads + i] = quantize4_e4m3(vs[i], sc_v[h]);
+          }
+        } else {
+          const size_t row = (size_t)hkv * D / 8;  // 16-byte chunks per pool row
+          const uint4* ks = reinterpret_cast<const uint4*>(p.k_new) + (size_t)b * row;
+          const uint4* vs = reinterpret_cast<const uint4*>(p.v_new) + (size_t)b * row;
+          for (size_t i = threadIdx.x; i < row; i += kThreads) {
+            reinterpret_cast<uint4*>(p.k_dst)[slot * row + i] = ks[i];
+            reinterpret_cast<uint4*>(p.v_dst)[slot * row + i] = vs[i];
+          }
         }
       }
     }
@@ -305,17 +346,17 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
         *abort_flag = 1;
         break;
       }
-      const int t0 = ic.t * kTile;
+      const int t0 = ic.t * TT;
       const int blk_first = t0 >> p.src.log2_bs;
-      const int blk_last = (t0 + kTile - 1) >> p.src.log2_bs;
+      const int blk_last = (t0 + TT - 1) >> p.src.log2_bs;
       if (tc_b != ic.b || blk_first < tc_base || blk_last >= tc_base + 32) {  // warp-uniform
         tc_b = ic.b;
         tc_base = blk_first;
         const int idx = tc_base + lane;
         tc_val = idx < ic_nblk ? p.block_tables[(size_t)ic.b * p.max_blocks + idx] : -1;
       }
-      issue_tile<D, kTma>(ring + stage * Gm::kStageBytes, &full[stage], &tmap_k, &tmap_v, p.src,
-                          ic.kvh, t0, ic_ctx, ic_nblk, tc_base, tc_val, lane);
+      issue_tile<D, kTma, EB, TT>(ring + stage * Gm::kStageBytes, &full[stage], &tmap_k, &tmap_v,
+                                  p.src, ic.kvh, t0, ic_ctx, ic_nblk, tc_base, tc_val, lane);
       ++issued;
       if (++ic.t == ic.n) {
         const int prev_b = ic.b;
@@ -365,10 +406,17 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
         if (4 * lane < D) {
           k_piece = *reinterpret_cast<const uint2*>(s_new + slot * 2 * D + 4 * lane);
           v_piece = *reinterpret_cast<const uint2*>(s_new + slot * 2 * D + D + 4 * lane);
+          if constexpr (kFp8) {  // quantized now: 4 codes in .x, fewer live registers
+            k_piece.x = quantize4_e4m3(k_piece, sc_k[kvh]);
+            v_piece.x = quantize4_e4m3(v_piece, sc_v[kvh]);
+          }
         }
       }
       if constexpr (kMma) {
-        load_q_frags_smem<D>(qf, sq + slot * kMaxGroup * D, G, lane);
+        if constexpr (kFp8)
+          load_q_frags_fp8<D>(qf, sq + slot * kMaxGroup * D, G, lane);
+        else
+          load_q_frags_smem<D>(qf, sq + slot * kMaxGroup * D, G, lane);
       } else {
         const __nv_bfloat16* src = sq + slot * kMaxGroup * D;
         for (int i = tid; i < kMaxGroup * D; i += NC * 32)
@@ -408,24 +456,41 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
       if constexpr (kAppend) {
         if (owns_new && t == uc.n - 1 && new_slot >= 0 && new_slot < p.num_slots) {
           if (4 * lane < D) {
-            const int r = (ctx - 1) & (kTile - 1);  // the new token's row in the tile
-            const int c = lane >> 1;                 // 16-byte chunk of this lane's 8 bytes
-            const uint32_t off = (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4) +
-                                 (lane & 1) * 8;
-            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(sK + off), "r"(k_piece.x),
-                         "r"(k_piece.y)
-                         : "memory");
-            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(sK + Gm::kKVBytes + off),
-                         "r"(v_piece.x), "r"(v_piece.y)
-                         : "memory");
-            const size_t g = ((size_t)new_slot * hkv + kvh) * D + 4 * lane;
-            *reinterpret_cast<uint2*>(p.k_dst + g) = k_piece;
-            *reinterpret_cast<uint2*>(p.v_dst + g) = v_piece;
+            const int r = (ctx - 1) & (TT - 1);  // the new token's row in the tile
+            if constexpr (kFp8) {
+              // this lane's 4 dims quantized to 4 bytes: chunk lane / 4, byte 4 * (lane % 4)
+              const uint32_t kq = k_piece.x, vq = v_piece.x;
+              const int c = lane >> 2;
+              const uint32_t off = (c >> 3) * Gm::kHalfStride + r * 128 +
+                                   (((c & 7) ^ (r & 7)) << 4) + (lane & 3) * 4;
+              asm volatile("st.shared.u32 [%0], %1;" ::"r"(sK + off), "r"(kq) : "memory");
+              asm volatile("st.shared.u32 [%0], %1;" ::"r"(sK + Gm::kKVBytes + off), "r"(vq)
+                           : "memory");
+              const size_t g = ((size_t)new_slot * hkv + kvh) * D + 4 * lane;  // bytes
+              *reinterpret_cast<uint32_t*>(p.k_dst + g) = kq;
+              *reinterpret_cast<uint32_t*>(p.v_dst + g) = vq;
+            } else {
+              const int c = lane >> 1;  // 16-byte chunk of this lane's 8 bytes
+              const uint32_t off = (c >> 3) * Gm::kHalfStride + r * 128 +
+                                   (((c & 7) ^ (r & 7)) << 4) + (lane & 1) * 8;
+              asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(sK + off), "r"(k_piece.x),
+                           "r"(k_piece.y)
+                           : "memory");
+              asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(sK + Gm::kKVBytes + off),
+                           "r"(v_piece.x), "r"(v_piece.y)
+                           : "memory");
+              const size_t g = (((size_t)new_slot * hkv + kvh) * D + 4 * lane) * 2;  // bytes
+              *reinterpret_cast<uint2*>(p.k_dst + g) = k_piece;
+              *reinterpret_cast<uint2*>(p.v_dst + g) = v_piece;
+            }
           }
           __syncwarp();
         }
       }
-      if constexpr (kMma)
+      if constexpr (kFp8)
+        attend_tile_fp8<D>(st, sK, sK + Gm::kKVBytes, qf, min(TT, ctx - t * TT),
+                           p.scale_log2 * sc_k[kvh], lane);
+      else if constexpr (kMma)
         attend_tile<D>(st, sK, sK + Gm::kKVBytes, qf, min(kTile, ctx - t * kTile), p.scale_log2,
                        lane);
       else
@@ -447,11 +512,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
       float* base = merge + (size_t)warp * kMaxGroup * D;
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) {
-        const int d0 = mt * 16 + r0;
-        base[tk * D + merge_col(tk, d0)] = st.o[mt][0];
-        base[(tk + 1) * D + merge_col(tk + 1, d0)] = st.o[mt][1];
-        base[tk * D + merge_col(tk, d0 + 8)] = st.o[mt][2];
-        base[(tk + 1) * D + merge_col(tk + 1, d0 + 8)] = st.o[mt][3];
+        // output dims of this lane's two accumulator rows (FP8 tiles permute them)
+        const int dA = kFp8 ? fp8_out_dim(mt, lane, false) : mt * 16 + r0;
+        const int dB = kFp8 ? fp8_out_dim(mt, lane, true) : mt * 16 + r0 + 8;
+        base[tk * D + merge_col(tk, dA)] = st.o[mt][0];
+        base[(tk + 1) * D + merge_col(tk + 1, dA)] = st.o[mt][1];
+        base[tk * D + merge_col(tk, dB)] = st.o[mt][2];
+        base[(tk + 1) * D + merge_col(tk + 1, dB)] = st.o[mt][3];
       }
     } else {
 #pragma unroll
@@ -497,17 +564,19 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
         acc[0] += wt * u.x; acc[1] += wt * u.y; acc[2] += wt * u.z; acc[3] += wt * u.w;
         acc[4] += wt * v.x; acc[5] += wt * v.y; acc[6] += wt * v.z; acc[7] += wt * v.w;
       }
+      // divisor of the output values: the running sum (and, FP8, over v_scale)
+      const float Ld = kFp8 ? Lsum / sc_v[kvh] : Lsum;
       if (!cut) {
         uint4 pk;
-        pk.x = pack_bf16x2(acc[0] / Lsum, acc[1] / Lsum);
-        pk.y = pack_bf16x2(acc[2] / Lsum, acc[3] / Lsum);
-        pk.z = pack_bf16x2(acc[4] / Lsum, acc[5] / Lsum);
-        pk.w = pack_bf16x2(acc[6] / Lsum, acc[7] / Lsum);
+        pk.x = pack_bf16x2(acc[0] / Ld, acc[1] / Ld);
+        pk.y = pack_bf16x2(acc[2] / Ld, acc[3] / Ld);
+        pk.z = pack_bf16x2(acc[4] / Ld, acc[5] / Ld);
+        pk.w = pack_bf16x2(acc[6] / Ld, acc[7] / Ld);
         *reinterpret_cast<uint4*>(orow + (size_t)g * D + c8 * 8) = pk;
       } else {
         float4* dst = reinterpret_cast<float4*>(p.rec_o + ((size_t)rec * kMaxGroup + g) * D + c8 * 8);
-        dst[0] = make_float4(acc[0] / Lsum, acc[1] / Lsum, acc[2] / Lsum, acc[3] / Lsum);
-        dst[1] = make_float4(acc[4] / Lsum, acc[5] / Lsum, acc[6] / Lsum, acc[7] / Lsum);
+        dst[0] = make_float4(acc[0] / Ld, acc[1] / Ld, acc[2] / Ld, acc[3] / Ld);
+        dst[1] = make_float4(acc[4] / Ld, acc[5] / Ld, acc[6] / Ld, acc[7] / Ld);
         if (c8 == 0) p.rec_lse[rec * kMaxGroup + g] = M + log2f(Lsum);
       }
     }
@@ -575,11 +644,12 @@ WsLayout ws_layout(int num_seqs, int num_kv_heads, int head_dim, int blocks) {
   return l;
 }
 
-template <int D, bool kTma, int NC, int STAGES, int BPS, bool kMma, bool kAppend>
+template <int D, bool kTma, int NC, int STAGES, int BPS, bool kMma, bool kAppend,
+          bool kFp8 = false>
 pa_status launch_shape(const CUtensorMap& mk, const CUtensorMap& mv, const BalParams& prm, int sms,
                        cudaStream_t stream) {
-  auto kern = balanced_decode_kernel<D, kTma, NC, STAGES, BPS, kMma, kAppend>;
-  const int smem = BalSmem<D, NC, STAGES, kMma>::bytes(prm.num_seqs);
+  auto kern = balanced_decode_kernel<D, kTma, NC, STAGES, BPS, kMma, kAppend, kFp8>;
+  const int smem = BalSmem<D, NC, STAGES, kMma, kFp8 ? 1 : 2>::bytes(prm.num_seqs);
   if (smem > 227 * 1024) return PA_ERR_UNSUPPORTED;
   int per_sm = 0;
   const pa_status s = prepare_kernel(reinterpret_cast<const void*>(kern), (NC + 1) * 32, smem,
@@ -603,6 +673,17 @@ bool fma_ablation() {
 template <int D, bool kTma>
 pa_status launch_balanced(const CUtensorMap& mk, const CUtensorMap& mv, const BalParams& prm,
                           int sms, cudaStream_t stream) {
+  if (prm.k_scale) {
+    if constexpr (D == 128) {
+      if (prm.slot_mapping)
+        return launch_shape<D, kTma, kConsumers, kStages, kBlocksPerSM, true, true, true>(
+            mk, mv, prm, sms, stream);
+      return launch_shape<D, kTma, kConsumers, kStages, kBlocksPerSM, true, false, true>(
+          mk, mv, prm, sms, stream);
+    } else {
+      return PA_ERR_UNSUPPORTED;
+    }
+  }
   if (prm.slot_mapping)
     return launch_shape<D, kTma, kConsumers, kStages, kBlocksPerSM, true, true>(mk, mv, prm, sms,
                                                                               stream);
@@ -666,7 +747,8 @@ pa_status balanced_entry(const void* q, const void* k_new, const void* v_new,
                          const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                          int32_t num_blocks, float scale, void* workspace, size_t workspace_bytes,
-                         void* out, void* stream) {
+                         void* out, void* stream, const float* k_scale = nullptr,
+                         const float* v_scale = nullptr) {
   if (num_seqs == 0) return PA_OK;
   pa_status s = check_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                   context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
@@ -675,6 +757,11 @@ pa_status balanced_entry(const void* q, const void* k_new, const void* v_new,
   const bool fused = k_new != nullptr;
   if (fused && (!v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new)))
     return PA_ERR_INVALID_ARG;
+  const bool fp8 = k_scale != nullptr;
+  if (fp8) {
+    if (!v_scale) return PA_ERR_INVALID_ARG;
+    if (head_dim != 128 || num_kv_heads > kMaxFp8Heads) return PA_ERR_UNSUPPORTED;
+  }
   const int sms = sm_count();
   if (sms <= 0) return PA_ERR_CUDA;
   const WsLayout lay = ws_layout(num_seqs, num_kv_heads, head_dim, sms * kMaxBlocksPerSM);
@@ -696,8 +783,8 @@ pa_status balanced_entry(const void* q, const void* k_new, const void* v_new,
   prm.counters = reinterpret_cast<int*>(ws + lay.counters);
   prm.rec_lse = reinterpret_cast<float*>(ws + lay.rec_lse);
   prm.rec_o = reinterpret_cast<float*>(ws + lay.rec_o);
-  prm.src.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
-  prm.src.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  prm.src.k_cache = static_cast<const unsigned char*>(k_cache);
+  prm.src.v_cache = static_cast<const unsigned char*>(v_cache);
   prm.src.num_kv_heads = num_kv_heads;
   prm.src.block_size = block_size;
   prm.src.log2_bs = ilog2(block_size);
@@ -710,9 +797,11 @@ pa_status balanced_entry(const void* q, const void* k_new, const void* v_new,
   prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
   prm.v_new = static_cast<const __nv_bfloat16*>(v_new);
   prm.slot_mapping = fused ? slot_mapping : nullptr;
-  prm.k_dst = static_cast<__nv_bfloat16*>(k_cache);
-  prm.v_dst = static_cast<__nv_bfloat16*>(v_cache);
+  prm.k_dst = static_cast<unsigned char*>(k_cache);
+  prm.v_dst = static_cast<unsigned char*>(v_cache);
   prm.num_slots = (long long)num_blocks * block_size;
+  prm.k_scale = k_scale;
+  prm.v_scale = v_scale;
 
   CUtensorMap mk, mv;
   std::memset(&mk, 0, sizeof(mk));
@@ -720,9 +809,11 @@ pa_status balanced_entry(const void* q, const void* k_new, const void* v_new,
   const bool tma = block_size >= 8;
   if (tma) {
     const long long rows = (long long)num_blocks * block_size;
-    const int box_rows = block_size < kTile ? block_size : kTile;
-    if (!make_cache_map(&mk, k_cache, num_kv_heads, head_dim, rows, box_rows) ||
-        !make_cache_map(&mv, v_cache, num_kv_heads, head_dim, rows, box_rows))
+    const int tt = fp8 ? tile_tokens<1>() : tile_tokens<2>();  // tokens per tile
+    const int box_rows = block_size < tt ? block_size : tt;
+    const int eb = fp8 ? 1 : 2;
+    if (!make_cache_map(&mk, k_cache, num_kv_heads, head_dim, rows, box_rows, eb) ||
+        !make_cache_map(&mv, v_cache, num_kv_heads, head_dim, rows, box_rows, eb))
       return PA_ERR_CUDA;
   }
   if (head_dim == 128)
@@ -761,6 +852,42 @@ extern "C" pa_status pa_append_decode(const void* q, const void* k_new, const vo
                             max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
                             head_dim, block_size, num_blocks, scale, workspace, workspace_bytes,
                             out, stream);
+}
+
+extern "C" pa_status pa_decode_balanced_fp8(const void* q, const void* k_cache,
+                                            const void* v_cache, const float* k_scale,
+                                            const float* v_scale, const int32_t* block_tables,
+                                            int32_t max_blocks_per_seq,
+                                            const int32_t* context_lens, int32_t num_seqs,
+                                            int32_t num_q_heads, int32_t num_kv_heads,
+                                            int32_t head_dim, int32_t block_size,
+                                            int32_t num_blocks, float scale, void* workspace,
+                                            size_t workspace_bytes, void* out, void* stream) {
+  if (num_seqs == 0) return PA_OK;
+  if (!k_scale || !v_scale) return PA_ERR_INVALID_ARG;
+  return pa::balanced_entry(q, nullptr, nullptr, nullptr, const_cast<void*>(k_cache),
+                            const_cast<void*>(v_cache), block_tables, max_blocks_per_seq,
+                            context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                            block_size, num_blocks, scale, workspace, workspace_bytes, out, stream,
+                            k_scale, v_scale);
+}
+
+extern "C" pa_status pa_append_decode_fp8(const void* q, const void* k_new, const void* v_new,
+                                          const int64_t* slot_mapping, void* k_cache,
+                                          void* v_cache, const float* k_scale,
+                                          const float* v_scale, const int32_t* block_tables,
+                                          int32_t max_blocks_per_seq,
+                                          const int32_t* context_lens, int32_t num_seqs,
+                                          int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t block_size,
+                                          int32_t num_blocks, float scale, void* workspace,
+                                          size_t workspace_bytes, void* out, void* stream) {
+  if (num_seqs == 0) return PA_OK;
+  if (!k_new || !k_scale || !v_scale) return PA_ERR_INVALID_ARG;
+  return pa::balanced_entry(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                            max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                            head_dim, block_size, num_blocks, scale, workspace, workspace_bytes,
+                            out, stream, k_scale, v_scale);
 }
 
 extern "C" pa_status pa_decode_balanced_static(const void* q, const void* k_cache,

@@ -28,10 +28,11 @@ bool validating();
 pa_status launch_status();
 
 // 2-D tensor map over a cache viewed as [rows = num_blocks*block_size,
-// cols = num_kv_heads*head_dim] bf16, box {64 columns, box_rows rows},
-// 128-byte swizzle, zero fill out of bounds.
+// cols = num_kv_heads*head_dim] elements of elem_bytes (2: bf16, 1: e4m3
+// bytes), box {128 bytes of columns, box_rows rows}, 128-byte swizzle, zero
+// fill out of bounds.
 bool make_cache_map(CUtensorMap* map, const void* base, int num_kv_heads, int head_dim,
-                    long long rows, int box_rows);
+                    long long rows, int box_rows, int elem_bytes = 2);
 
 // Validating mode: copies context_lens / block_tables to the host (stream
 // synchronised) and range-checks them. split_tokens > 0 also bounds contexts

@@ -1,6 +1,7 @@
-// pa_tile.cuh -- the 16-token K/V tile shared by both decode kernels: how a
-// tile is fetched into shared memory and how one warp folds it into its
-// running attention state for the GQA group of one KV head.
+// pa_tile.cuh -- the K/V tile shared by both decode kernels (16 tokens of
+// bf16, 32 tokens of e4m3): how a tile is fetched into shared memory and how
+// one warp folds it into its running attention state for the GQA group of one
+// KV head.
 //
 // The tile math is the streaming softmax of "Text Generation Inference:
 // Hugging Face's production-grade LLM inference server" (section "Under the
@@ -28,11 +29,18 @@ constexpr int kTile = 16;                // tokens per tile (the m of S^T)
 constexpr int kMaxGroup = 8;             // query heads per KV head (the n of the MMA)
 constexpr int kHalfBytes = kTile * 128;  // one 64-column half of a tile
 
-template <int D>
+// EB: bytes per cache element (2 = bf16, 1 = e4m3); TT: tokens per tile (16
+// for bf16, 32 for e4m3, so both stages hold 8 KB). A tile row is D * EB
+// bytes, stored as D * EB / 128 column "halves" of TT rows x 128 bytes.
+template <int D, int EB = 2, int TT = kTile>
 struct TileGeom {
-  static constexpr int kHalves = D / 64;
-  static constexpr int kKVBytes = kHalves * kHalfBytes;  // one K (or V) tile
-  static constexpr int kStageBytes = 2 * kKVBytes;       // K then V
+  static constexpr int kRowBytes = D * EB;
+  static constexpr int kHalves = kRowBytes / 128;
+  static_assert(kHalves >= 1 && kRowBytes % 128 == 0, "tile rows must be multiples of 128 bytes");
+  static constexpr int kBoxCols = 128 / EB;               // TMA box width in elements
+  static constexpr int kHalfStride = TT * 128;            // bytes of one column half
+  static constexpr int kKVBytes = kHalves * kHalfStride;  // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kKVBytes;        // K then V
 };
 
 // Running state of one warp for the GQA group of one KV head.
@@ -164,6 +172,151 @@ __device__ __forceinline__ void attend_tile(AttnState<D>& st, uint32_t sK, uint3
     a[2] &= vm23;
     a[3] &= vm23;
     mma_bf16_16816(st.o[mt], a, pb0, pb1);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// FP8 (e4m3) tiles: a tile row is D bytes, 32 rows per tile. K and V bytes are read with
+// ldmatrix, byte pairs standing in for b16 elements, and widened exactly to f16
+// (cvt.rn.f16x2.e4m3x2) for an f16 MMA. Within a 16-dim chunk, lane l's A
+// registers then hold dims 4c..4c+3 (c = l % 4) where the bf16 layout has
+// dims 2c, 2c+1, 2c+8, 2c+9; Q takes the same k order (load_q_frags_fp8), which
+// the dot product does not see. V comes through ldmatrix.trans: rows 0-7 of a
+// 16-dim output tile hold the even dims of the chunk and rows 8-15 the odd
+// ones (fp8_out_dim). The per-head scales are applied outside: the score
+// factor includes k_scale, the output is multiplied by v_scale.
+
+// Output dim of accumulator element (mt, upper rows?) of this lane.
+__device__ __forceinline__ int fp8_out_dim(int mt, int lane, bool upper) {
+  return mt * 16 + 2 * (lane >> 2) + (upper ? 1 : 0);
+}
+
+// Q^T B fragments (f16) in the fp8 tile's k order, from the group's bf16 q
+// rows in shared memory; heads >= G are zero.
+template <int D>
+__device__ __forceinline__ void load_q_frags_fp8(uint32_t (&qf)[D / 16][2],
+                                                 const __nv_bfloat16* sq, int G, int lane) {
+  const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) qf[ks][0] = qf[ks][1] = 0u;
+  if (g < G) {
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint2 v = *reinterpret_cast<const uint2*>(sq + g * D + ks * 16 + 4 * c);
+      qf[ks][0] = pack_f16x2(bf16_lo(v.x), bf16_hi(v.x));
+      qf[ks][1] = pack_f16x2(bf16_lo(v.y), bf16_hi(v.y));
+    }
+  }
+}
+
+// attend_tile for a 32-token e4m3 tile (head_dim 128: one 128-byte row per
+// token, kFp8Tile rows per K or V half); score_scale_log2 = scale * k_scale *
+// log2(e). Tokens 0-15 and 16-31 form two independent MMA chains; one
+// softmax update covers all 32.
+constexpr int kFp8Tile = 32;
+
+// A operand (16 tokens x 16 k) of one e4m3 K ldmatrix result: k[i] holds 4
+// codes (dims 4c..4c+3 of the k step) of token r0 (i even) or r0 + 8 (i odd).
+__device__ __forceinline__ void fp8_k_operand(const uint32_t (&k)[4], int i0, uint32_t (&a)[4]) {
+  a[0] = e4m3x2_to_f16x2(k[i0] & 0xFFFFu);
+  a[1] = e4m3x2_to_f16x2(k[i0 + 1] & 0xFFFFu);
+  a[2] = e4m3x2_to_f16x2(k[i0] >> 16);
+  a[3] = e4m3x2_to_f16x2(k[i0 + 1] >> 16);
+}
+
+template <int D>
+__device__ __forceinline__ void attend_tile_fp8(AttnState<D>& st, uint32_t sK, uint32_t sV,
+                                                const uint32_t (&qf)[D / 16][2], int valid,
+                                                float score_scale_log2, int lane) {
+  static_assert(D == 128, "e4m3 tiles are one 128-byte row per token");
+  const int r = lane & 15;     // the row whose address this lane gives ldmatrix
+  const int cadd = lane >> 4;  // chunk 2s (lanes 0-15) or 2s + 1 (lanes 16-31)
+  float sa[4] = {0.f, 0.f, 0.f, 0.f};  // tokens 0-15
+  float sb[4] = {0.f, 0.f, 0.f, 0.f};  // tokens 16-31
+#pragma unroll
+  for (int sidx = 0; sidx < D / 32; ++sidx) {
+    const uint32_t sw = (uint32_t)(((2 * sidx + cadd) ^ (r & 7)) << 4);
+    uint32_t ka[4], kb[4], a[4];
+    ldsm_x4(sK + r * 128 + sw, ka);
+    ldsm_x4(sK + (r + 16) * 128 + sw, kb);
+    fp8_k_operand(ka, 0, a);
+    mma_f16_16816(sa, a, qf[2 * sidx][0], qf[2 * sidx][1]);
+    fp8_k_operand(kb, 0, a);
+    mma_f16_16816(sb, a, qf[2 * sidx][0], qf[2 * sidx][1]);
+    fp8_k_operand(ka, 2, a);
+    mma_f16_16816(sa, a, qf[2 * sidx + 1][0], qf[2 * sidx + 1][1]);
+    fp8_k_operand(kb, 2, a);
+    mma_f16_16816(sb, a, qf[2 * sidx + 1][0], qf[2 * sidx + 1][1]);
+  }
+  const int r0 = lane >> 2;
+  const int tk = 2 * (lane & 3);
+  float y[8];  // tokens r0, r0 + 8, r0 + 16, r0 + 24 x heads tk, tk + 1
+  y[0] = r0 < valid ? sa[0] * score_scale_log2 : -INFINITY;
+  y[1] = r0 < valid ? sa[1] * score_scale_log2 : -INFINITY;
+  y[2] = r0 + 8 < valid ? sa[2] * score_scale_log2 : -INFINITY;
+  y[3] = r0 + 8 < valid ? sa[3] * score_scale_log2 : -INFINITY;
+  y[4] = r0 + 16 < valid ? sb[0] * score_scale_log2 : -INFINITY;
+  y[5] = r0 + 16 < valid ? sb[1] * score_scale_log2 : -INFINITY;
+  y[6] = r0 + 24 < valid ? sb[2] * score_scale_log2 : -INFINITY;
+  y[7] = r0 + 24 < valid ? sb[3] * score_scale_log2 : -INFINITY;
+  float mx0 = fmaxf(fmaxf(y[0], y[2]), fmaxf(y[4], y[6]));
+  float mx1 = fmaxf(fmaxf(y[1], y[3]), fmaxf(y[5], y[7]));
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+  }
+  const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
+  const float a0 = exp2f(st.m0 - mn0), a1 = exp2f(st.m1 - mn1);
+  uint32_t pw[4];  // f16 weights of tokens r0 + 8i, heads tk | tk + 1
+#pragma unroll
+  for (int i = 0; i < 4; ++i) pw[i] = pack_f16x2(exp2f(y[2 * i] - mn0), exp2f(y[2 * i + 1] - mn1));
+  st.l0 = st.l0 * a0 + ((f16_lo(pw[0]) + f16_lo(pw[1])) + (f16_lo(pw[2]) + f16_lo(pw[3])));
+  st.l1 = st.l1 * a1 + ((f16_hi(pw[0]) + f16_hi(pw[1])) + (f16_hi(pw[2]) + f16_hi(pw[3])));
+  st.m0 = mn0;
+  st.m1 = mn1;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    st.o[mt][0] *= a0;
+    st.o[mt][1] *= a1;
+    st.o[mt][2] *= a0;
+    st.o[mt][3] *= a1;
+  }
+  uint32_t pb[4];  // B fragments of P^T: tokens 0-7, 8-15, 16-23, 24-31
+#pragma unroll
+  for (int i = 0; i < 4; ++i) pb[i] = movmatrix_trans(pw[i]);
+  // the V rows this lane's A fragments hold: tokens tk + 8i and tk + 8i + 1
+  uint32_t vm[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+  if (valid < kFp8Tile) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      vm[i] = (tk + 8 * i < valid ? 0x0000ffffu : 0u) | (tk + 8 * i + 1 < valid ? 0xffff0000u : 0u);
+  }
+#pragma unroll
+  for (int sidx = 0; sidx < D / 32; ++sidx) {
+    const uint32_t sw = (uint32_t)(((2 * sidx + cadd) ^ (r & 7)) << 4);
+    uint32_t va[4], vb[4];
+    ldsm_x4_trans(sV + r * 128 + sw, va);
+    ldsm_x4_trans(sV + (r + 16) * 128 + sw, vb);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      // bytes: (token 2c: dim 2j, 2j+1), (token 2c+1: dim 2j, 2j+1) -> even | odd pairs
+      uint32_t e0 = byte_perm(va[2 * half], 0u, 0x3120u);      // tokens 0-7
+      uint32_t e1 = byte_perm(va[2 * half + 1], 0u, 0x3120u);  // tokens 8-15
+      uint32_t a[4];
+      a[0] = e4m3x2_to_f16x2(e0 & 0xFFFFu) & vm[0];
+      a[1] = e4m3x2_to_f16x2(e0 >> 16) & vm[0];
+      a[2] = e4m3x2_to_f16x2(e1 & 0xFFFFu) & vm[1];
+      a[3] = e4m3x2_to_f16x2(e1 >> 16) & vm[1];
+      mma_f16_16816(st.o[2 * sidx + half], a, pb[0], pb[1]);
+      e0 = byte_perm(vb[2 * half], 0u, 0x3120u);      // tokens 16-23
+      e1 = byte_perm(vb[2 * half + 1], 0u, 0x3120u);  // tokens 24-31
+      a[0] = e4m3x2_to_f16x2(e0 & 0xFFFFu) & vm[2];
+      a[1] = e4m3x2_to_f16x2(e0 >> 16) & vm[2];
+      a[2] = e4m3x2_to_f16x2(e1 & 0xFFFFu) & vm[3];
+      a[3] = e4m3x2_to_f16x2(e1 >> 16) & vm[3];
+      mma_f16_16816(st.o[2 * sidx + half], a, pb[2], pb[3]);
+    }
   }
 }
 
@@ -302,8 +455,8 @@ __device__ __forceinline__ void attend_tile_fma(AttnStateFma<D>& st, uint32_t sK
 
 // Where a tile's K/V rows come from.
 struct TileSrc {
-  const __nv_bfloat16* k_cache;  // for the cp.async gather (block sizes < 8)
-  const __nv_bfloat16* v_cache;
+  const unsigned char* k_cache;  // for the cp.async gather (block sizes < 8)
+  const unsigned char* v_cache;
   int num_kv_heads;
   int block_size;
   int log2_bs;
@@ -320,59 +473,67 @@ struct TileSrc {
 // from a coordinate past the pool, which TMA fills with zeros. Gather path:
 // every lane copies 16-byte chunks; tokens >= t_end and invalid blocks are
 // zero-filled without a read.
-template <int D, bool kTma>
+template <int D, bool kTma, int EB = 2, int TT = kTile>
 __device__ __forceinline__ void issue_tile(uint32_t sK, uint64_t* full, const CUtensorMap* tmap_k,
                                            const CUtensorMap* tmap_v, const TileSrc& src, int kvh,
                                            int t0, int t_end, int n_seq_blocks, int tc_base,
                                            int tc_val, int lane) {
-  using Gm = TileGeom<D>;
+  using Gm = TileGeom<D, EB, TT>;
   const int bs = src.block_size;
   const int blk_first = t0 >> src.log2_bs;
   const uint32_t sV = sK + Gm::kKVBytes;
   if constexpr (kTma) {
-    const int box_rows = bs < kTile ? bs : kTile;
+    // boxes of min(bs, TT) rows: TT / box_rows blocks per tile (bs >= 8)
+    constexpr int kMaxSub = TT / 8;
+    const int box_rows = bs < TT ? bs : TT;
+    const int nsub = TT / box_rows;
     const int oob_row = src.num_blocks * bs;  // < 2^31 (checked on the host)
-    const int phys0 = __shfl_sync(0xffffffffu, tc_val, (blk_first - tc_base) & 31);
-    const int phys1 = __shfl_sync(0xffffffffu, tc_val, (blk_first + 1 - tc_base) & 31);
-    const bool ok0 = blk_first < n_seq_blocks && phys0 >= 0 && phys0 < src.num_blocks;
-    const bool ok1 = blk_first + 1 < n_seq_blocks && phys1 >= 0 && phys1 < src.num_blocks;
-    const int row0 = ok0 ? (int)((unsigned)phys0 * (unsigned)bs +
-                                 (bs > kTile ? (unsigned)(t0 & (bs - 1)) : 0u))
-                         : oob_row;
-    const int row1 = ok1 ? (int)((unsigned)phys1 * (unsigned)bs) : oob_row;
+    int rows[kMaxSub];
+#pragma unroll
+    for (int j = 0; j < kMaxSub; ++j) {
+      const int phys = __shfl_sync(0xffffffffu, tc_val, (blk_first + j - tc_base) & 31);
+      const bool ok = j < nsub && blk_first + j < n_seq_blocks && phys >= 0 &&
+                      phys < src.num_blocks;
+      rows[j] = ok ? (int)((unsigned)phys * (unsigned)bs +
+                           (j == 0 && bs > TT ? (unsigned)(t0 & (bs - 1)) : 0u))
+                   : oob_row;
+    }
     if (lane == 0) {
       mbar_arrive_expect_tx(full, Gm::kStageBytes);
 #pragma unroll
       for (int h = 0; h < Gm::kHalves; ++h) {
-        const int x = kvh * D + h * 64;
-        const uint32_t off = h * kHalfBytes;
-        tma_load_2d(sK + off, tmap_k, x, row0, full);
-        tma_load_2d(sV + off, tmap_v, x, row0, full);
-        if (box_rows < kTile) {  // block_size 8: the tile's second block
-          tma_load_2d(sK + off + box_rows * 128, tmap_k, x, row1, full);
-          tma_load_2d(sV + off + box_rows * 128, tmap_v, x, row1, full);
+        const int x = kvh * D + h * Gm::kBoxCols;
+        const uint32_t off = h * Gm::kHalfStride;
+#pragma unroll
+        for (int j = 0; j < kMaxSub; ++j) {
+          if (j < nsub) {
+            tma_load_2d(sK + off + j * box_rows * 128, tmap_k, x, rows[j], full);
+            tma_load_2d(sV + off + j * box_rows * 128, tmap_v, x, rows[j], full);
+          }
         }
       }
     }
   } else {
-    constexpr int kChunks = D / 8;  // 16-byte chunks per row
-    const size_t row_elems = (size_t)src.num_kv_heads * D;
+    constexpr int kChunks = Gm::kRowBytes / 16;  // 16-byte chunks per row
+    const size_t row_bytes = (size_t)src.num_kv_heads * Gm::kRowBytes;
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
-      const __nv_bfloat16* cache = which == 0 ? src.k_cache : src.v_cache;
+      const unsigned char* cache = which == 0 ? src.k_cache : src.v_cache;
       const uint32_t dst_tile = which == 0 ? sK : sV;
 #pragma unroll
-      for (int k = 0; k < kTile * kChunks / 32; ++k) {
+      for (int k = 0; k < TT * kChunks / 32; ++k) {
         const int idx = k * 32 + lane;
         const int r = idx / kChunks, c = idx % kChunks;
         const int t = t0 + r;
         const int blk = t >> src.log2_bs;
         const int phys = __shfl_sync(0xffffffffu, tc_val, (blk - tc_base) & 31);
         const bool ok = t < t_end && blk < n_seq_blocks && phys >= 0 && phys < src.num_blocks;
-        const __nv_bfloat16* p =
-            ok ? cache + ((size_t)phys * bs + (t & (bs - 1))) * row_elems + (size_t)kvh * D + c * 8
+        const unsigned char* p =
+            ok ? cache + ((size_t)phys * bs + (t & (bs - 1))) * row_bytes +
+                     (size_t)kvh * Gm::kRowBytes + c * 16
                : cache;
-        const uint32_t dst = dst_tile + (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+        const uint32_t dst =
+            dst_tile + (c >> 3) * Gm::kHalfStride + r * 128 + (((c & 7) ^ (r & 7)) << 4);
         cp_async_16_zfill(dst, p, ok);
       }
     }
