@@ -9,6 +9,9 @@ bfloat16 data as raw ``uint16`` bit patterns in NumPy arrays, widens them to
 float64 and computes every result in float64 from the plain definitions the
 source pages give. Each function names the page and section it follows.
 
+``prefix_cache`` models the block pool with a prefix cache and copy-on-write
+(pinned by ``tests/test_oracle_prefix.py``).
+
 Every function here is pinned by ``tests/test_oracle_pins.py`` against facts
 the pages or mathematics fix (printed table values, closed forms, invariances,
 an independent library routine and brute force); none is "parity unpinned".
@@ -33,3 +36,4 @@ from .paged_attention import (  # noqa: F401
     dequantize_pool,
     decode_fp8,
 )
+from .prefix_cache import PrefixCacheModel, CapacityError, copy_blocks  # noqa: F401
