@@ -42,7 +42,9 @@ Readings where the pages leave a step open (each one is a rule below):
 * Fresh blocks are taken lowest id first.
 * A write into a block that is cached or referenced by another sequence is a
   copy-on-write of the whole block.
-* Capacity failure leaves the state as it was.
+* A call that needs more fresh blocks than the free blocks plus the blocks
+  eviction could free at its start (cached, unreferenced, nothing referenced
+  cached below them) fails before changing anything.
 
 Written as plain data structures and loops, favouring obviousness over speed.
 """
@@ -95,6 +97,21 @@ class PrefixCacheModel:
         self.free.add(b)
         return b
 
+    def _evictable(self) -> int:
+        count = 0
+        for key, b in self.cache.items():
+            if self.ref[b] != 0:
+                continue
+            below = [b2 for k2, b2 in self.cache.items()
+                     if len(k2) > len(key) and k2[:len(key)] == key]
+            if all(self.ref[b2] == 0 for b2 in below):
+                count += 1
+        return count
+
+    def _reserve(self, needed: int):
+        if needed > len(self.free) + self._evictable():
+            raise CapacityError("pool exhausted")
+
     def _take(self) -> int:
         if not self.free:
             self._evict_one()
@@ -106,14 +123,6 @@ class PrefixCacheModel:
         self.ref[b] -= 1
         if self.ref[b] == 0 and b not in self.key_of:
             self.free.add(b)
-
-    def _snapshot(self):
-        return (set(self.free), list(self.ref), dict(self.cache), dict(self.key_of),
-                dict(self.last_use), {k: {"blocks": list(v["blocks"]), "ntok": v["ntok"]}
-                                      for k, v in self.seqs.items()})
-
-    def _restore(self, snap):
-        (self.free, self.ref, self.cache, self.key_of, self.last_use, self.seqs) = snap
 
     # ------------------------------------------------------------- the API
     def admit(self, tokens):
@@ -127,25 +136,27 @@ class PrefixCacheModel:
             raise ValueError("empty prompt")
         self.tick += 1
         bs = self.block_size
-        snap = self._snapshot()
         matched = []
         while (len(matched) + 1) * bs <= n:
             key = tokens[:(len(matched) + 1) * bs]
             if key not in self.cache:
                 break
             matched.append(self.cache[key])
-        for i, b in enumerate(matched):          # references first: no eviction can take them
+        for b in matched:                        # references first: no eviction can take them
             self.ref[b] += 1
+        try:
+            self._reserve(-(-n // bs) - len(matched))
+        except CapacityError:
+            for b in matched:
+                self.ref[b] -= 1
+            raise
+        for i in range(len(matched)):
             self.last_use[tokens[:(i + 1) * bs]] = self.tick
         blocks = list(matched)
-        try:
-            while len(blocks) * bs < n:
-                b = self._take()
-                self.ref[b] += 1
-                blocks.append(b)
-        except CapacityError:
-            self._restore(snap)
-            raise
+        while len(blocks) * bs < n:
+            b = self._take()
+            self.ref[b] += 1
+            blocks.append(b)
         cached = len(matched) * bs
         if cached == n:
             cached = n - 1                        # one position is always computed
@@ -163,27 +174,31 @@ class PrefixCacheModel:
         if not 0 <= p0 <= seq["ntok"] or p1 < p0:
             raise ValueError("positions must continue the sequence")
         bs = self.block_size
-        snap = self._snapshot()
+        needed = 0
+        for i in range(p0 // bs, (p1 - 1) // bs + 1 if p1 > p0 else p0 // bs):
+            if i >= len(seq["blocks"]):
+                needed += 1
+            else:
+                b = seq["blocks"][i]
+                if self.ref[b] > 1 or b in self.key_of:
+                    needed += 1
+        self._reserve(needed)
         slots, copies = [], []
-        try:
-            for p in range(p0, p1):
-                i = p // bs
-                if i == len(seq["blocks"]):
-                    b = self._take()
-                    self.ref[b] += 1
-                    seq["blocks"].append(b)
-                else:
-                    old = seq["blocks"][i]
-                    if self.ref[old] > 1 or old in self.key_of:
-                        new = self._take()
-                        self.ref[new] += 1
-                        copies.append((old, new))
-                        seq["blocks"][i] = new
-                        self._drop_ref(old)
-                slots.append(seq["blocks"][i] * bs + p % bs)
-        except CapacityError:
-            self._restore(snap)
-            raise
+        for p in range(p0, p1):
+            i = p // bs
+            if i == len(seq["blocks"]):
+                b = self._take()
+                self.ref[b] += 1
+                seq["blocks"].append(b)
+            else:
+                old = seq["blocks"][i]
+                if self.ref[old] > 1 or old in self.key_of:
+                    new = self._take()
+                    self.ref[new] += 1
+                    copies.append((old, new))
+                    seq["blocks"][i] = new
+                    self._drop_ref(old)
+            slots.append(seq["blocks"][i] * bs + p % bs)
         seq["ntok"] = max(seq["ntok"], p1)
         return slots, copies
 
