@@ -169,10 +169,10 @@ class PrefixCacheModel:
         """Slots for writing positions [p0, p1) of a sequence, growing it as
         needed. A write into a block that is cached or shared first copies the
         block. Returns (slots, copies) with copies a list of (src, dst)."""
-        self.tick += 1
         seq = self.seqs[sid]
         if not 0 <= p0 <= seq["ntok"] or p1 < p0:
             raise ValueError("positions must continue the sequence")
+        self.tick += 1
         bs = self.block_size
         needed = 0
         for i in range(p0 // bs, (p1 - 1) // bs + 1 if p1 > p0 else p0 // bs):
@@ -204,8 +204,8 @@ class PrefixCacheModel:
 
     def fork(self, sid: int) -> int:
         """A new sequence sharing every block of `sid` (parallel sampling)."""
-        self.tick += 1
         seq = self.seqs[sid]
+        self.tick += 1
         for b in seq["blocks"]:
             self.ref[b] += 1
         child = self.next_seq
@@ -217,8 +217,8 @@ class PrefixCacheModel:
         """The sequence ends with K/V computed for `tokens` (positions
         [0, len(tokens))). Its full blocks enter the cache unless their prefix
         is cached already; then every reference it holds is dropped."""
-        self.tick += 1
         seq = self.seqs.pop(sid)
+        self.tick += 1
         tokens = tuple(int(t) for t in tokens)
         bs = self.block_size
         nfull = min(len(tokens), seq["ntok"]) // bs
