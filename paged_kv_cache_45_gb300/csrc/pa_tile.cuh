@@ -483,32 +483,58 @@ __device__ __forceinline__ void issue_tile(uint32_t sK, uint64_t* full, const CU
   const int blk_first = t0 >> src.log2_bs;
   const uint32_t sV = sK + Gm::kKVBytes;
   if constexpr (kTma) {
-    // boxes of min(bs, TT) rows: TT / box_rows blocks per tile (bs >= 8)
-    constexpr int kMaxSub = TT / 8;
-    const int box_rows = bs < TT ? bs : TT;
-    const int nsub = TT / box_rows;
+    // Boxes of min(bs, TT) rows. The loader issues every tile of the block,
+    // so this stays straight-line for the common shapes: one box per column
+    // half when a block holds the whole tile, two when it holds half of it.
     const int oob_row = src.num_blocks * bs;  // < 2^31 (checked on the host)
-    int rows[kMaxSub];
-#pragma unroll
-    for (int j = 0; j < kMaxSub; ++j) {
+    auto row_of = [&](int j, unsigned off) {
       const int phys = __shfl_sync(0xffffffffu, tc_val, (blk_first + j - tc_base) & 31);
-      const bool ok = j < nsub && blk_first + j < n_seq_blocks && phys >= 0 &&
-                      phys < src.num_blocks;
-      rows[j] = ok ? (int)((unsigned)phys * (unsigned)bs +
-                           (j == 0 && bs > TT ? (unsigned)(t0 & (bs - 1)) : 0u))
-                   : oob_row;
-    }
-    if (lane == 0) {
-      mbar_arrive_expect_tx(full, Gm::kStageBytes);
+      const bool ok = blk_first + j < n_seq_blocks && phys >= 0 && phys < src.num_blocks;
+      return ok ? (int)((unsigned)phys * (unsigned)bs + off) : oob_row;
+    };
+    if (bs >= TT) {
+      const int row = row_of(0, (unsigned)(t0 & (bs - 1)));
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, Gm::kStageBytes);
 #pragma unroll
-      for (int h = 0; h < Gm::kHalves; ++h) {
-        const int x = kvh * D + h * Gm::kBoxCols;
-        const uint32_t off = h * Gm::kHalfStride;
+        for (int h = 0; h < Gm::kHalves; ++h) {
+          const int x = kvh * D + h * Gm::kBoxCols;
+          tma_load_2d(sK + h * Gm::kHalfStride, tmap_k, x, row, full);
+          tma_load_2d(sV + h * Gm::kHalfStride, tmap_v, x, row, full);
+        }
+      }
+    } else if (2 * bs == TT) {
+      const int row0 = row_of(0, 0u), row1 = row_of(1, 0u);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, Gm::kStageBytes);
 #pragma unroll
-        for (int j = 0; j < kMaxSub; ++j) {
-          if (j < nsub) {
-            tma_load_2d(sK + off + j * box_rows * 128, tmap_k, x, rows[j], full);
-            tma_load_2d(sV + off + j * box_rows * 128, tmap_v, x, rows[j], full);
+        for (int h = 0; h < Gm::kHalves; ++h) {
+          const int x = kvh * D + h * Gm::kBoxCols;
+          const uint32_t off = h * Gm::kHalfStride;
+          tma_load_2d(sK + off, tmap_k, x, row0, full);
+          tma_load_2d(sV + off, tmap_v, x, row0, full);
+          tma_load_2d(sK + off + bs * 128, tmap_k, x, row1, full);
+          tma_load_2d(sV + off + bs * 128, tmap_v, x, row1, full);
+        }
+      }
+    } else {  // 8 <= bs < TT / 2: TT / bs boxes
+      constexpr int kMaxSub = TT / 8;
+      const int nsub = TT / bs;
+      int rows[kMaxSub];
+#pragma unroll
+      for (int j = 0; j < kMaxSub; ++j) rows[j] = row_of(j, 0u);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, Gm::kStageBytes);
+#pragma unroll
+        for (int h = 0; h < Gm::kHalves; ++h) {
+          const int x = kvh * D + h * Gm::kBoxCols;
+          const uint32_t off = h * Gm::kHalfStride;
+#pragma unroll
+          for (int j = 0; j < kMaxSub; ++j) {
+            if (j < nsub) {
+              tma_load_2d(sK + off + j * bs * 128, tmap_k, x, rows[j], full);
+              tma_load_2d(sV + off + j * bs * 128, tmap_v, x, rows[j], full);
+            }
           }
         }
       }
