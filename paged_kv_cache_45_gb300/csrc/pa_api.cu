@@ -46,20 +46,36 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 pa_status prepare_kernel(const void* func, int threads, int smem_bytes, int* blocks_per_sm) {
   static std::mutex mu;
-  static std::map<std::tuple<const void*, int, int, int>, int> cache;  // -> blocks per SM
+  // The dynamic shared-memory limit is one attribute per kernel and device:
+  // it only ever grows here (to the largest size launched so far), so a
+  // smaller launch in between never leaves it below a size cached earlier.
+  static std::map<std::pair<const void*, int>, int> limit;
+  static std::map<std::tuple<const void*, int, int, int>, int> occupancy;  // -> blocks per SM
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
-  const auto key = std::make_tuple(func, dev, threads, smem_bytes);
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return PA_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(key);
-  if (it == cache.end()) {
-    int per_sm = 0;
+  int& lim = limit[std::make_pair(func, dev)];
+  if (smem_bytes > lim) {
     if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, threads, smem_bytes) !=
-            cudaSuccess)
+        cudaSuccess) {
+      cudaGetLastError();  // reported here, not by a later launch check
       return PA_ERR_CUDA;
-    it = cache.emplace(key, per_sm < 1 ? 1 : per_sm).first;
+    }
+    lim = smem_bytes;
+  }
+  const auto key = std::make_tuple(func, dev, threads, smem_bytes);
+  auto it = occupancy.find(key);
+  if (it == occupancy.end()) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, threads, smem_bytes) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return PA_ERR_CUDA;
+    }
+    it = occupancy.emplace(key, per_sm < 1 ? 1 : per_sm).first;
   }
   if (blocks_per_sm) *blocks_per_sm = it->second;
   return PA_OK;
@@ -162,6 +178,7 @@ extern "C" const char* pa_status_str(pa_status status) {
     case PA_ERR_CUDA: return "PA_ERR_CUDA";
     case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
     case PA_ERR_DEVICE: return "PA_ERR_DEVICE";
+    case PA_ERR_CAPACITY: return "PA_ERR_CAPACITY";
   }
   return "PA_ERR_UNKNOWN";
 }

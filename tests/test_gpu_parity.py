@@ -144,6 +144,20 @@ def test_balanced_workspace_is_reusable_and_deterministic(cuda_lib):
     P.assert_close(P.to_f64(outs[0]), P.oracle_out(case), "balanced reuse")
 
 
+def test_batch_size_may_shrink_and_grow_between_calls(cuda_lib):
+    # the kernel's shared memory grows with the batch (its prefix sums); a
+    # smaller batch in between must not leave the kernel unable to launch the
+    # larger one again
+    rng = np.random.default_rng(5)
+    big = wl.make_case("grow", 620, list(rng.integers(1, 40, 2999)), 8, 2, 128, 16)
+    small = wl.make_case("shrink", 621, [5, 70, 300] * 4 + [9], 8, 2, 128, 16)
+    for case in (big, small, big, small):
+        out, _, _ = run_step(cuda_lib, case, split=BAL)
+        seqs = None if case.batch < 100 else list(range(0, case.batch, 37))
+        got = P.to_f64(out) if seqs is None else P.to_f64(out)[seqs]
+        P.assert_close(got, P.oracle_out(case, seqs=seqs), f"B={case.batch}")
+
+
 def test_balanced_rejects_small_workspace(cuda_lib):
     b = cuda_lib
     case = wl.tiny_case(0)
