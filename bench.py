@@ -56,7 +56,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2048)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["cb70b", "8b", "long", "prefix"], default="cb70b")
+    ap.add_argument("--workload", choices=["cb70b", "8b", "long", "prefix", "cow"],
+                    default="cb70b",
+                    help="cow: the copy-on-write step of the prefix cache (its own metric)")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
                     help="fp8: the same workload on an e4m3 KV pool with per-head scales "
                          "(balanced schedule only)")
@@ -95,6 +97,10 @@ def describe(workload: str, batch: int = 256) -> str:
                 "128, bf16, block_size 16, 1% of K rows x8, no append",
         "prefix": "radix prefix sharing: B=128, 2048-token prefix in the same 128 blocks, "
                   "private suffix uniform [64, 1024] + 1 appended, 8B heads",
+        "cow": "copy-on-write after forking: {batch} sequences forked, the first append of "
+               "each child copies its shared partial block (K and V, block_size 16, 8 KV heads, "
+               "head_dim 128, bf16: 32 KiB each); 32 disjoint copy sets over a 1 GiB pool "
+               "cycled",
     }[workload].replace("{batch}", str(batch))
 
 
@@ -628,10 +634,175 @@ def run_reference(args):
     }), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# the copy-on-write step (prefix cache + pa_copy_blocks)
+# ---------------------------------------------------------------------------
+
+COW_METRIC = "copy-on-write block copy GB/s (bytes read + written), forked batch"
+
+
+def cow_cpu_baseline(batch: int, block_elems: int, budget_s: float):
+    """The oracle's block copy on the host (NumPy, one thread) over the same
+    kind of step: `batch` 32 KiB K and V block copies per step."""
+    import numpy as np
+    from oracle import prefix_cache as pc
+    nb = 1 + 2 * batch
+    k = np.zeros((nb, block_elems), dtype=np.uint16)
+    v = np.zeros_like(k)
+    pairs = [(1 + i, 1 + batch + i) for i in range(batch)]
+    steps, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s or steps < 3:
+        pc.copy_blocks(k, v, pairs)
+        steps += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(4 * batch * block_elems * 2 * steps / dt / 1e9, 3), "unit": "GB/s",
+            "cores": 1, "kind": "oracle",
+            "sample": f"{steps} steps of {batch} K+V block copies (oracle copy_blocks, NumPy, "
+                      f"blocks reused: host-cache resident), {dt:.1f} s"}
+
+
+def run_cow(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from paged_kv_cache_45_gb300 import binding as b
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    B, bs, hkv, d, sets = args.batch, 16, 8, 128, 32
+    block_elems = bs * hkv * d
+    block_bytes = block_elems * 2
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cow_cpu_baseline(B, block_elems, min(args.cpu_seconds, 5.0))
+
+    # device pool and copy sets: every step copies B fresh blocks; 32 disjoint
+    # sets (1 GiB of K+V) cycle, so a set's blocks are out of the L2 when reused
+    nb = 1 + 2 * B * sets
+    k_cache = torch.zeros((nb, bs, hkv, d), dtype=torch.bfloat16, device=device)
+    v_cache = torch.zeros_like(k_cache)
+    rng = np.random.default_rng(args.seed + rank)
+    ids = rng.permutation(np.arange(1, nb)).astype(np.int32).reshape(sets, 2, B)
+    src = [torch.from_numpy(ids[i, 0].copy()).to(device) for i in range(sets)]
+    dst = [torch.from_numpy(ids[i, 1].copy()).to(device) for i in range(sets)]
+    stream = torch.cuda.current_stream(device)
+    for w in range(args.warmup):
+        b.pa_copy_blocks(k_cache, v_cache, src[w % sets], dst[w % sets])
+    torch.cuda.synchronize()
+    K = args.steps
+    t_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
+    if sampler:
+        sampler.__enter__()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_ev[0].record(stream)
+    for k in range(K):
+        b.pa_copy_blocks(k_cache, v_cache, src[k % sets], dst[k % sets])
+    t_ev[1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    if sampler:
+        sampler.__exit__(None, None, None)
+    total_s = t_ev[0].elapsed_time(t_ev[1]) / 1e3
+    step_bytes = 4 * B * block_bytes                  # K and V, read and written
+    # per-launch events (the roofline's kernel duration)
+    KI = min(K, 256)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(KI)]
+    for k in range(KI):
+        evs[k][0].record(stream)
+        b.pa_copy_blocks(k_cache, v_cache, src[k % sets], dst[k % sets])
+        evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    kern_s = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3 / KI
+
+    # end to end through the public API: the host prefix cache forks the batch,
+    # the children's first append asks for the copies, the pairs go to the
+    # device, the kernel copies; the children are then discarded (host)
+    pcache = b.PrefixCache(nb, bs)
+    parents = []
+    for i in range(B):
+        sid, cached = pcache.admit(list(range(i * 1000, i * 1000 + 3 * bs + 5)))
+        pcache.write_slots(sid, cached, 3 * bs + 5)
+        parents.append(sid)
+    E = min(args.e2e_steps, K)
+    pin_src = torch.empty(B, dtype=torch.int32, pin_memory=True)
+    pin_dst = torch.empty(B, dtype=torch.int32, pin_memory=True)
+    dsrc = torch.empty(B, dtype=torch.int32, device=device)
+    ddst = torch.empty(B, dtype=torch.int32, device=device)
+    e2e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    e2e_ev[0].record(stream)
+    for k in range(E):
+        kids = pcache.fork_batch(parents)
+        _, (cs, cd) = pcache.append_tokens(kids)
+        stream.synchronize()                          # the pinned buffers are reused
+        pin_src.numpy()[:] = cs
+        pin_dst.numpy()[:] = cd
+        dsrc.copy_(pin_src, non_blocking=True)
+        ddst.copy_(pin_dst, non_blocking=True)
+        b.pa_copy_blocks(k_cache, v_cache, dsrc, ddst)
+        pcache.discard(kids)
+    e2e_ev[1].record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e2e_ev[0].elapsed_time(e2e_ev[1]) / 1e3
+    stats = torch.tensor([total_s, step_bytes * K, e2e_s, step_bytes * E], dtype=torch.float64,
+                         device=device)
+    if world > 1:
+        total_s, all_bytes, e2e_s, e2e_bytes = combine_ranks(stats)
+    else:
+        all_bytes, e2e_bytes = step_bytes * K, step_bytes * E
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = measured_hbm_peak()
+    gbs = all_bytes / total_s / 1e9
+    kern_gbs = step_bytes / kern_s / 1e9
+    line = {
+        "metric": COW_METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(total_s / K * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (bytes)",
+        "data": "synthetic (zero-filled pool; seeded block ids)",
+        "config": {"workload": describe("cow", B), "batch": B, "block_bytes": block_bytes,
+                   "l2": "32 disjoint copy sets (1 GiB) cycled: each set is out of the 129 MB "
+                         "L2 when it comes round again",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_of_hbm_peak": round(100 * gbs / peak, 2),
+        "roofline": {"bound": "hbm", "kernel": "copy_blocks_kernel", "achieved": round(kern_gbs, 2),
+                     "peak": peak, "unit": "GB/s", "frac": round(kern_gbs / peak, 4),
+                     "peak_kind": f"{peak_kind} hbm_gbs (a copy: bytes read + written)",
+                     "traffic": None, "algorithmic_bytes_per_launch": step_bytes,
+                     "measured": f"CUDA events around each launch, {KI} launches"},
+        "e2e": {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 0, "steps": E,
+                "note": "host prefix cache fork + append (decides the copies), H2D of the "
+                        "pairs, copy kernel, host discard; the result stays in the pool"},
+        "gpu_launches": K,
+        "timing": "CUDA events bracketing the K steps on the launching stream",
+    }
+    if sampler:
+        line["clocks"] = sampler.summary()
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "cow":
+        run_cow(args)
     else:
         run_gpu(args)
 

@@ -20,13 +20,17 @@
  *             the show" (paging, GQA).
  *   [LIFE]    "The inference request lifecycle", section "KV cache grows with
  *             the sum of cached tokens" (GQA: fewer KV heads, same query heads).
+ *   [PYS-RADIX] pyshine "text-generation-inference", section "The radix
+ *             prefix cache"; [PYS-BATCH] same page, "Inside the batching task".
  *
  * Conventions for every entry point:
  *   - bf16 means IEEE bfloat16 (2 bytes). All tensors are dense, row-major,
  *     in the shapes given, and DEVICE memory owned by the caller, except where
  *     a parameter says "host".
- *   - The library allocates no memory, keeps no state between calls (apart
- *     from one 4-byte device error word per device, see pa_last_device_error)
+ *   - The library allocates no device memory, keeps no state between calls
+ *     (apart from one 4-byte device error word per device, see
+ *     pa_last_device_error, and the host-side prefix cache objects the caller
+ *     creates and destroys, see pa_prefix_cache_create)
  *     and launches only on `stream` (a cudaStream_t; NULL = legacy default
  *     stream). Calls return as soon as the kernels are queued; they do not
  *     synchronise, except in validating mode (environment PA_VALIDATE=1),
@@ -66,7 +70,8 @@ typedef enum {
   PA_ERR_UNSUPPORTED = -2, /* valid but not built: head_dim, group size, block size  */
   PA_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed                    */
   PA_ERR_WORKSPACE = -4,   /* split mode without partial buffers                      */
-  PA_ERR_DEVICE = -5       /* a kernel's bounded wait ran out (see pa_last_device_error) */
+  PA_ERR_DEVICE = -5,      /* a kernel's bounded wait ran out (see pa_last_device_error) */
+  PA_ERR_CAPACITY = -6     /* prefix cache: not enough free or evictable blocks          */
 } pa_status;
 
 /*
@@ -306,6 +311,122 @@ pa_status pa_last_device_error(int32_t* code);
  * the context stays usable. No counterpart on the pages (they describe the
  * serving system's failure handling, not kernels'). */
 pa_status pa_selftest_wait_timeout(int32_t limit_us, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Prefix cache with copy-on-write (host side) and the block copy (device).
+ *
+ * [TGI-PA] prefix sharing: requests with the same system prompt point their
+ * tables at the same physical blocks; a write into a shared block first
+ * copies it to a fresh block and repoints the writer's table.
+ * [PYS-RADIX] pyshine "text-generation-inference", section "The radix prefix
+ * cache": block 0 reserved, a free list plus a compressed prefix tree keyed
+ * by token ids at block granularity, references on the match before any
+ * eviction, least-recently-used eviction of unreferenced prefixes when the
+ * free list is empty, node splits on partial overlap, double-cached blocks
+ * back to the free list on release. [PYS-BATCH] same page, section "Inside
+ * the batching task": a fully cached prompt gives one token back.
+ *
+ * A pa_prefix_cache is a host object managing block ids 1..num_blocks-1 of a
+ * pool and the block tables of live sequences; it touches no device memory.
+ * Its rules:
+ *   - only full blocks are cached, each keyed by the whole token prefix it
+ *     ends; fresh blocks are taken lowest id first;
+ *   - every mutating call advances a tick; a match, an insertion and the
+ *     touch on release stamp the blocks on the request's path with it;
+ *     eviction frees one block at a time, the unreferenced leaf with the
+ *     oldest (tick, block id);
+ *   - a write into a block that is cached or shared by another sequence is
+ *     a copy-on-write: the call returns the (src, dst) block pairs, which the
+ *     caller copies on the device (pa_copy_blocks) before writing K/V rows;
+ *   - a call that needs more fresh blocks than the free blocks plus the
+ *     blocks eviction could free returns PA_ERR_CAPACITY and changes nothing
+ *     (pa_prefix_append_tokens: nothing for the sequence that failed).
+ * Not thread-safe: one caller at a time per object. Sequence ids are > 0.
+ * ---------------------------------------------------------------------- */
+typedef struct pa_prefix_cache pa_prefix_cache;
+
+/* New empty cache for a pool of num_blocks (>= 2) blocks of block_size
+ * tokens. *out receives the object (host memory owned by the library until
+ * pa_prefix_cache_destroy). */
+pa_status pa_prefix_cache_create(int32_t num_blocks, int32_t block_size, pa_prefix_cache** out);
+void pa_prefix_cache_destroy(pa_prefix_cache* cache);
+
+/* Admit a request with prompt tokens[0, num_tokens) (host, num_tokens >= 1):
+ * match the longest cached block prefix, reference it, and give the new
+ * sequence fresh blocks for the rest of the prompt. *seq_id receives the
+ * sequence, *cached_tokens how many leading positions already hold their
+ * K/V (the match, minus one when it covers the whole prompt). The caller
+ * then writes positions [*cached_tokens, num_tokens) via
+ * pa_prefix_write_slots. */
+pa_status pa_prefix_admit(pa_prefix_cache* cache, const int32_t* tokens, int32_t num_tokens,
+                          int64_t* seq_id, int32_t* cached_tokens);
+
+/* Slots (host int64 [pos_end - pos_begin], block * block_size + offset) for
+ * writing positions [pos_begin, pos_end) of a sequence; pos_begin must not
+ * exceed its current length, which grows to pos_end. Blocks that must be
+ * copied first come back as copy_src[i] -> copy_dst[i] (host int32,
+ * capacity max_copies; too small gives PA_ERR_INVALID_ARG before any change),
+ * *num_copies of them. */
+pa_status pa_prefix_write_slots(pa_prefix_cache* cache, int64_t seq_id, int32_t pos_begin,
+                                int32_t pos_end, int64_t* slots, int32_t* copy_src,
+                                int32_t* copy_dst, int32_t max_copies, int32_t* num_copies);
+
+/* One decode position for each of seq_ids[0, num_seqs) in order (the slot of
+ * each sequence's next token into slots[i]: the step's slot_mapping), with
+ * the copies they need (max_copies >= num_seqs). On PA_ERR_CAPACITY,
+ * *num_done sequences were extended and their copies are returned. */
+pa_status pa_prefix_append_tokens(pa_prefix_cache* cache, const int64_t* seq_ids,
+                                  int32_t num_seqs, int64_t* slots, int32_t* copy_src,
+                                  int32_t* copy_dst, int32_t max_copies, int32_t* num_copies,
+                                  int32_t* num_done);
+
+/* A new sequence sharing every block of seq_id (parallel sampling); the
+ * first write of either into a shared block copies it. */
+pa_status pa_prefix_fork(pa_prefix_cache* cache, int64_t seq_id, int64_t* child_id);
+
+/* pa_prefix_fork for each of seq_ids[0, num_seqs) in order; child_ids (host
+ * int64 [num_seqs]) receives the new sequences. Unknown ids: nothing done. */
+pa_status pa_prefix_fork_batch(pa_prefix_cache* cache, const int64_t* seq_ids, int32_t num_seqs,
+                               int64_t* child_ids);
+
+/* End sequences without caching anything (pa_prefix_release with no
+ * tokens: an aborted request, a discarded sample). Unknown ids: nothing
+ * done. */
+pa_status pa_prefix_discard(pa_prefix_cache* cache, const int64_t* seq_ids, int32_t num_seqs);
+
+/* End a sequence whose positions [0, num_tokens) hold the K/V of tokens
+ * (host): its full blocks along that path enter the cache unless the prefix
+ * is cached already (then they return to the free list with the rest of its
+ * unreferenced blocks). */
+pa_status pa_prefix_release(pa_prefix_cache* cache, int64_t seq_id, const int32_t* tokens,
+                            int32_t num_tokens);
+
+/* A sequence's block table (host int32, capacity max_blocks), *num_blocks
+ * entries, and its length in *num_tokens (may be NULL). */
+pa_status pa_prefix_table(pa_prefix_cache* cache, int64_t seq_id, int32_t* table,
+                          int32_t max_blocks, int32_t* num_blocks, int32_t* num_tokens);
+
+/* Block tables of seq_ids[0, num_seqs) as rows of a host int32
+ * [num_seqs, max_blocks] array (unused entries 0) and their lengths in
+ * context_lens (host int32 [num_seqs]): the decode step's inputs. */
+pa_status pa_prefix_tables(pa_prefix_cache* cache, const int64_t* seq_ids, int32_t num_seqs,
+                           int32_t* tables, int32_t max_blocks, int32_t* context_lens);
+
+/* Free blocks, cached blocks, and blocks referenced by live sequences (each
+ * pointer may be NULL). */
+pa_status pa_prefix_stats(const pa_prefix_cache* cache, int32_t* free_blocks,
+                          int32_t* cached_blocks, int32_t* used_blocks);
+
+/* Copy-on-write on the device: for i < num_copies, block dst[i] of both
+ * caches becomes a byte copy of block src[i]. src, dst: device int32
+ * [num_copies]; a block is block_bytes bytes (block_size * num_kv_heads *
+ * head_dim * bytes per value; a multiple of 16; caches 16-byte aligned).
+ * dst ids must be distinct and none may appear in src (the copies then run
+ * in parallel). Ids outside [0, num_blocks) are skipped by the kernel and,
+ * in validating mode, rejected with PA_ERR_INVALID_ARG along with overlaps. */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst,
+                         int32_t num_copies, int32_t num_blocks, int64_t block_bytes,
+                         void* stream);
 
 /* Human-readable name of a status. Never NULL. */
 const char* pa_status_str(pa_status status);

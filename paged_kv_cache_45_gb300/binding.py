@@ -50,6 +50,19 @@ _SIGS = {
     "pa_kv_bytes_per_token": (_i64, [_i32, _i32, _i32, _i32]),
     "pa_last_device_error": (_i32, [ctypes.POINTER(_i32)]),
     "pa_selftest_wait_timeout": (_i32, [_i32, _p]),
+    "pa_prefix_cache_create": (_i32, [_i32, _i32, _p]),
+    "pa_prefix_cache_destroy": (None, [_p]),
+    "pa_prefix_admit": (_i32, [_p, _p, _i32, _p, _p]),
+    "pa_prefix_write_slots": (_i32, [_p, _i64, _i32, _i32, _p, _p, _p, _i32, _p]),
+    "pa_prefix_append_tokens": (_i32, [_p, _p, _i32, _p, _p, _p, _i32, _p, _p]),
+    "pa_prefix_fork": (_i32, [_p, _i64, _p]),
+    "pa_prefix_fork_batch": (_i32, [_p, _p, _i32, _p]),
+    "pa_prefix_discard": (_i32, [_p, _p, _i32]),
+    "pa_prefix_release": (_i32, [_p, _i64, _p, _i32]),
+    "pa_prefix_table": (_i32, [_p, _i64, _p, _i32, _p, _p]),
+    "pa_prefix_tables": (_i32, [_p, _p, _i32, _p, _i32, _p]),
+    "pa_prefix_stats": (_i32, [_p, _p, _p, _p]),
+    "pa_copy_blocks": (_i32, [_p, _p, _p, _p, _i32, _i32, _i64, _p]),
     "pa_status_str": (ctypes.c_char_p, [_i32]),
     "pa_version": (ctypes.c_char_p, []),
 }
@@ -411,3 +424,158 @@ def plan_split(context_lens_host, num_kv_heads: int, sms: int = 152, blocks_per_
     while split < per_block and split < hi:
         split *= 2
     return 0 if lens.max() <= split else int(split)
+
+
+# ---------------------------------------------------------------------------
+# prefix cache (host) and copy-on-write (device)
+# ---------------------------------------------------------------------------
+
+PA_ERR_CAPACITY = -6
+
+
+class CapacityError(PagedKVError):
+    """The pool has no free or evictable block for the call (nothing changed)."""
+
+
+def _host_i32(values):
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(values, dtype=np.int32))
+    return a, a.ctypes.data
+
+
+class PrefixCache:
+    """Host block pool with a radix prefix cache and copy-on-write
+    (``pa_prefix_*``). Methods mirror the C calls; copies come back as
+    (src, dst) block pairs for :func:`pa_copy_blocks`."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        h = ctypes.c_void_p()
+        _check("pa_prefix_cache_create",
+               _lib.pa_prefix_cache_create(int(num_blocks), int(block_size), ctypes.byref(h)))
+        self._h = h
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def close(self):
+        if self._h:
+            _lib.pa_prefix_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _status(fn, st):
+        if st == PA_ERR_CAPACITY:
+            raise CapacityError(fn, st)
+        _check(fn, st)
+
+    def admit(self, tokens):
+        arr, ptr = _host_i32(tokens)
+        sid, cached = _i64(), _i32()
+        self._status("pa_prefix_admit", _lib.pa_prefix_admit(
+            self._h, ptr, len(arr), ctypes.byref(sid), ctypes.byref(cached)))
+        return sid.value, cached.value
+
+    def write_slots(self, seq_id, p0, p1):
+        import numpy as np
+        n = max(p1 - p0, 0)
+        slots = np.zeros(max(n, 1), dtype=np.int64)
+        nb = (p1 - 1) // self.block_size - p0 // self.block_size + 1 if n else 0
+        src = np.zeros(max(nb, 1), dtype=np.int32)
+        dst = np.zeros(max(nb, 1), dtype=np.int32)
+        nc = _i32()
+        self._status("pa_prefix_write_slots", _lib.pa_prefix_write_slots(
+            self._h, int(seq_id), int(p0), int(p1), slots.ctypes.data, src.ctypes.data,
+            dst.ctypes.data, len(src), ctypes.byref(nc)))
+        return [int(x) for x in slots[:n]], [(int(src[i]), int(dst[i])) for i in range(nc.value)]
+
+    def append_tokens(self, seq_ids):
+        """One decode position per sequence: (slots int64 array, copies, done)."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        n = len(ids)
+        slots = np.zeros(max(n, 1), dtype=np.int64)
+        src = np.zeros(max(n, 1), dtype=np.int32)
+        dst = np.zeros(max(n, 1), dtype=np.int32)
+        nc, done = _i32(), _i32()
+        st = _lib.pa_prefix_append_tokens(self._h, ids.ctypes.data, n, slots.ctypes.data,
+                                          src.ctypes.data, dst.ctypes.data, len(src),
+                                          ctypes.byref(nc), ctypes.byref(done))
+        copies = (src[:nc.value].copy(), dst[:nc.value].copy())
+        if st == PA_ERR_CAPACITY:
+            err = CapacityError("pa_prefix_append_tokens", st)
+            err.done, err.slots, err.copies = done.value, slots[:done.value], copies
+            raise err
+        _check("pa_prefix_append_tokens", st)
+        return slots[:n], copies
+
+    def fork(self, seq_id):
+        child = _i64()
+        self._status("pa_prefix_fork", _lib.pa_prefix_fork(self._h, int(seq_id),
+                                                           ctypes.byref(child)))
+        return child.value
+
+    def fork_batch(self, seq_ids):
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        out = np.zeros(max(len(ids), 1), dtype=np.int64)
+        self._status("pa_prefix_fork_batch", _lib.pa_prefix_fork_batch(
+            self._h, ids.ctypes.data, len(ids), out.ctypes.data))
+        return out[:len(ids)]
+
+    def discard(self, seq_ids):
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        self._status("pa_prefix_discard", _lib.pa_prefix_discard(self._h, ids.ctypes.data,
+                                                                 len(ids)))
+
+    def release(self, seq_id, tokens):
+        arr, ptr = _host_i32(tokens)
+        self._status("pa_prefix_release", _lib.pa_prefix_release(self._h, int(seq_id), ptr,
+                                                                 len(arr)))
+
+    def table(self, seq_id):
+        import numpy as np
+        cap = self.num_blocks
+        buf = np.zeros(cap, dtype=np.int32)
+        nb, nt = _i32(), _i32()
+        self._status("pa_prefix_table", _lib.pa_prefix_table(
+            self._h, int(seq_id), buf.ctypes.data, cap, ctypes.byref(nb), ctypes.byref(nt)))
+        return [int(x) for x in buf[:nb.value]]
+
+    def tables(self, seq_ids, max_blocks):
+        """(block_tables int32 [n, max_blocks], context_lens int32 [n]) as numpy."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        t = np.zeros((len(ids), max_blocks), dtype=np.int32)
+        lens = np.zeros(len(ids), dtype=np.int32)
+        self._status("pa_prefix_tables", _lib.pa_prefix_tables(
+            self._h, ids.ctypes.data, len(ids), t.ctypes.data, int(max_blocks),
+            lens.ctypes.data))
+        return t, lens
+
+    def stats(self):
+        f, c, u = _i32(), _i32(), _i32()
+        _check("pa_prefix_stats", _lib.pa_prefix_stats(self._h, ctypes.byref(f), ctypes.byref(c),
+                                                       ctypes.byref(u)))
+        return f.value, c.value, u.value
+
+
+def pa_copy_blocks(k_cache, v_cache, src, dst, stream=None) -> None:
+    """Block dst[i] of both caches becomes a copy of block src[i] (device int32)."""
+    if tuple(k_cache.shape) != tuple(v_cache.shape) or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must match")
+    if src.numel() != dst.numel():
+        raise ValueError("src and dst must have the same length")
+    n = src.numel()
+    if n == 0:
+        return
+    nb = k_cache.shape[0]
+    block_bytes = k_cache[0].numel() * k_cache.element_size()
+    _check("pa_copy_blocks", _lib.pa_copy_blocks(
+        _t(k_cache, k_cache.dtype, "k_cache"), _t(v_cache, v_cache.dtype, "v_cache"),
+        _t(src, torch.int32, "src"), _t(dst, torch.int32, "dst"), n, nb, block_bytes,
+        _stream(stream)))

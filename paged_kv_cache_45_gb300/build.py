@@ -1,6 +1,6 @@
 """Build ``libpagedkv.so`` in-tree with nvcc for sm_103a (GB300).
 
-Each ``csrc/*.cu`` file compiles in parallel to ``_build/*.o``; the objects
+Each ``csrc/*.cu`` and ``csrc/*.cpp`` file compiles in parallel to ``_build/*.o``; the objects
 link into ``paged_kv_cache_45_gb300/libpagedkv.so`` (static CUDA runtime, no
 other dependency). Rebuilds only when a source or header is newer than the
 library, unless ``force``. Run ``python -m paged_kv_cache_45_gb300.build``.
@@ -34,7 +34,7 @@ def nvcc() -> str:
 
 
 def sources() -> list[str]:
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _inputs() -> list[str]:
@@ -50,7 +50,7 @@ def up_to_date() -> bool:
 
 
 def _compile(src: str, ptxas_verbose: bool) -> tuple[str, str]:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+    obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
     cmd = [nvcc(), *ARCH, *FLAGS, "-c", src, "-o", obj]
     if ptxas_verbose:
         cmd += ["-Xptxas", "-v"]
