@@ -28,6 +28,7 @@ from .paged_attention import (  # noqa: F401
     decode_split_partials,
     lse_merge,
     decode_pseudocode_loops,
+    decode_multi,
     e4m3_value,
     e4m3_encode,
     e4m3_decode,

@@ -323,6 +323,54 @@ def decode_pseudocode_loops(q, k_cache, v_cache, block_tables, context_lens,
 
 
 # ---------------------------------------------------------------------------
+# several query tokens per sequence (chunked prefill, speculative verification)
+# ---------------------------------------------------------------------------
+# "Text Generation Inference ...", section "Advanced Pattern: Chunked Prefill
+# (TGI v3)": a prompt is processed in chunks interleaved with decode steps;
+# "How to Speed Up LLM Inference ...", section "Speculative decoding: more
+# than one token per weight-read": the target model checks the gamma drafted
+# tokens plus one in a single pass. Either way a sequence brings q_len new
+# query tokens, appended at the end of its context. Reading taken (the pages
+# state no mask): the new tokens hold the last q_len positions of the context
+# (after the append), and the token at position p attends to positions
+# 0..p -- everything before it and itself, nothing after (causal).
+
+def decode_multi(q_rows, k_cache, v_cache, block_tables, context_lens, q_start,
+                 scale: float) -> np.ndarray:
+    """float64 attention output ``[R, H_q, D]`` for packed query rows.
+
+    ``q_rows`` holds bf16 bits ``[R, H_q, D]``: sequence ``b`` owns rows
+    ``q_start[b] .. q_start[b+1]-1``, its ``n_b`` new tokens in order, and row
+    ``q_start[b] + i`` sits at position ``p = context_lens[b] - n_b + i``. For
+    each such row and query head ``h``: ``softmax(scale * K[0..p, h // G] q) @
+    V[0..p, h // G]``. Rows with ``p < 0`` (more new tokens than context) are
+    zero.
+    """
+    G = _group(q_rows, k_cache)
+    R, hq, d = q_rows.shape
+    out = np.zeros((R, hq, d), dtype=np.float64)
+    for b in range(len(context_lens)):
+        r0, r1 = int(q_start[b]), int(q_start[b + 1])
+        n = r1 - r0
+        ctx = int(context_lens[b])
+        if n == 0 or ctx == 0:
+            continue
+        K = bf16_bits_to_f64(gather_sequence(k_cache, block_tables[b], ctx))
+        V = bf16_bits_to_f64(gather_sequence(v_cache, block_tables[b], ctx))
+        for i in range(n):
+            pos = ctx - n + i
+            if pos < 0:
+                continue
+            qi = bf16_bits_to_f64(q_rows[r0 + i])
+            for h in range(hq):
+                kvh = h // G
+                s = scale * (K[:pos + 1, kvh, :] @ qi[h])
+                w = np.exp(s - s.max())
+                out[r0 + i, h] = (w @ V[:pos + 1, kvh, :]) / w.sum()
+    return out
+
+
+# ---------------------------------------------------------------------------
 # FP8 (e4m3) KV cache
 # ---------------------------------------------------------------------------
 # "How to Speed Up LLM Inference: KV Cache to Production Serving" (section "The

@@ -214,6 +214,101 @@ def make_case(name: str, seed: int, ctx_before, num_q_heads: int, num_kv_heads: 
 
 
 # ---------------------------------------------------------------------------
+# several new query tokens per sequence (chunked prefill, speculative verify)
+# ---------------------------------------------------------------------------
+
+@dataclass
+class MultiCase:
+    """Inputs of one step in which sequence ``b`` appends ``q_len[b]`` tokens
+    and queries with all of them. Query and new K/V rows are packed: sequence
+    ``b`` owns rows ``q_start[b] .. q_start[b+1]-1``. Caches hold the state
+    before the append; ``context_lens`` count tokens after it."""
+    name: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    scale: float
+    q: torch.Tensor                 # bf16 [R, Hq, D]
+    q_start: torch.Tensor           # int32 [B + 1]
+    k_cache: torch.Tensor           # bf16 [NB, bs, Hkv, D]
+    v_cache: torch.Tensor
+    block_tables: torch.Tensor      # int32 [B, MB]
+    context_lens: torch.Tensor      # int32 [B]
+    k_new: torch.Tensor             # bf16 [R, Hkv, D]
+    v_new: torch.Tensor
+    slot_mapping: torch.Tensor      # int64 [R]
+    seq_blocks: list = field(default_factory=list)
+
+    @property
+    def batch(self) -> int:
+        return int(self.context_lens.shape[0])
+
+    @property
+    def rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def max_q_len(self) -> int:
+        qs = self.q_start.numpy()
+        return int((qs[1:] - qs[:-1]).max()) if self.batch else 0
+
+
+def make_multi_case(name: str, seed: int, ctx_before, q_lens, num_q_heads: int,
+                    num_kv_heads: int, head_dim: int, block_size: int, *,
+                    spare_frac: float = 0.10, scale: float | None = None) -> MultiCase:
+    """Seeded step with ``q_lens[b]`` new tokens after ``ctx_before[b]`` cached
+    ones. Blocks come off a shuffled free list (block 0 reserved); every slot
+    nobody owns is NaN."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx0 = np.asarray(ctx_before, dtype=np.int64)
+    ql = np.asarray(q_lens, dtype=np.int64)
+    B = len(ctx0)
+    ctx1 = ctx0 + ql
+    bs = block_size
+    need = [-(-int(c) // bs) for c in ctx1]
+    num_blocks = int(math.ceil((1.0 + spare_frac) * sum(need))) + 1
+    order = 1 + rng.permutation(num_blocks - 1)
+    alloc = BlockAllocator(num_blocks, order=order)
+    seq_blocks = [alloc.allocate(n) for n in need]
+    H, D = num_kv_heads, head_dim
+    k_cache = nan_pool(num_blocks, bs, H, D)
+    v_cache = nan_pool(num_blocks, bs, H, D)
+    kflat, vflat = k_cache.view(-1, H, D), v_cache.view(-1, H, D)
+    gk, gv, gq, gn = (_torch_gen(seed, p) for p in (11, 12, 13, 14))
+    for b in range(B):
+        n = int(ctx0[b])
+        if n:
+            rows = token_rows(seq_blocks[b], n, bs)
+            kflat[rows] = randn_bf16(gk, (n, H, D))
+            vflat[rows] = randn_bf16(gv, (n, H, D))
+    R = int(ql.sum())
+    q_start = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    slots = np.concatenate([token_rows(seq_blocks[b], int(ql[b]), bs, start=int(ctx0[b]))
+                            for b in range(B)] + [np.zeros(0, dtype=np.int64)]).astype(np.int64)
+    return MultiCase(
+        name=name, num_q_heads=num_q_heads, num_kv_heads=H, head_dim=D, block_size=bs,
+        num_blocks=num_blocks, scale=(1.0 / math.sqrt(D)) if scale is None else scale,
+        q=randn_bf16(gq, (R, num_q_heads, D)), q_start=torch.from_numpy(q_start),
+        k_cache=k_cache, v_cache=v_cache,
+        block_tables=pad_tables(seq_blocks, max(max(need, default=1), 1)),
+        context_lens=torch.from_numpy(ctx1.astype(np.int32)),
+        k_new=randn_bf16(gn, (R, H, D)), v_new=randn_bf16(gn, (R, H, D)),
+        slot_mapping=torch.from_numpy(slots), seq_blocks=seq_blocks)
+
+
+def spec_verify_case(seed: int = 0, batch: int = 256, q_len: int = 4) -> MultiCase:
+    """Speculative verification on the 70B shape: ``batch`` sequences with
+    lengths log-uniform in [128, 8192], each checking ``q_len`` new tokens (the
+    drafted ones plus one); 64 query heads on 8 KV heads, head_dim 128,
+    block_size 16."""
+    rng = np.random.Generator(np.random.PCG64(seed + 21_000))
+    ctx = loguniform(rng, 128, 8192, batch)
+    return make_multi_case(f"spec_b{batch}_q{q_len}", seed, ctx, [q_len] * batch, 64, 8, 128, 16)
+
+
+# ---------------------------------------------------------------------------
 # the five workloads
 # ---------------------------------------------------------------------------
 
