@@ -56,9 +56,11 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2048)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["cb70b", "8b", "long", "prefix", "cow"],
+    ap.add_argument("--workload", choices=["cb70b", "8b", "long", "prefix", "spec", "cow"],
                     default="cb70b",
-                    help="cow: the copy-on-write step of the prefix cache (its own metric)")
+                    help="spec: 4 query tokens per sequence (speculative verification, "
+                         "pa_decode_multi); cow: the copy-on-write step of the prefix cache "
+                         "(its own metric)")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
                     help="fp8: the same workload on an e4m3 KV pool with per-head scales "
                          "(balanced schedule only)")
@@ -97,6 +99,10 @@ def describe(workload: str, batch: int = 256) -> str:
                 "128, bf16, block_size 16, 1% of K rows x8, no append",
         "prefix": "radix prefix sharing: B=128, 2048-token prefix in the same 128 blocks, "
                   "private suffix uniform [64, 1024] + 1 appended, 8B heads",
+        "spec": "speculative verification, 70B shape: B={batch} sequences, ctx log-uniform "
+                "[128, 8192], 4 new query tokens each (causal), 64 q heads / 8 KV heads, "
+                "head_dim 128, bf16, block_size 16; pa_kv_append of the 4 rows + "
+                "pa_decode_multi",
         "cow": "copy-on-write after forking: {batch} sequences forked, the first append of "
                "each child copies its shared partial block (K and V, block_size 16, 8 KV heads, "
                "head_dim 128, bf16: 32 KiB each); 32 disjoint copy sets over a 1 GiB pool "
@@ -114,7 +120,18 @@ class Steps:
         self.workload = workload
         self.items = []
         self.fp8 = kv_dtype == "fp8"
-        if workload == "cb70b":
+        self.multi = workload == "spec"
+        if workload == "spec":
+            case = wl.spec_verify_case(seed, batch=batch, q_len=4)
+            self.k_cache, self.v_cache = case.k_cache.to(device), case.v_cache.to(device)
+            self.scale, self.hkv, self.hq, self.d = (case.scale, case.num_kv_heads,
+                                                     case.num_q_heads, case.head_dim)
+            self.max_context = int(case.block_tables.shape[1]) * case.block_size
+            self.max_q_len = case.max_q_len
+            self.items.append(dict(fill=None, q=case.q, k_new=case.k_new, v_new=case.v_new,
+                                   slots=case.slot_mapping, tables=case.block_tables,
+                                   lens=case.context_lens, qstart=case.q_start))
+        elif workload == "cb70b":
             cb = wl.ContinuousBatching(seed=seed, batch=batch)
             self.k_cache, self.v_cache = cb.initial_caches(device)
             self.scale, self.hkv, self.hq, self.d = cb.scale, cb.Hkv, cb.Hq, cb.D
@@ -139,7 +156,8 @@ class Steps:
                                    lens=case.context_lens))
         for it in self.items:   # host copies (pinned) for e2e, device copies for the step
             it["host"] = {k: it[k].pin_memory() for k in ("q", "k_new", "v_new", "slots", "tables",
-                                                           "lens") if it[k] is not None}
+                                                           "lens", "qstart")
+                          if it.get(k) is not None}
             it["dev"] = {k: v.to(device) for k, v in it["host"].items()}
             it["kv_bytes"] = (int(it["lens"].to(torch.int64).sum()) * 2 * self.hkv * self.d *
                               (1 if self.fp8 else 2))
@@ -244,7 +262,26 @@ KERNEL_SOURCES = {
     "balanced_decode_kernel": ("pa_decode_balanced.cu", "pa_tile.cuh", "pa_device.cuh"),
     "balanced_decode_kernel[e4m3]": ("pa_decode_balanced.cu", "pa_tile.cuh", "pa_device.cuh"),
     "paged_decode_kernel": ("pa_decode.cu", "pa_tile.cuh", "pa_device.cuh"),
+    "multi_decode_kernel": ("pa_decode_multi.cu", "pa_tile.cuh", "pa_device.cuh"),
 }
+
+
+class MultiWorkspace:
+    """Output and split-mode buffers of pa_decode_multi (rows, not sequences)."""
+
+    def __init__(self, b, steps, split, device):
+        import torch
+        R = int(steps.items[0]["q"].shape[0])
+        self.balanced = False
+        self.split_tokens = split
+        self.max_splits = b.pa_decode_num_splits(steps.max_context, split) if split else 0
+        self.out = torch.empty((R, steps.hq, steps.d), dtype=torch.bfloat16, device=device)
+        S = max(self.max_splits, 1)
+        self.part_out = torch.empty((R, steps.hq, S, steps.d), dtype=torch.float32,
+                                    device=device) if split else None
+        self.part_lse = torch.empty((R, steps.hq, S), dtype=torch.float32,
+                                    device=device) if split else None
+        self.row_lens = torch.empty(R, dtype=torch.int32, device=device) if split else None
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -313,7 +350,9 @@ def run_gpu(args):
     if steps.fp8 and args.schedule != "balanced":
         raise SystemExit("--kv-dtype fp8 runs the balanced schedule only")
     sms = b.num_sms(local)
-    if args.schedule == "balanced":
+    if steps.multi:
+        split = max(args.split, 0)
+    elif args.schedule == "balanced":
         split = b.BALANCED
     elif args.split >= 0:
         split = args.split
@@ -321,8 +360,11 @@ def run_gpu(args):
         split = 4096
     else:
         split = max(b.plan_split(it["lens"].numpy(), steps.hkv, sms) for it in steps.items)
-    ws = b.DecodeWorkspace(steps.batch, steps.hq, steps.d, split, steps.max_context, device,
-                           num_kv_heads=steps.hkv)
+    if steps.multi:
+        ws = MultiWorkspace(b, steps, split, device)
+    else:
+        ws = b.DecodeWorkspace(steps.batch, steps.hq, steps.d, split, steps.max_context, device,
+                               num_kv_heads=steps.hkv)
     stream = torch.cuda.current_stream(device)
 
     def fill(it):
@@ -337,6 +379,24 @@ def run_gpu(args):
     fused = args.step == "fused" and ws.balanced and steps.items[0]["dev"].get("k_new") is not None
 
     def step(dv, ev=None):
+        if steps.multi:
+            if ev is not None:
+                ev[0].record(stream)
+            b.pa_kv_append(dv["k_new"], dv["v_new"], dv["slots"], steps.k_cache, steps.v_cache)
+            if ev is not None:
+                ev[1].record(stream)
+            b.pa_decode_multi(dv["q"], steps.k_cache, steps.v_cache, dv["tables"], dv["lens"],
+                              dv["qstart"], steps.max_q_len, steps.scale, ws.out,
+                              ws.split_tokens, ws.max_splits, ws.part_out, ws.part_lse,
+                              ws.row_lens)
+            if ev is not None:
+                ev[2].record(stream)
+            if ws.split_tokens:
+                b.pa_decode_splitk_reduce(ws.part_out, ws.part_lse, ws.row_lens, ws.split_tokens,
+                                          ws.out)
+            if ev is not None:
+                ev[3].record(stream)
+            return
         if fused:
             if ev is not None:
                 ev[0].record(stream)
@@ -478,7 +538,7 @@ def run_gpu(args):
     dec_gbs_rank0 = dec_bytes / dec_s / 1e9
     kv_tokens_per_launch = kv_tokens / KI
     kernel = ("balanced_decode_kernel" + ("[e4m3]" if steps.fp8 else "")) if ws.balanced \
-        else "paged_decode_kernel"
+        else ("multi_decode_kernel" if steps.multi else "paged_decode_kernel")
     traffic = traffic_per_launch(kernel, kv_tokens_per_launch)
     clocks = sampler.summary() if sampler else None
     line = {
@@ -497,7 +557,9 @@ def run_gpu(args):
         "config": {"workload": describe(args.workload, args.batch) +
                    (" (e4m3 KV pool, per-KV-head scales)" if steps.fp8 else ""),
                    "schedule": "balanced" if ws.balanced else
-                   f"split (pa_decode split_tokens={ws.split_tokens} + pa_decode_splitk_reduce)",
+                   (f"multi (one block per KV head, split, sequence; split_tokens="
+                    f"{ws.split_tokens})" if steps.multi else
+                    f"split (pa_decode split_tokens={ws.split_tokens} + pa_decode_splitk_reduce)"),
                    "step": "fused: pa_append_decode, one launch" if fused else
                    "separate: pa_kv_append + decode launches",
                    "split_tokens": ws.split_tokens, "max_splits": ws.max_splits,

@@ -312,6 +312,39 @@ pa_status pa_last_device_error(int32_t* code);
  * serving system's failure handling, not kernels'). */
 pa_status pa_selftest_wait_timeout(int32_t limit_us, void* stream);
 
+/* Attention for several new query tokens per sequence under a causal mask:
+ * a chunk of a prompt ([TGI], section "Advanced Pattern: Chunked Prefill
+ * (TGI v3)") or the drafted tokens plus one of a speculative step ([SPEED],
+ * section "Speculative decoding: more than one token per weight-read").
+ *   q          bf16 [num_q_rows, num_q_heads, head_dim]: packed query rows;
+ *              sequence b owns rows q_start[b] .. q_start[b+1]-1 (its n_b new
+ *              tokens in order, already appended to the caches, e.g. by
+ *              pa_kv_append), so row q_start[b] + i is position
+ *              context_lens[b] - n_b + i and attends to positions 0 .. that
+ *              position (a row before position 0 gives zeros).
+ *   q_start    int32 [num_seqs + 1], q_start[0] = 0, q_start[num_seqs] =
+ *              num_q_rows, non-decreasing.
+ *   max_q_len  an upper bound of every n_b; max_q_len * (num_q_heads /
+ *              num_kv_heads) <= 64, else PA_ERR_UNSUPPORTED. A sequence with
+ *              more rows than max_q_len is skipped and sets bit 16 of the
+ *              device error word (rejected in validating mode).
+ *   split_tokens / max_splits / part_out / part_lse: as in pa_decode, with
+ *              rows in place of sequences (part_out [num_q_rows, num_q_heads,
+ *              max_splits, head_dim]); split mode also writes each row's
+ *              attended length to row_lens (int32 [num_q_rows]), then
+ *              pa_decode_splitk_reduce(part_out, part_lse, row_lens,
+ *              num_q_rows, ...) writes out.
+ *   out        bf16 [num_q_rows, num_q_heads, head_dim] (one split).
+ * Other arguments, layouts and errors as pa_decode. */
+pa_status pa_decode_multi(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          const int32_t* context_lens, const int32_t* q_start, int32_t num_seqs,
+                          int32_t num_q_rows, int32_t max_q_len, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                          int32_t num_blocks, float scale, int32_t split_tokens,
+                          int32_t max_splits, float* part_out, float* part_lse,
+                          int32_t* row_lens, void* out, void* stream);
+
 /* ------------------------------------------------------------------------
  * Prefix cache with copy-on-write (host side) and the block copy (device).
  *

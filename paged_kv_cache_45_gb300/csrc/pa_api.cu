@@ -165,7 +165,8 @@ extern "C" int64_t pa_kv_bytes_per_token(int32_t num_layers, int32_t num_kv_head
 extern "C" pa_status pa_last_device_error(int32_t* code) {
   if (!code) return PA_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
-  const unsigned int v = pa::take_decode_errors() | pa::take_balanced_errors();
+  const unsigned int v =
+      pa::take_decode_errors() | pa::take_balanced_errors() | pa::take_multi_errors();
   *code = (int32_t)v;
   return v ? PA_ERR_DEVICE : PA_OK;
 }

@@ -17,6 +17,7 @@ enum : unsigned int {
   kErrWaitEmpty = 2u,  // the loader waited too long for a free stage
   kErrDrain = 4u,      // the loader could not confirm its copies had landed
   kErrSelfTest = 8u,   // pa_selftest_wait_timeout's wait ran out, as intended
+  kErrShape = 16u,     // a sequence brought more query tokens than the launch was sized for
 };
 
 // A wait that runs this long is treated as lost and reported (≈1 s).

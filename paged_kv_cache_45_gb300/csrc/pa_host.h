@@ -59,5 +59,6 @@ pa_status prepare_kernel(const void* func, int threads, int smem_bytes, int* blo
 // Reads and clears a translation unit's device error word (synchronous).
 unsigned int take_decode_errors();
 unsigned int take_balanced_errors();
+unsigned int take_multi_errors();
 
 }  // namespace pa
