@@ -258,11 +258,13 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = {
-    "balanced_decode_kernel": ("pa_decode_balanced.cu", "pa_tile.cuh", "pa_device.cuh"),
-    "balanced_decode_kernel[e4m3]": ("pa_decode_balanced.cu", "pa_tile.cuh", "pa_device.cuh"),
-    "paged_decode_kernel": ("pa_decode.cu", "pa_tile.cuh", "pa_device.cuh"),
-    "multi_decode_kernel": ("pa_decode_multi.cu", "pa_tile.cuh", "pa_device.cuh"),
+KERNEL_SOURCES = {   # the files whose change invalidates a kernel's recorded DRAM traffic
+    "balanced_decode_kernel": ("pa_decode_balanced.cu", "pa_tile.cuh", "pa_device.cuh",
+                               "pa_api.cu"),
+    "balanced_decode_kernel[e4m3]": ("pa_decode_balanced.cu", "pa_tile.cuh", "pa_device.cuh",
+                                     "pa_api.cu"),
+    "paged_decode_kernel": ("pa_decode.cu", "pa_tile.cuh", "pa_device.cuh", "pa_api.cu"),
+    "multi_decode_kernel": ("pa_decode_multi.cu", "pa_tile.cuh", "pa_device.cuh", "pa_api.cu"),
 }
 
 

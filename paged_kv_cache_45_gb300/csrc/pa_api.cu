@@ -91,9 +91,15 @@ bool make_cache_map(CUtensorMap* map, const void* base, int hkv, int d, long lon
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt =
       elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  // L2 fetches grow to 256 B only where one (token, KV head) row spans 256 B;
+  // a 128-byte row (e4m3 at head_dim 128, bf16 at 64) would drag in its
+  // neighbour head's row, which another block reads at another time.
+  const CUtensorMapL2promotion promo = (long long)d * elem_bytes >= 256
+                                           ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                           : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
   CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
