@@ -97,6 +97,22 @@ bool make_cache_map(CUtensorMap* map, const void* base, int hkv, int d, long lon
   const CUtensorMapL2promotion promo = (long long)d * elem_bytes >= 256
                                            ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
                                            : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
+  if ((long long)d * elem_bytes == 256 && box_rows >= 16) {
+    // 3-D view (64 columns, rows, 128-byte column halves of all heads): one
+    // box {64, box_rows, 2} lands both halves of a (token range, head) tile in
+    // the [half][row] shared-memory layout the 2-D boxes produce, so a tile
+    // costs one TMA instruction per K or V instead of two. (The halves' stride,
+    // 128 B, is below the rows' stride.)
+    cuuint64_t dims3[3] = {(cuuint64_t)(128 / elem_bytes), (cuuint64_t)rows,
+                           (cuuint64_t)hkv * d * elem_bytes / 128};
+    cuuint64_t strides3[2] = {(cuuint64_t)hkv * d * elem_bytes, 128};
+    cuuint32_t box3[3] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)box_rows, 2};
+    cuuint32_t estr3[3] = {1, 1, 1};
+    CUresult r = enc(map, dt, 3, const_cast<void*>(base), dims3, strides3, box3, estr3,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+  }
   CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -27,10 +27,12 @@ bool validating();
 // Maps the last launch error to a status, clearing it.
 pa_status launch_status();
 
-// 2-D tensor map over a cache viewed as [rows = num_blocks*block_size,
+// Tensor map over a cache viewed as [rows = num_blocks*block_size,
 // cols = num_kv_heads*head_dim] elements of elem_bytes (2: bf16, 1: e4m3
-// bytes), box {128 bytes of columns, box_rows rows}, 128-byte swizzle, zero
-// fill out of bounds.
+// bytes), 128-byte swizzle, zero fill out of bounds. 2-D with box {128 bytes
+// of columns, box_rows rows}; for 256-byte head rows and box_rows >= 16, 3-D
+// (128-byte columns, rows, column halves) with box {128 bytes, box_rows, 2},
+// which issue_tile loads with one instruction per K or V tile.
 bool make_cache_map(CUtensorMap* map, const void* base, int num_kv_heads, int head_dim,
                     long long rows, int box_rows, int elem_bytes = 2);
 

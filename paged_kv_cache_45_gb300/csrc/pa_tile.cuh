@@ -568,11 +568,18 @@ __device__ __forceinline__ void issue_tile(uint32_t sK, uint64_t* full, const CU
       const int row = row_of(0, (unsigned)(t0 & (bs - 1)));
       if (lane == 0) {
         mbar_arrive_expect_tx(full, Gm::kStageBytes);
+        if constexpr (Gm::kHalves == 2) {
+          // 256-byte rows: the map is 3-D (64 columns, rows, column halves),
+          // one box carries both halves of the tile
+          tma_load_3d(sK, tmap_k, 0, row, 2 * kvh, full);
+          tma_load_3d(sV, tmap_v, 0, row, 2 * kvh, full);
+        } else {
 #pragma unroll
-        for (int h = 0; h < Gm::kHalves; ++h) {
-          const int x = kvh * D + h * Gm::kBoxCols;
-          tma_load_2d(sK + h * Gm::kHalfStride, tmap_k, x, row, full);
-          tma_load_2d(sV + h * Gm::kHalfStride, tmap_v, x, row, full);
+          for (int h = 0; h < Gm::kHalves; ++h) {
+            const int x = kvh * D + h * Gm::kBoxCols;
+            tma_load_2d(sK + h * Gm::kHalfStride, tmap_k, x, row, full);
+            tma_load_2d(sV + h * Gm::kHalfStride, tmap_v, x, row, full);
+          }
         }
       }
     } else if (2 * bs == TT) {
