@@ -70,6 +70,9 @@ def parse_args():
     ap.add_argument("--step", choices=["fused", "separate"], default="fused",
                     help="fused: pa_append_decode (append + balanced decode in one launch); "
                          "separate: pa_kv_append, then the decode of --schedule")
+    ap.add_argument("--multi-schedule", choices=["split", "balanced"], default="split",
+                    help="spec workload: pa_decode_multi over context splits (--split, default "
+                         "1024) + reduce, or pa_decode_multi_balanced")
     ap.add_argument("--split", type=int, default=-1,
                     help="split_tokens for --schedule split (-1: planned; 0: no split)")
     ap.add_argument("--seed", type=int, default=0)
@@ -259,12 +262,14 @@ def measured_hbm_peak():
 
 
 KERNEL_SOURCES = {   # the files whose change invalidates a kernel's recorded DRAM traffic
-    "balanced_decode_kernel": ("pa_decode_balanced.cu", "pa_tile.cuh", "pa_device.cuh",
-                               "pa_api.cu"),
-    "balanced_decode_kernel[e4m3]": ("pa_decode_balanced.cu", "pa_tile.cuh", "pa_device.cuh",
-                                     "pa_api.cu"),
+    "balanced_decode_kernel": ("pa_decode_balanced.cu", "pa_balance.cuh", "pa_tile.cuh",
+                               "pa_device.cuh", "pa_api.cu"),
+    "balanced_decode_kernel[e4m3]": ("pa_decode_balanced.cu", "pa_balance.cuh", "pa_tile.cuh",
+                                     "pa_device.cuh", "pa_api.cu"),
     "paged_decode_kernel": ("pa_decode.cu", "pa_tile.cuh", "pa_device.cuh", "pa_api.cu"),
     "multi_decode_kernel": ("pa_decode_multi.cu", "pa_tile.cuh", "pa_device.cuh", "pa_api.cu"),
+    "balanced_multi_kernel": ("pa_decode_multi.cu", "pa_balance.cuh", "pa_tile.cuh",
+                              "pa_device.cuh", "pa_api.cu"),
 }
 
 
@@ -275,6 +280,11 @@ class MultiWorkspace:
         import torch
         R = int(steps.items[0]["q"].shape[0])
         self.balanced = False
+        self.multi_balanced = split < 0
+        split = max(split, 0)
+        self.scratch = torch.zeros(b.pa_decode_multi_balanced_workspace_bytes(
+            steps.batch, steps.hkv, steps.d), dtype=torch.uint8, device=device) \
+            if self.multi_balanced else None
         self.split_tokens = split
         self.max_splits = b.pa_decode_num_splits(steps.max_context, split) if split else 0
         self.out = torch.empty((R, steps.hq, steps.d), dtype=torch.bfloat16, device=device)
@@ -352,8 +362,9 @@ def run_gpu(args):
     if steps.fp8 and args.schedule != "balanced":
         raise SystemExit("--kv-dtype fp8 runs the balanced schedule only")
     sms = b.num_sms(local)
-    if steps.multi:
-        split = max(args.split, 0)
+    if steps.multi:   # -1: the balanced schedule (pa_decode_multi_balanced)
+        split = -1 if args.multi_schedule == "balanced" else (args.split if args.split >= 0
+                                                              else 1024)
     elif args.schedule == "balanced":
         split = b.BALANCED
     elif args.split >= 0:
@@ -387,10 +398,15 @@ def run_gpu(args):
             b.pa_kv_append(dv["k_new"], dv["v_new"], dv["slots"], steps.k_cache, steps.v_cache)
             if ev is not None:
                 ev[1].record(stream)
-            b.pa_decode_multi(dv["q"], steps.k_cache, steps.v_cache, dv["tables"], dv["lens"],
-                              dv["qstart"], steps.max_q_len, steps.scale, ws.out,
-                              ws.split_tokens, ws.max_splits, ws.part_out, ws.part_lse,
-                              ws.row_lens)
+            if ws.multi_balanced:
+                b.pa_decode_multi_balanced(dv["q"], steps.k_cache, steps.v_cache, dv["tables"],
+                                           dv["lens"], dv["qstart"], steps.max_q_len,
+                                           steps.scale, ws.scratch, ws.out)
+            else:
+                b.pa_decode_multi(dv["q"], steps.k_cache, steps.v_cache, dv["tables"],
+                                  dv["lens"], dv["qstart"], steps.max_q_len, steps.scale,
+                                  ws.out, ws.split_tokens, ws.max_splits, ws.part_out,
+                                  ws.part_lse, ws.row_lens)
             if ev is not None:
                 ev[2].record(stream)
             if ws.split_tokens:
@@ -540,7 +556,8 @@ def run_gpu(args):
     dec_gbs_rank0 = dec_bytes / dec_s / 1e9
     kv_tokens_per_launch = kv_tokens / KI
     kernel = ("balanced_decode_kernel" + ("[e4m3]" if steps.fp8 else "")) if ws.balanced \
-        else ("multi_decode_kernel" if steps.multi else "paged_decode_kernel")
+        else (("balanced_multi_kernel" if ws.multi_balanced else "multi_decode_kernel")
+              if steps.multi else "paged_decode_kernel")
     traffic = traffic_per_launch(kernel, kv_tokens_per_launch)
     clocks = sampler.summary() if sampler else None
     line = {
@@ -559,8 +576,10 @@ def run_gpu(args):
         "config": {"workload": describe(args.workload, args.batch) +
                    (" (e4m3 KV pool, per-KV-head scales)" if steps.fp8 else ""),
                    "schedule": "balanced" if ws.balanced else
-                   (f"multi (one block per KV head, split, sequence; split_tokens="
-                    f"{ws.split_tokens})" if steps.multi else
+                   (("multi, balanced persistent (pa_decode_multi_balanced)"
+                     if ws.multi_balanced else
+                     f"multi (one block per KV head, split, sequence; split_tokens="
+                     f"{ws.split_tokens})") if steps.multi else
                     f"split (pa_decode split_tokens={ws.split_tokens} + pa_decode_splitk_reduce)"),
                    "step": "fused: pa_append_decode, one launch" if fused else
                    "separate: pa_kv_append + decode launches",

@@ -345,6 +345,27 @@ pa_status pa_decode_multi(const void* q, const void* k_cache, const void* v_cach
                           int32_t max_splits, float* part_out, float* part_lse,
                           int32_t* row_lens, void* out, void* stream);
 
+/* pa_decode_multi on the work-balanced persistent schedule of
+ * pa_decode_balanced: one launch, every block the same number of K/V tiles,
+ * units cut by a block's range merged in the kernel by log-sum-exp (no
+ * reduce launch). workspace: caller-owned device memory of at least
+ * pa_decode_multi_balanced_workspace_bytes(num_seqs, num_kv_heads, head_dim)
+ * bytes, 256-byte aligned, zero-filled before its first use and left reusable
+ * (too small: PA_ERR_WORKSPACE); calls sharing a workspace must not overlap.
+ * Other arguments, limits and errors as pa_decode_multi. */
+pa_status pa_decode_multi_balanced(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, const int32_t* q_start,
+                                   int32_t num_seqs, int32_t num_q_rows, int32_t max_q_len,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int32_t num_blocks, float scale,
+                                   void* workspace, size_t workspace_bytes, void* out,
+                                   void* stream);
+
+/* Workspace bytes pa_decode_multi_balanced needs on the current device. */
+size_t pa_decode_multi_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads,
+                                                int32_t head_dim);
+
 /* ------------------------------------------------------------------------
  * Prefix cache with copy-on-write (host side) and the block copy (device).
  *

@@ -52,6 +52,9 @@ _SIGS = {
     "pa_selftest_wait_timeout": (_i32, [_i32, _p]),
     "pa_decode_multi": (_i32, [_p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32,
                                _i32, _i32, _f32, _i32, _i32, _p, _p, _p, _p, _p]),
+    "pa_decode_multi_balanced": (_i32, [_p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32,
+                                        _i32, _i32, _i32, _i32, _f32, _p, _sz, _p, _p]),
+    "pa_decode_multi_balanced_workspace_bytes": (_sz, [_i32, _i32, _i32]),
     "pa_prefix_cache_create": (_i32, [_i32, _i32, _p]),
     "pa_prefix_cache_destroy": (None, [_p]),
     "pa_prefix_admit": (_i32, [_p, _p, _i32, _p, _p]),
@@ -197,13 +200,51 @@ def pa_decode_multi(q, k_cache, v_cache, block_tables, context_lens, q_start, ma
         _stream(stream)))
 
 
+def pa_decode_multi_balanced(q, k_cache, v_cache, block_tables, context_lens, q_start,
+                             max_q_len: int, scale: float, workspace, out, stream=None) -> None:
+    """pa_decode_multi on the balanced persistent schedule; ``workspace`` a
+    zero-filled uint8 CUDA tensor of ``pa_decode_multi_balanced_workspace_bytes``."""
+    R, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    B = context_lens.numel()
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shapes do not match q")
+    if tuple(out.shape) != (R, hq, d) or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("out / block_tables shape mismatch")
+    if q_start.numel() != B + 1:
+        raise ValueError("q_start must have num_seqs + 1 entries")
+    _check("pa_decode_multi_balanced", _lib.pa_decode_multi_balanced(
+        _t(q, torch.bfloat16, "q"), _t(k_cache, torch.bfloat16, "k_cache"),
+        _t(v_cache, torch.bfloat16, "v_cache"), _t(block_tables, torch.int32, "block_tables"),
+        int(block_tables.shape[1]), _t(context_lens, torch.int32, "context_lens"),
+        _t(q_start, torch.int32, "q_start"), B, R, int(max_q_len), hq, hkv, d, bs, nb,
+        float(scale), _t(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _t(out, torch.bfloat16, "out"), _stream(stream)))
+
+
+def pa_decode_multi_balanced_workspace_bytes(num_seqs: int, num_kv_heads: int,
+                                             head_dim: int) -> int:
+    return int(_lib.pa_decode_multi_balanced_workspace_bytes(int(num_seqs), int(num_kv_heads),
+                                                             int(head_dim)))
+
+
+BALANCED_MULTI = -1
+
+
 def decode_multi(q, k_cache, v_cache, block_tables, context_lens, q_start, max_q_len: int,
                  scale: float, split_tokens: int = 0, max_context: int | None = None,
                  out=None, stream=None):
-    """pa_decode_multi with its split-mode buffers and the reduce; returns out."""
+    """pa_decode_multi with its split-mode buffers and the reduce (or, with
+    ``split_tokens == BALANCED_MULTI``, pa_decode_multi_balanced); returns out."""
     R, hq, d = q.shape
     if out is None:
         out = torch.empty((R, hq, d), dtype=torch.bfloat16, device=q.device)
+    if split_tokens == BALANCED_MULTI:
+        ws = torch.zeros(pa_decode_multi_balanced_workspace_bytes(
+            context_lens.numel(), k_cache.shape[2], d), dtype=torch.uint8, device=q.device)
+        pa_decode_multi_balanced(q, k_cache, v_cache, block_tables, context_lens, q_start,
+                                 max_q_len, scale, ws, out, stream=stream)
+        return out
     if split_tokens <= 0:
         pa_decode_multi(q, k_cache, v_cache, block_tables, context_lens, q_start, max_q_len,
                         scale, out, stream=stream)

@@ -36,6 +36,7 @@
 
 #include "pa_device.cuh"
 #include "pa_host.h"
+#include "pa_balance.cuh"
 #include "pa_tile.cuh"
 #include "pagedkv.h"
 
@@ -116,50 +117,10 @@ struct BalSmem {
   static constexpr int bytes(int B) { return kScanOff + (B + 1) * 4 + 1024; }
 };
 
-template <int TT>
-__device__ __forceinline__ int tiles_of(int ctx, int cap) {
-  ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-  return (ctx + TT - 1) / TT;
-}
-
-// Largest worker whose range [w N / W, (w + 1) N / W) starts at or before tile g.
-__device__ __forceinline__ int owner_of(long long g, long long N, long long W) {
-  return (int)(((g + 1) * W - 1) / N);
-}
-
 // Column of element d of head row h in the merge buffer: XOR-swizzled in
 // groups of 8 floats so the 4 head rows one store instruction touches fall
 // in 4 different bank groups (8-float groups stay contiguous for float4).
 __device__ __forceinline__ int merge_col(int h, int d) { return d ^ ((h >> 1) << 3); }
-
-// Position (sequence, KV head, tile) in the unit list.
-struct Cursor {
-  int b, kvh, t, n;
-
-  // Place the cursor on global tile g (g < N).
-  __device__ __forceinline__ void seek(long long g, const int* S, int B, int hkv) {
-    int lo = 0, hi = B - 1;  // largest b with hkv * S[b] <= g
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if ((long long)hkv * S[mid] <= g) lo = mid; else hi = mid - 1;
-    }
-    b = lo;
-    n = S[b + 1] - S[b];
-    const long long r = g - (long long)hkv * S[b];
-    kvh = (int)(r / n);
-    t = (int)(r - (long long)kvh * n);
-  }
-
-  // Move to the first tile of the next unit.
-  __device__ __forceinline__ void next_unit(const int* S, int B, int hkv) {
-    t = 0;
-    if (++kvh == hkv) {
-      kvh = 0;
-      do { ++b; } while (b < B && S[b + 1] == S[b]);
-      n = b < B ? S[b + 1] - S[b] : 0;
-    }
-  }
-};
 
 // Four e4m3 codes (one u32, low byte first) of four bf16 values / scale.
 __device__ __forceinline__ uint32_t quantize4_e4m3(uint2 v, float scale) {
@@ -229,29 +190,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
   }
 
   // ---- S[b] = tiles of the sequences before b (exclusive prefix sum) -------
-  {
-    const int tid = threadIdx.x;
-    const int seg = (B + kThreads - 1) / kThreads;
-    const int lo = min(tid * seg, B), hi = min(lo + seg, B);
-    int sum = 0;
-    for (int i = lo; i < hi; ++i) sum += tiles_of<TT>(p.context_lens[i], cap);
-    int incl = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += warp_tot[w];
-    int run = base + incl - sum;
-    for (int i = lo; i < hi; ++i) {
-      S[i] = run;
-      run += tiles_of<TT>(p.context_lens[i], cap);
-    }
-    if (tid == kThreads - 1) S[B] = base + incl;
-  }
+  tile_prefix_sum<TT, kThreads>(S, warp_tot, p.context_lens, B, cap);
   fence_mbar_init();
   __syncthreads();
 

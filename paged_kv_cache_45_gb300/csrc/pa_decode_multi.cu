@@ -17,16 +17,24 @@
 // split into them (a tile's stage is released when all NC consumer warps have
 // read it), so each K/V byte is still read from HBM once per block while the
 // tensor-core work grows with n_b. Per-column causal limits mask the scores
-// (attend_tile_causal); no merge between warps is needed. Outputs go through
+// (attend_tile_causal_nt); no merge between warps is needed. Outputs go through
 // shared memory so that every row is written with coalesced stores: bf16 rows
 // (one split) or fp32 partials + natural-log LSEs for pa_decode_splitk_reduce,
 // whose per-row context lengths this kernel writes to row_lens.
+//
+// balanced_multi_kernel runs the same column-warp tile math on the
+// work-balanced persistent schedule of pa_balance.cuh (one launch, every block
+// the same number of tiles, no tail): a unit is (sequence, KV head) over the
+// sequence's context, each of its tiles folded by every column warp; a unit
+// cut by a block range leaves per-column records that the block publishing
+// the last of them merges by log-sum-exp, column warp by column warp.
 
 #include <math.h>
 
 #include <cstring>
 #include <vector>
 
+#include "pa_balance.cuh"
 #include "pa_device.cuh"
 #include "pa_host.h"
 #include "pa_tile.cuh"
@@ -187,7 +195,8 @@ __global__ void __launch_bounds__((kMaxColumnWarps + 1) * 32, 2)
 
   // -------------------------------------------------------------- consumers
   // B operand of Q^T: this lane's column is 8 * warp + lane / 4
-  uint32_t qf[D / 16][2];
+  uint32_t qfs[1][D / 16][2];
+  auto& qf = qfs[0];
   {
     const int c = 8 * warp + (lane >> 2);
     const int i = c / G;
@@ -208,7 +217,8 @@ __global__ void __launch_bounds__((kMaxColumnWarps + 1) * 32, 2)
   const int ca = 8 * warp + tk;
   const int lim_a = ca / G < n ? ctx - n + ca / G : -1;
   const int lim_b = (ca + 1) / G < n ? ctx - n + (ca + 1) / G : -1;
-  AttnState<D> st;
+  AttnState<D> sts[1];
+  AttnState<D>& st = sts[0];
   st.reset();
   bool aborted = false;
   for (int i = 0; i < n_tiles; ++i) {
@@ -226,9 +236,10 @@ __global__ void __launch_bounds__((kMaxColumnWarps + 1) * 32, 2)
     const uint32_t sK = ring + stage * Gm::kStageBytes;
     const int t0 = t_begin + i * kTile;
     const int valid = min(kTile, t_end - t0);
-    const int va = max(0, min(valid, lim_a - t0 + 1));
-    const int vb = max(0, min(valid, lim_b - t0 + 1));
-    attend_tile_causal<D>(st, sK, sK + Gm::kKVBytes, qf, valid, va, vb, p.scale_log2, lane);
+    const int va[1] = {max(0, min(valid, lim_a - t0 + 1))};
+    const int vb[1] = {max(0, min(valid, lim_b - t0 + 1))};
+    attend_tile_causal_nt<D, 1>(sts, sK, sK + Gm::kKVBytes, qfs, valid, va, vb, p.scale_log2,
+                                lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
   }
@@ -300,6 +311,361 @@ pa_status launch_multi(const CUtensorMap& mk, const CUtensorMap& mv, const Multi
   dim3 grid(num_kv_heads, prm.split_tokens > 0 ? prm.max_splits : 1, B);
   kern<<<grid, threads, L::kAlloc, stream>>>(mk, mv, prm);
   return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// the work-balanced persistent schedule
+// ---------------------------------------------------------------------------
+
+constexpr int kMaxCols = kMaxColumnWarps * 8;  // (token, head) columns of a unit
+constexpr int kMultiBlocksPerSM = 4;           // the most a launch uses (workspace sizing)
+
+struct BalMultiParams {
+  const __nv_bfloat16* q;      // [R, Hq, D]
+  const int32_t* q_start;      // [B + 1]
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  __nv_bfloat16* out;          // [R, Hq, D]
+  int* counters;               // [B * Hkv * kMaxColumnWarps], zero between launches
+  float* rec_lse;              // [blocks][2][kMaxCols], base 2
+  float* rec_o;                // [blocks][2][kMaxCols][D]
+  TileSrc src;
+  int max_blocks;
+  int num_seqs;
+  int num_q_heads;
+  int group;
+  float scale_log2;
+};
+
+template <int D, int NC, int NT>
+struct BalMultiSmem {
+  static constexpr int kStageBytes = TileGeom<D>::kStageBytes;
+  static constexpr int kRingBytes = kMultiStages * kStageBytes;
+  static constexpr int kOutOff = kRingBytes;                        // [NC][8 NT][D] fp32 staging
+  static constexpr int kBarOff = kOutOff + NC * 8 * NT * D * 4;     // full, empty
+  static constexpr int kMiscOff = kBarOff + 2 * kMultiStages * 8;   // abort flag
+  static constexpr int kTotOff = kMiscOff + 16;                     // warp totals [NC + 1]
+  static constexpr int kScanOff = kTotOff + ((NC + 1) * 4 + 15) / 16 * 16;  // S[B + 1]
+  static constexpr int bytes(int B) { return kScanOff + (B + 1) * 4 + 1024; }
+};
+
+// NC column warps of 8 columns each. (Two groups of 8 columns a warp, the
+// K/V fragments read once for both, measured slower on the speculative-verify
+// batch: 0.556 against 0.542 ms; the per-warp state stays one group.)
+template <int D, bool kTma, int NC, int BPS>
+__global__ void __launch_bounds__((NC + 1) * 32, BPS)
+    balanced_multi_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v, const BalMultiParams p) {
+  constexpr int NT = 1;  // groups of 8 columns per warp
+  using L = BalMultiSmem<D, NC, NT>;
+  constexpr int CW = 8 * NT;
+  using Gm = TileGeom<D>;
+  constexpr int STAGES = kMultiStages;
+  constexpr int kThreads = (NC + 1) * 32;
+  constexpr int TT = kTile;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* stage_out = reinterpret_cast<float*>(smem + L::kOutOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* empty = full + STAGES;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
+  int* warp_tot = reinterpret_cast<int*>(smem + L::kTotOff);
+  int* S = reinterpret_cast<int*>(smem + L::kScanOff);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int B = p.num_seqs;
+  const int hkv = p.src.num_kv_heads;
+  const int G = p.group;
+  const int cap = p.max_blocks << p.src.log2_bs;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], kTma ? 1 : 32);
+      mbar_init(&empty[s], NC);
+    }
+    *abort_flag = 0;
+  }
+  // a sequence with query rows holds its context's tiles; one without, none
+  tile_prefix_sum_of<kThreads>(S, warp_tot, B, [&](int i) {
+    return p.q_start[i + 1] > p.q_start[i] ? tiles_of<TT>(p.context_lens[i], cap) : 0;
+  });
+  fence_mbar_init();
+  __syncthreads();
+
+  // query rows of sequences with no context: zero rows
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    if (S[b + 1] != S[b]) continue;
+    const int r0 = p.q_start[b], n = p.q_start[b + 1] - r0;
+    uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)r0 * p.num_q_heads * D);
+    for (int i = threadIdx.x; i < n * p.num_q_heads * D / 8; i += kThreads)
+      dst[i] = make_uint4(0, 0, 0, 0);
+  }
+
+  const long long N = (long long)S[B] * hkv;
+  const long long W = min((long long)gridDim.x, N);
+  const int c = blockIdx.x;
+  if (c >= W) return;
+  const long long g0 = (long long)c * N / W, g1 = (long long)(c + 1) * N / W;
+  const int count = (int)(g1 - g0);
+  const uint32_t ring = smem_u32(smem);
+
+  if (warp == NC) {
+    // ------------------------------------------------------------ loader warp
+    if (kTma && lane == 0) {
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+    }
+    Cursor ic;
+    ic.seek(g0, S, B, hkv);
+    int ic_ctx = 0, ic_nblk = 0, ic_b = -1;
+    int tc_b = -1, tc_base = 0, tc_val = -1;
+    int issued = 0;
+    for (int j = 0; j < count; ++j) {
+      if (__any_sync(0xffffffffu, *abort_flag)) break;
+      if (ic.b != ic_b) {
+        ic_b = ic.b;
+        ic_ctx = min(max(p.context_lens[ic.b], 0), cap);
+        ic_nblk = (ic_ctx + p.src.block_size - 1) >> p.src.log2_bs;
+      }
+      const int stage = j % STAGES;
+      if (j >= STAGES &&
+          !__all_sync(0xffffffffu, mbar_wait(&empty[stage], ((j / STAGES) - 1) & 1))) {
+        if (lane == 0) report(kErrWaitEmpty);
+        *abort_flag = 1;
+        break;
+      }
+      const int t0 = ic.t * TT;
+      const int blk_first = t0 >> p.src.log2_bs;
+      const int blk_last = (t0 + TT - 1) >> p.src.log2_bs;
+      if (tc_b != ic.b || blk_first < tc_base || blk_last >= tc_base + 32) {  // warp-uniform
+        tc_b = ic.b;
+        tc_base = blk_first;
+        const int idx = tc_base + lane;
+        tc_val = idx < ic_nblk ? p.block_tables[(size_t)ic.b * p.max_blocks + idx] : -1;
+      }
+      issue_tile<D, kTma>(ring + stage * Gm::kStageBytes, &full[stage], &tmap_k, &tmap_v, p.src,
+                          ic.kvh, t0, ic_ctx, ic_nblk, tc_base, tc_val, lane);
+      ++issued;
+      if (++ic.t == ic.n) ic.next_unit(S, B, hkv);
+    }
+    const int first = issued > STAGES ? issued - STAGES : 0;
+    for (int j = first; j < issued; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[j % STAGES], (j / STAGES) & 1))) {
+        if (lane == 0) report(kErrDrain);
+        break;
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int tk = 2 * (lane & 3);
+  const int r0 = lane >> 2;
+  float* buf = stage_out + (size_t)warp * CW * D;
+  Cursor uc;
+  uc.seek(g0, S, B, hkv);
+  uint32_t qf[NT][D / 16][2];
+  AttnState<D> st[NT];
+  int lim_a[NT], lim_b[NT];
+  int j0 = 0;
+  while (j0 < count) {
+    const int b = uc.b, kvh = uc.kvh;
+    const int m = min(uc.n - uc.t, count - j0);  // this block's tiles of the unit
+    const int ctx = min(max(__ldg(p.context_lens + b), 0), cap);
+    const int row0 = __ldg(p.q_start + b);
+    const int n = __ldg(p.q_start + b + 1) - row0;
+    if (n * G > NC * CW && warp == 0 && lane == 0) report(kErrShape);
+#pragma unroll
+    for (int g8 = 0; g8 < NT; ++g8) {
+      // B operand of Q^T for group g8: this lane's column is CW warp + 8 g8 + lane / 4
+      const int cq = CW * warp + 8 * g8 + (lane >> 2);
+      const int i = cq / G;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) qf[g8][ks][0] = qf[g8][ks][1] = 0u;
+      if (i < n) {
+        const unsigned int* rowp = reinterpret_cast<const unsigned int*>(
+            p.q + ((size_t)(row0 + i) * p.num_q_heads + kvh * G + cq % G) * D + 2 * (lane & 3));
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          qf[g8][ks][0] = __ldg(rowp + ks * 8);
+          qf[g8][ks][1] = __ldg(rowp + ks * 8 + 4);
+        }
+      }
+      const int ca = CW * warp + 8 * g8 + tk;
+      lim_a[g8] = ca / G < n ? ctx - n + ca / G : -1;
+      lim_b[g8] = (ca + 1) / G < n ? ctx - n + (ca + 1) / G : -1;
+      st[g8].reset();
+    }
+    for (int j = j0; j < j0 + m; ++j) {  // every column warp folds every tile
+      if (__any_sync(0xffffffffu, *abort_flag)) break;
+      const int stage = j % STAGES;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], (j / STAGES) & 1))) {
+        if (lane == 0) report(kErrWaitFull);
+        *abort_flag = 1;
+        break;
+      }
+      const uint32_t sK = ring + stage * Gm::kStageBytes;
+      const int t0 = (uc.t + (j - j0)) * TT;
+      const int valid = min(TT, ctx - t0);
+      int va[NT], vb[NT];
+#pragma unroll
+      for (int g8 = 0; g8 < NT; ++g8) {
+        va[g8] = max(0, min(valid, lim_a[g8] - t0 + 1));
+        vb[g8] = max(0, min(valid, lim_b[g8] - t0 + 1));
+      }
+      attend_tile_causal_nt<D, NT>(st, sK, sK + Gm::kKVBytes, qf, valid, va, vb, p.scale_log2,
+                                   lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+    if (__any_sync(0xffffffffu, *abort_flag)) break;
+
+    // ---- this warp's columns: rows, or records of a unit cut by a range -----
+    const int ncols = min(CW, n * G - CW * warp);  // valid columns of this warp
+    if (ncols > 0) {
+      const long long U = (long long)hkv * S[b] + (long long)kvh * uc.n;
+      const int c0 = owner_of(U, N, W), c1 = owner_of(U + uc.n - 1, N, W);
+      const bool cut = c0 != c1;
+      float la[NT], lb[NT];  // base-2 log-sum-exp of this lane's columns (-inf: no token)
+#pragma unroll
+      for (int g8 = 0; g8 < NT; ++g8) {
+        st[g8].reduce_l();
+        const float i0 = st[g8].l0 > 0.f ? 1.f / st[g8].l0 : 0.f;
+        const float i1 = st[g8].l1 > 0.f ? 1.f / st[g8].l1 : 0.f;
+        const int ja = 8 * g8 + tk, jb = ja + 1;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          const int d0 = mt * 16 + r0;
+          buf[ja * D + out_col(ja, d0)] = st[g8].o[mt][0] * i0;
+          buf[jb * D + out_col(jb, d0)] = st[g8].o[mt][1] * i1;
+          buf[ja * D + out_col(ja, d0 + 8)] = st[g8].o[mt][2] * i0;
+          buf[jb * D + out_col(jb, d0 + 8)] = st[g8].o[mt][3] * i1;
+        }
+        la[g8] = st[g8].l0 > 0.f ? st[g8].m0 + log2f(st[g8].l0) : -INFINITY;
+        lb[g8] = st[g8].l1 > 0.f ? st[g8].m1 + log2f(st[g8].l1) : -INFINITY;
+      }
+      __syncwarp();
+      const int rec = 2 * c + (c == c0 ? 1 : 0);
+      for (int jc = 0; jc < ncols; ++jc) {
+        const int col = CW * warp + jc;
+        const size_t r = (size_t)(row0 + col / G) * p.num_q_heads + kvh * G + col % G;
+        float mine = -INFINITY;  // this lane's candidate for column jc's lse
+#pragma unroll
+        for (int g8 = 0; g8 < NT; ++g8)
+          if ((jc >> 3) == g8) mine = (jc & 1) ? lb[g8] : la[g8];
+        const float lse = __shfl_sync(0xffffffffu, mine, (jc >> 1) & 3);
+        if (!cut) {
+          for (int d4 = lane; d4 < D / 4; d4 += 32) {
+            const float4 v = *reinterpret_cast<const float4*>(buf + jc * D + out_col(jc, 4 * d4));
+            uint2 pk;
+            pk.x = pack_bf16x2(v.x, v.y);
+            pk.y = pack_bf16x2(v.z, v.w);
+            *reinterpret_cast<uint2*>(p.out + r * D + 4 * d4) = pk;
+          }
+        } else {
+          float* dst = p.rec_o + ((size_t)rec * kMaxCols + col) * D;
+          for (int d4 = lane; d4 < D / 4; d4 += 32)
+            *reinterpret_cast<float4*>(dst + 4 * d4) =
+                *reinterpret_cast<const float4*>(buf + jc * D + out_col(jc, 4 * d4));
+          if (lane == 0) p.rec_lse[rec * kMaxCols + col] = lse;
+        }
+      }
+      if (cut) {
+        // publish: the warp's record stores, then one lane's GPU-scope fence
+        // and ticket (cumulative over what the warp wrote)
+        __syncwarp();
+        int ticket = 0;
+        int* counter = p.counters + ((size_t)b * hkv + kvh) * kMaxColumnWarps + warp;
+        if (lane == 0) {
+          fence_acq_rel_gpu();
+          ticket = atomicAdd(counter, 1);
+          fence_acq_rel_gpu();
+        }
+        ticket = __shfl_sync(0xffffffffu, ticket, 0);
+        if (ticket == c1 - c0) {  // the last block on the unit merges the records
+          for (int jc = 0; jc < ncols; ++jc) {
+            const int col = CW * warp + jc;
+            const size_t r = (size_t)(row0 + col / G) * p.num_q_heads + kvh * G + col % G;
+            float M = -INFINITY;
+            for (int cc = c0; cc <= c1; ++cc)
+              M = fmaxf(M, __ldcg(p.rec_lse + (2 * cc + (cc == c0 ? 1 : 0)) * kMaxCols + col));
+            for (int d4 = lane; d4 < D / 4; d4 += 32) {
+              float Wsum = 0.f;
+              float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (M != -INFINITY) {
+                for (int cc = c0; cc <= c1; ++cc) {
+                  const int rr = 2 * cc + (cc == c0 ? 1 : 0);
+                  const float wt = exp2f(__ldcg(p.rec_lse + rr * kMaxCols + col) - M);
+                  const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                      p.rec_o + ((size_t)rr * kMaxCols + col) * D + 4 * d4));
+                  Wsum += wt;
+                  acc.x += wt * v.x; acc.y += wt * v.y; acc.z += wt * v.z; acc.w += wt * v.w;
+                }
+              }
+              const float f = Wsum > 0.f ? 1.f / Wsum : 0.f;
+              uint2 pk;
+              pk.x = pack_bf16x2(acc.x * f, acc.y * f);
+              pk.y = pack_bf16x2(acc.z * f, acc.w * f);
+              *reinterpret_cast<uint2*>(p.out + r * D + 4 * d4) = pk;
+            }
+          }
+          if (lane == 0) *counter = 0;
+        }
+      }
+      __syncwarp();  // the staging buffer is read before the next unit's writes
+    }
+    j0 += m;
+    uc.next_unit(S, B, hkv);
+  }
+}
+
+struct MultiWsLayout {
+  size_t counters, rec_lse, rec_o, total;
+};
+
+MultiWsLayout multi_ws_layout(int num_seqs, int num_kv_heads, int head_dim, int blocks) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  MultiWsLayout l;
+  l.counters = 0;
+  l.rec_lse = up((size_t)num_seqs * num_kv_heads * kMaxColumnWarps * sizeof(int));
+  l.rec_o = l.rec_lse + up((size_t)blocks * 2 * kMaxCols * sizeof(float));
+  l.total = l.rec_o + up((size_t)blocks * 2 * kMaxCols * head_dim * sizeof(float));
+  return l;
+}
+
+template <int D, bool kTma, int NC, int BPS>
+pa_status launch_bal_multi(const CUtensorMap& mk, const CUtensorMap& mv, const BalMultiParams& prm,
+                           int sms, cudaStream_t stream) {
+  auto kern = balanced_multi_kernel<D, kTma, NC, BPS>;
+  const int smem = BalMultiSmem<D, NC, 1>::bytes(prm.num_seqs);
+  if (smem > 227 * 1024) return PA_ERR_UNSUPPORTED;
+  int per_sm = 0;
+  const pa_status s =
+      prepare_kernel(reinterpret_cast<const void*>(kern), (NC + 1) * 32, smem, &per_sm);
+  if (s != PA_OK) return s;
+  per_sm = per_sm > BPS ? BPS : per_sm;
+  kern<<<sms * per_sm, (NC + 1) * 32, smem, stream>>>(mk, mv, prm);
+  return launch_status();
+}
+
+// Column warps: the fewest of 1, 2, 4, 8 covering max_q_len * G columns.
+template <int D, bool kTma>
+pa_status launch_bal_multi_for(int cols, const CUtensorMap& mk, const CUtensorMap& mv,
+                               const BalMultiParams& prm, int sms, cudaStream_t stream) {
+  if (cols <= 8) return launch_bal_multi<D, kTma, 1, 4>(mk, mv, prm, sms, stream);
+  if (cols <= 16) return launch_bal_multi<D, kTma, 2, 4>(mk, mv, prm, sms, stream);
+  if (cols <= 32) return launch_bal_multi<D, kTma, 4, 4>(mk, mv, prm, sms, stream);
+  return launch_bal_multi<D, kTma, 8, 2>(mk, mv, prm, sms, stream);
+}
+
+int multi_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return sms;
 }
 
 pa_status check_q_start(const int32_t* q_start, const int32_t* context_lens, int B, int R,
@@ -404,4 +770,83 @@ extern "C" pa_status pa_decode_multi(const void* q, const void* k_cache, const v
                : launch_multi<128, false>(mk, mv, prm, nc, num_seqs, num_kv_heads, st);
   return tma ? launch_multi<64, true>(mk, mv, prm, nc, num_seqs, num_kv_heads, st)
              : launch_multi<64, false>(mk, mv, prm, nc, num_seqs, num_kv_heads, st);
+}
+
+extern "C" size_t pa_decode_multi_balanced_workspace_bytes(int32_t num_seqs,
+                                                           int32_t num_kv_heads,
+                                                           int32_t head_dim) {
+  using namespace pa;
+  const int sms = multi_sm_count();
+  if (num_seqs <= 0 || num_kv_heads <= 0 || head_dim <= 0 || sms <= 0) return 0;
+  return multi_ws_layout(num_seqs, num_kv_heads, head_dim, sms * kMultiBlocksPerSM).total;
+}
+
+extern "C" pa_status pa_decode_multi_balanced(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, const int32_t* q_start,
+    int32_t num_seqs, int32_t num_q_rows, int32_t max_q_len, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+    void* workspace, size_t workspace_bytes, void* out, void* stream) {
+  using namespace pa;
+  if (num_q_rows < 0 || max_q_len < 1) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0 || num_q_rows == 0) return PA_OK;
+  pa_status s = check_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                  context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                  block_size, num_blocks, scale, out);
+  if (s != PA_OK) return s;
+  if (!q_start) return PA_ERR_INVALID_ARG;
+  const int G = num_q_heads / num_kv_heads;
+  if ((long long)max_q_len * G > kMaxCols) return PA_ERR_UNSUPPORTED;
+  const int sms = multi_sm_count();
+  if (sms <= 0) return PA_ERR_CUDA;
+  const MultiWsLayout lay =
+      multi_ws_layout(num_seqs, num_kv_heads, head_dim, sms * kMultiBlocksPerSM);
+  if (!workspace || workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  if (validating()) {
+    s = check_tables(block_tables, max_blocks_per_seq, context_lens, num_seqs, num_blocks,
+                     block_size, 0, 0, st);
+    if (s != PA_OK) return s;
+    s = check_q_start(q_start, context_lens, num_seqs, num_q_rows, max_q_len, st);
+    if (s != PA_OK) return s;
+  }
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  BalMultiParams prm;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.q_start = q_start;
+  prm.block_tables = block_tables;
+  prm.context_lens = context_lens;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.counters = reinterpret_cast<int*>(ws + lay.counters);
+  prm.rec_lse = reinterpret_cast<float*>(ws + lay.rec_lse);
+  prm.rec_o = reinterpret_cast<float*>(ws + lay.rec_o);
+  prm.src.k_cache = static_cast<const unsigned char*>(k_cache);
+  prm.src.v_cache = static_cast<const unsigned char*>(v_cache);
+  prm.src.num_kv_heads = num_kv_heads;
+  prm.src.block_size = block_size;
+  prm.src.log2_bs = ilog2(block_size);
+  prm.src.num_blocks = num_blocks;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.num_seqs = num_seqs;
+  prm.num_q_heads = num_q_heads;
+  prm.group = G;
+  prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  CUtensorMap mk, mv;
+  std::memset(&mk, 0, sizeof(mk));
+  std::memset(&mv, 0, sizeof(mv));
+  const bool tma = block_size >= 8;
+  if (tma) {
+    const long long rows = (long long)num_blocks * block_size;
+    const int box_rows = block_size < kTile ? block_size : kTile;
+    if (!make_cache_map(&mk, k_cache, num_kv_heads, head_dim, rows, box_rows) ||
+        !make_cache_map(&mv, v_cache, num_kv_heads, head_dim, rows, box_rows))
+      return PA_ERR_CUDA;
+  }
+  const int cols = max_q_len * G;
+  if (head_dim == 128)
+    return tma ? launch_bal_multi_for<128, true>(cols, mk, mv, prm, sms, st)
+               : launch_bal_multi_for<128, false>(cols, mk, mv, prm, sms, st);
+  return tma ? launch_bal_multi_for<64, true>(cols, mk, mv, prm, sms, st)
+             : launch_bal_multi_for<64, false>(cols, mk, mv, prm, sms, st);
 }

@@ -176,17 +176,23 @@ __device__ __forceinline__ void attend_tile(AttnState<D>& st, uint32_t sK, uint3
 }
 
 // attend_tile for query columns with their own causal limits (several new
-// tokens of one sequence side by side on the n = 8 side): rows >= valid_a
+// tokens of one sequence side by side on the n = 8 side), NT groups of 8
+// columns at once (the K and V fragments are read once for all groups;
+// st[i], qf[i], valid_a[i], valid_b[i] belong to group i): rows >= valid_a
 // (>= valid_b) are masked for this lane's column 2 (lane % 4) (its column
 // + 1); V rows >= valid (the tile's end, >= both) are zeroed. A column whose
 // every score so far is masked keeps m = -inf, l = 0, O = 0 (the exponents
 // use 0 in place of a -inf maximum, so no NaN appears).
-template <int D>
-__device__ __forceinline__ void attend_tile_causal(AttnState<D>& st, uint32_t sK, uint32_t sV,
-                                                   const uint32_t (&qf)[D / 16][2], int valid,
-                                                   int valid_a, int valid_b, float scale_log2,
-                                                   int lane) {
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
+template <int D, int NT>
+__device__ __forceinline__ void attend_tile_causal_nt(AttnState<D> (&st)[NT], uint32_t sK,
+                                                      uint32_t sV,
+                                                      const uint32_t (&qf)[NT][D / 16][2],
+                                                      int valid, const int (&valid_a)[NT],
+                                                      const int (&valid_b)[NT], float scale_log2,
+                                                      int lane) {
+  float s[NT][4];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
   {
     const int r = lane & 15;
 #pragma unroll
@@ -194,39 +200,44 @@ __device__ __forceinline__ void attend_tile_causal(AttnState<D>& st, uint32_t sK
       const int cg = 2 * ks + (lane >> 4);
       uint32_t a[4];
       ldsm_x4(sK + (cg >> 3) * kHalfBytes + r * 128 + (((cg & 7) ^ (r & 7)) << 4), a);
-      mma_bf16_16816(s, a, qf[ks][0], qf[ks][1]);
+#pragma unroll
+      for (int i = 0; i < NT; ++i) mma_bf16_16816(s[i], a, qf[i][ks][0], qf[i][ks][1]);
     }
   }
   const int r0 = lane >> 2;
   const int tk = 2 * (lane & 3);
-  const float y0 = r0 < valid_a ? s[0] * scale_log2 : -INFINITY;
-  const float y1 = r0 < valid_b ? s[1] * scale_log2 : -INFINITY;
-  const float y2 = r0 + 8 < valid_a ? s[2] * scale_log2 : -INFINITY;
-  const float y3 = r0 + 8 < valid_b ? s[3] * scale_log2 : -INFINITY;
-  float mx0 = fmaxf(y0, y2), mx1 = fmaxf(y1, y3);
+  uint32_t pb0[NT], pb1[NT];
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-  }
-  const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
-  const float e0 = mn0 == -INFINITY ? 0.f : mn0, e1 = mn1 == -INFINITY ? 0.f : mn1;
-  const float a0 = exp2f(st.m0 - e0), a1 = exp2f(st.m1 - e1);
-  const uint32_t p01 = pack_bf16x2(exp2f(y0 - e0), exp2f(y1 - e1));
-  const uint32_t p23 = pack_bf16x2(exp2f(y2 - e0), exp2f(y3 - e1));
-  st.l0 = st.l0 * a0 + (bf16_lo(p01) + bf16_lo(p23));
-  st.l1 = st.l1 * a1 + (bf16_hi(p01) + bf16_hi(p23));
-  st.m0 = mn0;
-  st.m1 = mn1;
+  for (int i = 0; i < NT; ++i) {
+    const float y0 = r0 < valid_a[i] ? s[i][0] * scale_log2 : -INFINITY;
+    const float y1 = r0 < valid_b[i] ? s[i][1] * scale_log2 : -INFINITY;
+    const float y2 = r0 + 8 < valid_a[i] ? s[i][2] * scale_log2 : -INFINITY;
+    const float y3 = r0 + 8 < valid_b[i] ? s[i][3] * scale_log2 : -INFINITY;
+    float mx0 = fmaxf(y0, y2), mx1 = fmaxf(y1, y3);
 #pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt) {
-    st.o[mt][0] *= a0;
-    st.o[mt][1] *= a1;
-    st.o[mt][2] *= a0;
-    st.o[mt][3] *= a1;
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(st[i].m0, mx0), mn1 = fmaxf(st[i].m1, mx1);
+    const float e0 = mn0 == -INFINITY ? 0.f : mn0, e1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float a0 = exp2f(st[i].m0 - e0), a1 = exp2f(st[i].m1 - e1);
+    const uint32_t p01 = pack_bf16x2(exp2f(y0 - e0), exp2f(y1 - e1));
+    const uint32_t p23 = pack_bf16x2(exp2f(y2 - e0), exp2f(y3 - e1));
+    st[i].l0 = st[i].l0 * a0 + (bf16_lo(p01) + bf16_lo(p23));
+    st[i].l1 = st[i].l1 * a1 + (bf16_hi(p01) + bf16_hi(p23));
+    st[i].m0 = mn0;
+    st[i].m1 = mn1;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      st[i].o[mt][0] *= a0;
+      st[i].o[mt][1] *= a1;
+      st[i].o[mt][2] *= a0;
+      st[i].o[mt][3] *= a1;
+    }
+    pb0[i] = movmatrix_trans(p01);
+    pb1[i] = movmatrix_trans(p23);
   }
-  const uint32_t pb0 = movmatrix_trans(p01);
-  const uint32_t pb1 = movmatrix_trans(p23);
   uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
   if (valid < kTile) {
     vm01 = (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
@@ -243,7 +254,8 @@ __device__ __forceinline__ void attend_tile_causal(AttnState<D>& st, uint32_t sK
     a[1] &= vm01;
     a[2] &= vm23;
     a[3] &= vm23;
-    mma_bf16_16816(st.o[mt], a, pb0, pb1);
+#pragma unroll
+    for (int i = 0; i < NT; ++i) mma_bf16_16816(st[i].o[mt], a, pb0[i], pb1[i]);
   }
 }
 

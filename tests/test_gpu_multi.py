@@ -53,6 +53,48 @@ def test_multi_matches_oracle(cuda_lib, qlen, hq, hkv, d, bs):
     P.assert_close(P.to_f64(out), oracle_multi(case), f"q_len<={qlen} G={hq // hkv} bs={bs}")
 
 
+@pytest.mark.parametrize("qlen,hq,hkv,d,bs", [
+    (1, 8, 1, 128, 16), (4, 8, 1, 128, 16), (8, 64, 8, 128, 16), (3, 8, 2, 128, 16),
+    (16, 8, 2, 64, 16), (64, 4, 4, 128, 16), (5, 16, 2, 64, 8), (7, 8, 2, 128, 1),
+    (2, 8, 8, 128, 32), (6, 32, 8, 128, 16)])
+def test_balanced_multi_matches_oracle(cuda_lib, qlen, hq, hkv, d, bs):
+    rng = np.random.default_rng(qlen * 100 + hq + bs)
+    qlens = [int(x) for x in rng.integers(1, qlen + 1, len(CTX))]
+    qlens[0] = qlen
+    case = wl.make_multi_case("mqb", 40 + qlen + bs, CTX, qlens, hq, hkv, d, bs)
+    out = run_multi(cuda_lib, case, split=cuda_lib.BALANCED_MULTI)
+    P.assert_close(P.to_f64(out), oracle_multi(case), f"balanced q_len<={qlen} G={hq // hkv}")
+
+
+@pytest.mark.parametrize("lens", [[5000, 3, 0, 700, 1], [1] * 40, [9000] * 3 + [17] * 50],
+                         ids=["mixed", "tiny_units", "long_and_short"])
+def test_balanced_multi_cut_units_and_sequences_without_rows(cuda_lib, lens):
+    # long contexts are cut across many blocks (per-column records merged in
+    # the kernel); a sequence with no query rows holds no tiles
+    qlens = [(i % 4) for i in range(len(lens))]
+    qlens[0] = 4
+    ctx0 = [max(c, 4) for c in lens]
+    case = wl.make_multi_case("mqbc", 77 + len(lens), ctx0, qlens, 64, 8, 128, 16)
+    b = cuda_lib
+    ws = torch.zeros(b.pa_decode_multi_balanced_workspace_bytes(case.batch, 8, 128),
+                     dtype=torch.uint8, device="cuda")
+    d = dict(q=case.q.cuda(), k=case.k_cache.cuda(), v=case.v_cache.cuda())
+    b.pa_kv_append(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), d["k"], d["v"])
+    outs = []
+    for _ in range(2):                              # the workspace is reusable
+        out = torch.full_like(d["q"], float("nan"))
+        b.pa_decode_multi_balanced(d["q"], d["k"], d["v"], case.block_tables.cuda(),
+                                   case.context_lens.cuda(), case.q_start.cuda(),
+                                   case.max_q_len, case.scale, ws, out)
+        outs.append(out)
+    torch.cuda.synchronize()
+    P.assert_close(P.to_f64(outs[0]), oracle_multi(case), "balanced cut units")
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    counters = ws[: case.batch * 8 * 8 * 4].view(torch.int32)
+    assert torch.all(counters == 0)
+    assert b.pa_last_device_error() == 0
+
+
 @pytest.mark.parametrize("split", [16, 64, 256])
 def test_multi_with_context_splits(cuda_lib, split):
     case = wl.make_multi_case("mqs", 50 + split, [0, 3, 60, 300, 1000, 33], [4, 2, 8, 1, 8, 5],
@@ -86,9 +128,10 @@ def test_prompt_fed_chunk_by_chunk_equals_full_causal_attention(cuda_lib):
     assert a == n
 
 
-def test_speculative_verify_70b_shape_sampled(cuda_lib):
+@pytest.mark.parametrize("balanced", [False, True], ids=["split", "balanced"])
+def test_speculative_verify_70b_shape_sampled(cuda_lib, balanced):
     case = wl.spec_verify_case(seed=0, batch=256, q_len=4)
-    out = P.to_f64(run_multi(cuda_lib, case))
+    out = P.to_f64(run_multi(cuda_lib, case, split=cuda_lib.BALANCED_MULTI if balanced else 0))
     sub = [0, 17, 101, 199, 255]
     qs = case.q_start.numpy()
     kc, vc = pa.kv_append(wl.bits(case.k_cache), wl.bits(case.v_cache), wl.bits(case.k_new),
