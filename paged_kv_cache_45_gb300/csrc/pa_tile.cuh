@@ -154,9 +154,10 @@ __device__ __forceinline__ void attend_tile(AttnState<D>& st, uint32_t sK, uint3
   const uint32_t pb0 = movmatrix_trans(p01);  // P^T tokens 0-7 as the MMA's B operand
   const uint32_t pb1 = movmatrix_trans(p23);  // tokens 8-15
 
-  // O^T += V^T . P^T
+  // O^T += V^T . P^T (the V masks only on a partial tile)
   uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
-  if (valid < kTile) {
+  const bool masked = valid < kTile;
+  if (masked) {
     vm01 = (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
     vm23 = (tk + 8 < valid ? 0x0000ffffu : 0u) | (tk + 9 < valid ? 0xffff0000u : 0u);
   }
@@ -167,10 +168,12 @@ __device__ __forceinline__ void attend_tile(AttnState<D>& st, uint32_t sK, uint3
     const int cg = 2 * mt + (mi & 1);
     uint32_t a[4];
     ldsm_x4_trans(sV + (cg >> 3) * kHalfBytes + r * 128 + (((cg & 7) ^ (r & 7)) << 4), a);
-    a[0] &= vm01;
-    a[1] &= vm01;
-    a[2] &= vm23;
-    a[3] &= vm23;
+    if (masked) {
+      a[0] &= vm01;
+      a[1] &= vm01;
+      a[2] &= vm23;
+      a[3] &= vm23;
+    }
     mma_bf16_16816(st.o[mt], a, pb0, pb1);
   }
 }
@@ -301,11 +304,17 @@ constexpr int kFp8Tile = 32;
 
 // A operand (16 tokens x 16 k) of one e4m3 K ldmatrix result: k[i] holds 4
 // codes (dims 4c..4c+3 of the k step) of token r0 (i even) or r0 + 8 (i odd).
+// Both byte pairs of a u32 widened: lo <- bytes 0, 1; hi <- bytes 2, 3 (the
+// register's 16-bit halves feed the conversions directly).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
+}
 __device__ __forceinline__ void fp8_k_operand(const uint32_t (&k)[4], int i0, uint32_t (&a)[4]) {
-  a[0] = e4m3x2_to_f16x2(k[i0] & 0xFFFFu);
-  a[1] = e4m3x2_to_f16x2(k[i0 + 1] & 0xFFFFu);
-  a[2] = e4m3x2_to_f16x2(k[i0] >> 16);
-  a[3] = e4m3x2_to_f16x2(k[i0 + 1] >> 16);
+  e4m3x4_to_f16x2x2(k[i0], a[0], a[2]);
+  e4m3x4_to_f16x2x2(k[i0 + 1], a[1], a[3]);
 }
 
 template <int D>
@@ -371,7 +380,8 @@ __device__ __forceinline__ void attend_tile_fp8(AttnState<D>& st, uint32_t sK, u
   for (int i = 0; i < 4; ++i) pb[i] = movmatrix_trans(pw[i]);
   // the V rows this lane's A fragments hold: tokens tk + 8i and tk + 8i + 1
   uint32_t vm[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-  if (valid < kFp8Tile) {
+  const bool masked = valid < kFp8Tile;
+  if (masked) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
       vm[i] = (tk + 8 * i < valid ? 0x0000ffffu : 0u) | (tk + 8 * i + 1 < valid ? 0xffff0000u : 0u);
@@ -388,17 +398,19 @@ __device__ __forceinline__ void attend_tile_fp8(AttnState<D>& st, uint32_t sK, u
       uint32_t e0 = byte_perm(va[2 * half], 0u, 0x3120u);      // tokens 0-7
       uint32_t e1 = byte_perm(va[2 * half + 1], 0u, 0x3120u);  // tokens 8-15
       uint32_t a[4];
-      a[0] = e4m3x2_to_f16x2(e0 & 0xFFFFu) & vm[0];
-      a[1] = e4m3x2_to_f16x2(e0 >> 16) & vm[0];
-      a[2] = e4m3x2_to_f16x2(e1 & 0xFFFFu) & vm[1];
-      a[3] = e4m3x2_to_f16x2(e1 >> 16) & vm[1];
+      e4m3x4_to_f16x2x2(e0, a[0], a[1]);
+      e4m3x4_to_f16x2x2(e1, a[2], a[3]);
+      if (masked) {
+        a[0] &= vm[0]; a[1] &= vm[0]; a[2] &= vm[1]; a[3] &= vm[1];
+      }
       mma_f16_16816(st.o[2 * sidx + half], a, pb[0], pb[1]);
       e0 = byte_perm(vb[2 * half], 0u, 0x3120u);      // tokens 16-23
       e1 = byte_perm(vb[2 * half + 1], 0u, 0x3120u);  // tokens 24-31
-      a[0] = e4m3x2_to_f16x2(e0 & 0xFFFFu) & vm[2];
-      a[1] = e4m3x2_to_f16x2(e0 >> 16) & vm[2];
-      a[2] = e4m3x2_to_f16x2(e1 & 0xFFFFu) & vm[3];
-      a[3] = e4m3x2_to_f16x2(e1 >> 16) & vm[3];
+      e4m3x4_to_f16x2x2(e0, a[0], a[1]);
+      e4m3x4_to_f16x2x2(e1, a[2], a[3]);
+      if (masked) {
+        a[0] &= vm[2]; a[1] &= vm[2]; a[2] &= vm[3]; a[3] &= vm[3];
+      }
       mma_f16_16816(st.o[2 * sidx + half], a, pb[2], pb[3]);
     }
   }
