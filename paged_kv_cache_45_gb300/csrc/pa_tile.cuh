@@ -144,12 +144,16 @@ __device__ __forceinline__ void attend_tile(AttnState<D>& st, uint32_t sK, uint3
   st.l1 = st.l1 * a1 + (bf16_hi(p01) + bf16_hi(p23));
   st.m0 = mn0;
   st.m1 = mn1;
+  // O is rescaled only when some running max moved (a factor of exactly 1
+  // leaves it unchanged, and after the first tiles the max rarely moves)
+  if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt) {
-    st.o[mt][0] *= a0;
-    st.o[mt][1] *= a1;
-    st.o[mt][2] *= a0;
-    st.o[mt][3] *= a1;
+    for (int mt = 0; mt < D / 16; ++mt) {
+      st.o[mt][0] *= a0;
+      st.o[mt][1] *= a1;
+      st.o[mt][2] *= a0;
+      st.o[mt][3] *= a1;
+    }
   }
   const uint32_t pb0 = movmatrix_trans(p01);  // P^T tokens 0-7 as the MMA's B operand
   const uint32_t pb1 = movmatrix_trans(p23);  // tokens 8-15
@@ -231,18 +235,21 @@ __device__ __forceinline__ void attend_tile_causal_nt(AttnState<D> (&st)[NT], ui
     st[i].l1 = st[i].l1 * a1 + (bf16_hi(p01) + bf16_hi(p23));
     st[i].m0 = mn0;
     st[i].m1 = mn1;
+    if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {  // only when a max moved
 #pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-      st[i].o[mt][0] *= a0;
-      st[i].o[mt][1] *= a1;
-      st[i].o[mt][2] *= a0;
-      st[i].o[mt][3] *= a1;
+      for (int mt = 0; mt < D / 16; ++mt) {
+        st[i].o[mt][0] *= a0;
+        st[i].o[mt][1] *= a1;
+        st[i].o[mt][2] *= a0;
+        st[i].o[mt][3] *= a1;
+      }
     }
     pb0[i] = movmatrix_trans(p01);
     pb1[i] = movmatrix_trans(p23);
   }
   uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
-  if (valid < kTile) {
+  const bool masked = valid < kTile;
+  if (masked) {
     vm01 = (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
     vm23 = (tk + 8 < valid ? 0x0000ffffu : 0u) | (tk + 9 < valid ? 0xffff0000u : 0u);
   }
@@ -253,10 +260,12 @@ __device__ __forceinline__ void attend_tile_causal_nt(AttnState<D> (&st)[NT], ui
     const int cg = 2 * mt + (mi & 1);
     uint32_t a[4];
     ldsm_x4_trans(sV + (cg >> 3) * kHalfBytes + r * 128 + (((cg & 7) ^ (r & 7)) << 4), a);
-    a[0] &= vm01;
-    a[1] &= vm01;
-    a[2] &= vm23;
-    a[3] &= vm23;
+    if (masked) {
+      a[0] &= vm01;
+      a[1] &= vm01;
+      a[2] &= vm23;
+      a[3] &= vm23;
+    }
 #pragma unroll
     for (int i = 0; i < NT; ++i) mma_bf16_16816(st[i].o[mt], a, pb0[i], pb1[i]);
   }
@@ -368,12 +377,16 @@ __device__ __forceinline__ void attend_tile_fp8(AttnState<D>& st, uint32_t sK, u
   st.l1 = st.l1 * a1 + ((f16_hi(pw[0]) + f16_hi(pw[1])) + (f16_hi(pw[2]) + f16_hi(pw[3])));
   st.m0 = mn0;
   st.m1 = mn1;
+  // O is rescaled only when some running max moved (a factor of exactly 1
+  // leaves it unchanged, and after the first tiles the max rarely moves)
+  if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt) {
-    st.o[mt][0] *= a0;
-    st.o[mt][1] *= a1;
-    st.o[mt][2] *= a0;
-    st.o[mt][3] *= a1;
+    for (int mt = 0; mt < D / 16; ++mt) {
+      st.o[mt][0] *= a0;
+      st.o[mt][1] *= a1;
+      st.o[mt][2] *= a0;
+      st.o[mt][3] *= a1;
+    }
   }
   uint32_t pb[4];  // B fragments of P^T: tokens 0-7, 8-15, 16-23, 24-31
 #pragma unroll
