@@ -158,6 +158,36 @@ def test_batch_size_may_shrink_and_grow_between_calls(cuda_lib):
         P.assert_close(got, P.oracle_out(case, seqs=seqs), f"B={case.batch}")
 
 
+def test_largest_batches(cuda_lib):
+    # The balanced kernel keeps the batch's tile prefix sums in shared memory:
+    # 30,000 sequences still fit (one block per SM); 60,000 do not and are
+    # refused with PA_ERR_UNSUPPORTED before any launch, while the fixed-split
+    # kernel (one block per sequence x KV head, grid z up to 65,535) runs them.
+    b = cuda_lib
+    rng = np.random.default_rng(9)
+    for B in (30000, 60000):
+        case = wl.make_case(f"big{B}", 630, list(rng.integers(0, 4, B)), 8, 2, 128, 16,
+                            append=False)
+        d = P.dev(case)
+        seqs = list(range(0, B, 997)) + [B - 1]
+        want = P.oracle_out(case, seqs=seqs)
+        if B == 30000:
+            out = b.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                           d["context_lens"], case.scale, split_tokens=b.BALANCED)
+            torch.cuda.synchronize()
+            P.assert_close(P.to_f64(out)[seqs], want, "balanced B=30000")
+        else:
+            with pytest.raises(b.PagedKVError) as e:
+                b.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                         d["context_lens"], case.scale, split_tokens=b.BALANCED)
+            assert e.value.status == -2
+            out = b.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                           d["context_lens"], case.scale)
+            torch.cuda.synchronize()
+            P.assert_close(P.to_f64(out)[seqs], want, "fixed split B=60000")
+        assert b.pa_last_device_error() == 0
+
+
 def test_balanced_rejects_small_workspace(cuda_lib):
     b = cuda_lib
     case = wl.tiny_case(0)
