@@ -7,19 +7,24 @@
 // PagedAttention" and "Under the Hood: Flash Attention"), scheduled for a
 // continuously batched set of sequences whose lengths differ by 60x:
 //
-//   * the work is the list of 16-token tiles of every (sequence, KV head)
-//     unit, sequence-major; its length N = Hkv * sum_b ceil(ctx_b / 16) is
-//     computed on the device by every block from context_lens (a prefix sum
-//     in shared memory), so the host needs neither the lengths nor a sync;
+//   * the work is the list of TT-token tiles (16 for bf16, 32 for e4m3) of
+//     every (sequence, KV head) unit, sequence-major; its length
+//     N = Hkv * sum_b ceil(ctx_b / TT) is computed on the device by every
+//     block from context_lens (a prefix sum in shared memory, pa_balance.cuh),
+//     so the host needs neither the lengths nor a sync;
 //   * each block of a persistent grid (kBlocksPerSM per SM) owns the
 //     contiguous tile range [c N / C, (c + 1) N / C): every block streams the
 //     same number of tiles (to one) whatever the length mix, and no block is
 //     launched for an empty context split;
 //   * inside a block, the structure of pa_decode: a loader warp streams the
 //     range's K/V tiles through a ring of stages (TMA, or a cp.async gather
-//     below block size 8), crossing unit boundaries without a pause, and four
-//     consumer warps fold tiles round-robin, each serving the whole GQA group;
-//   * at the end of each unit the four warps' states are merged through
+//     below block size 8), crossing unit boundaries without a pause, and the
+//     consumer warps (four for bf16, two for e4m3) fold tiles round-robin,
+//     each serving the whole GQA group;
+//   * the fused step (pa_append_decode) also writes each sequence's new K/V
+//     row: the warp that folds a unit's last tile stores that KV head's row
+//     to the pool and patches it into the landed tile;
+//   * at the end of each unit the consumer warps' states are merged through
 //     shared memory. A unit inside one block's range is written as bf16. A
 //     unit cut by a range boundary leaves one normalised fp32 partial + base-2
 //     log-sum-exp per block; the block that arrives last on the unit's

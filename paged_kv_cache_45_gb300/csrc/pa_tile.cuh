@@ -1,7 +1,7 @@
-// pa_tile.cuh -- the K/V tile shared by both decode kernels (16 tokens of
+// pa_tile.cuh -- the K/V tile shared by the decode kernels (16 tokens of
 // bf16, 32 tokens of e4m3): how a tile is fetched into shared memory and how
 // one warp folds it into its running attention state for the GQA group of one
-// KV head.
+// KV head (or, for several query tokens, for 8 (token, head) columns).
 //
 // The tile math is the streaming softmax of "Text Generation Inference:
 // Hugging Face's production-grade LLM inference server" (section "Under the
@@ -16,9 +16,9 @@
 //
 // Shared-memory tile layout: K then V; each is D/64 column halves of 16 rows x
 // 128 bytes with the 128-byte swizzle (16-byte chunk c of row r stored at
-// chunk c ^ (r & 7)), the layout a TMA box {64 columns, 16 rows} with
-// CU_TENSOR_MAP_SWIZZLE_128B writes. ldmatrix reads of 8 rows then hit 8
-// distinct bank groups.
+// chunk c ^ (r & 7)), the layout TMA boxes {64 columns, 16 rows} -- or one
+// 3-D box {64 columns, 16 rows, 2 halves} -- with CU_TENSOR_MAP_SWIZZLE_128B
+// write. ldmatrix reads of 8 rows then hit 8 distinct bank groups.
 #pragma once
 
 #include "pa_device.cuh"
