@@ -56,7 +56,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2048)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["cb70b", "8b", "long", "prefix", "spec", "cow"],
+    ap.add_argument("--workload", choices=["cb70b", "8b", "long", "prefix", "spec", "prefill",
+                                           "cow"],
                     default="cb70b",
                     help="spec: 4 query tokens per sequence (speculative verification, "
                          "pa_decode_multi); cow: the copy-on-write step of the prefix cache "
@@ -102,6 +103,10 @@ def describe(workload: str, batch: int = 256) -> str:
                 "128, bf16, block_size 16, 1% of K rows x8, no append",
         "prefix": "radix prefix sharing: B=128, 2048-token prefix in the same 128 blocks, "
                   "private suffix uniform [64, 1024] + 1 appended, 8B heads",
+        "prefill": "chunked prefill, 70B shape: 8 sequences each bringing a 2048-token chunk "
+                   "after 6144 cached tokens (causal), 64 q heads / 8 KV heads, head_dim 128, "
+                   "bf16, block_size 16; pa_kv_append of the chunk + pa_decode_multi "
+                   "(row-block kernel)",
         "spec": "speculative verification, 70B shape: B={batch} sequences, ctx log-uniform "
                 "[128, 8192], 4 new query tokens each (causal), 64 q heads / 8 KV heads, "
                 "head_dim 128, bf16, block_size 16; pa_kv_append of the 4 rows + "
@@ -123,9 +128,10 @@ class Steps:
         self.workload = workload
         self.items = []
         self.fp8 = kv_dtype == "fp8"
-        self.multi = workload == "spec"
-        if workload == "spec":
-            case = wl.spec_verify_case(seed, batch=batch, q_len=4)
+        self.multi = workload in ("spec", "prefill")
+        if self.multi:
+            case = (wl.spec_verify_case(seed, batch=batch, q_len=4) if workload == "spec" else
+                    prefill_case(seed))
             self.k_cache, self.v_cache = case.k_cache.to(device), case.v_cache.to(device)
             self.scale, self.hkv, self.hq, self.d = (case.scale, case.num_kv_heads,
                                                      case.num_q_heads, case.head_dim)
@@ -134,6 +140,11 @@ class Steps:
             self.items.append(dict(fill=None, q=case.q, k_new=case.k_new, v_new=case.v_new,
                                    slots=case.slot_mapping, tables=case.block_tables,
                                    lens=case.context_lens, qstart=case.q_start))
+            # attention FLOPs: 2 products x 2 FLOP x D per (row, attended key)
+            qs, cl = case.q_start.numpy().astype(np.int64), case.context_lens.numpy()
+            attended = sum(int((cl[i] - (qs[i + 1] - qs[i]) + 1 + cl[i]) * (qs[i + 1] - qs[i])) // 2
+                           for i in range(len(cl)))
+            self.items[-1]["flops"] = 4 * self.d * self.hq * attended
         elif workload == "cb70b":
             cb = wl.ContinuousBatching(seed=seed, batch=batch)
             self.k_cache, self.v_cache = cb.initial_caches(device)
@@ -270,6 +281,8 @@ KERNEL_SOURCES = {   # the files whose change invalidates a kernel's recorded DR
     "multi_decode_kernel": ("pa_decode_multi.cu", "pa_tile.cuh", "pa_device.cuh", "pa_api.cu"),
     "balanced_multi_kernel": ("pa_decode_multi.cu", "pa_balance.cuh", "pa_tile.cuh",
                               "pa_device.cuh", "pa_api.cu"),
+    "rowblock_decode_kernel": ("pa_decode_multi.cu", "pa_tile.cuh", "pa_device.cuh",
+                               "pa_api.cu"),
 }
 
 
@@ -365,6 +378,8 @@ def run_gpu(args):
     if steps.multi:   # -1: the balanced schedule (pa_decode_multi_balanced)
         split = -1 if args.multi_schedule == "balanced" else (args.split if args.split >= 0
                                                               else 1024)
+        if args.workload == "prefill":
+            split = 0     # long chunks run on the row-block kernel, unsplit
     elif args.schedule == "balanced":
         split = b.BALANCED
     elif args.split >= 0:
@@ -611,12 +626,24 @@ def run_gpu(args):
     kernel = ("balanced_decode_kernel" + ("[e4m3]" if steps.fp8 else "")) if ws.balanced \
         else (("balanced_multi_kernel" if ws.multi_balanced else "multi_decode_kernel")
               if steps.multi else "paged_decode_kernel")
+    if args.workload == "prefill":
+        kernel = "rowblock_decode_kernel"
     traffic = traffic_per_launch(kernel, kv_tokens_per_launch)
     clocks = sampler.summary() if sampler else None
+    prefill = args.workload == "prefill"
+    if prefill:   # compute-bound: TFLOP/s against the measured bf16 tensor peak
+        flops = steps.items[0]["flops"]
+        tflops = flops * K / total_s / 1e12
+        kern_tflops = flops * KI / dec_s / 1e12
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+                tpeak, tkind = float(json.load(fh)["bf16_tflops"]), "measured"
+        except Exception:
+            tpeak, tkind = 1900.0, "fallback"
     line = {
-        "metric": METRIC,
-        "value": round(gbs, 2),
-        "unit": "GB/s",
+        "metric": PREFILL_METRIC if prefill else METRIC,
+        "value": round(tflops, 2) if prefill else round(gbs, 2),
+        "unit": "TFLOP/s" if prefill else "GB/s",
         "n_gpus": world,
         "steps": K,
         "warmup": args.warmup,
@@ -628,7 +655,9 @@ def run_gpu(args):
         "data": "synthetic (seeded N(0,1) bf16 q/K/V; seeded lengths and block placement)",
         "config": {"workload": describe(args.workload, args.batch) +
                    (" (e4m3 KV pool, per-KV-head scales)" if steps.fp8 else ""),
-                   "schedule": "balanced" if ws.balanced else
+                   "schedule": "row blocks (64 (token, head) rows x KV head x sequence per "
+                               "block, unsplit)" if args.workload == "prefill" else
+                   "balanced" if ws.balanced else
                    (("multi, balanced persistent (pa_decode_multi_balanced)"
                      if ws.multi_balanced else
                      f"multi (one block per KV head, split, sequence; split_tokens="
@@ -667,6 +696,20 @@ def run_gpu(args):
         "timing": "CUDA events bracketing the K steps on the launching stream, "
                   "barrier + synchronize on both sides",
     }
+    if prefill:
+        line["roofline"] = {
+            "bound": "tensor", "kernel": kernel, "achieved": round(kern_tflops, 2),
+            "peak": tpeak, "unit": "TFLOP/s", "frac": round(kern_tflops / tpeak, 4),
+            "peak_kind": f"{tkind} bf16_tflops (cuBLAS burst; this kernel uses mma.sync)",
+            "traffic": None if traffic is None else int(traffic),
+            "algorithmic_flops_per_launch": int(flops),
+            "measured": f"CUDA events around each decode launch, {KI} steps"}
+        line["kv_gbs"] = round(gbs, 2)
+        line["e2e"]["value"] = round(flops * E / e2e_s / 1e12, 2)
+        line["e2e"]["unit"] = "TFLOP/s"
+        line["config"]["l2"] = "inputs larger than L2: 268 MB of K/V read every step"
+        line.pop("pct_of_hbm_peak", None)
+        line.pop("pct_of_datasheet_8tbs", None)
     if clocks is not None:
         line["clocks"] = clocks
     if cpu is not None:
@@ -679,6 +722,41 @@ def run_gpu(args):
 # ---------------------------------------------------------------------------
 # the oracle on the host cores: CPU baseline and the reference arm
 # ---------------------------------------------------------------------------
+
+def prefill_case(seed: int, n_seqs: int = 8):
+    """The chunked-prefill step: n_seqs sequences, 6144 cached + 2048 new tokens."""
+    from paged_kv_cache_45_gb300 import workloads as wl
+    return wl.make_multi_case("prefill", seed, [6144] * n_seqs, [2048] * n_seqs, 64, 8, 128, 16)
+
+
+def prefill_cpu_baseline(seed: int, budget_s: float):
+    """The oracle's decode_multi on the host over a bounded sample of the
+    prefill step: the chunk's rows of one sequence, taken in order, each row
+    at its own causal context (row i of the chunk sees 6144 + i + 1 keys)."""
+    import numpy as np
+    import oracle
+    from oracle import paged_attention as pa
+    from paged_kv_cache_45_gb300 import workloads as wl
+    case = prefill_case(seed, n_seqs=1)
+    kc, vc = pa.kv_append(wl.bits(case.k_cache), wl.bits(case.v_cache), wl.bits(case.k_new),
+                          wl.bits(case.v_new), case.slot_mapping.numpy())
+    q, bt = wl.bits(case.q), case.block_tables.numpy()
+    n, ctx = int(case.q_start[1]), int(case.context_lens[0])
+    flops, secs, rows = 0, 0.0, 0
+    while rows < n and (secs < budget_s or rows < 2):
+        pos = ctx - n + rows
+        t0 = time.perf_counter()
+        oracle.decode_multi(q[rows:rows + 1], kc, vc, bt, np.array([pos + 1]),
+                            np.array([0, 1]), case.scale)
+        secs += time.perf_counter() - t0
+        flops += 4 * case.head_dim * case.num_q_heads * (pos + 1)
+        rows += 1
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"the first {rows} rows of one sequence's 2048-token chunk (each at its "
+                      f"causal context, 6145.. keys, 64 heads), fp64 oracle decode_multi, one "
+                      f"BLAS thread, {secs:.1f} s"}
+
 
 def oracle_sample_case(seed: int, n_seqs: int = 48):
     """A bounded sample of the 70B-shape batch: n_seqs sequences with lengths
@@ -736,8 +814,13 @@ def single_thread_env():
     return env
 
 
+def prefill_cpu_baseline_child(seed: int, budget_s: float) -> None:
+    print(json.dumps(prefill_cpu_baseline(seed, budget_s)))
+
+
 def cpu_baseline_subprocess(args):
-    code = ("import bench; bench.cpu_baseline_child(%d, %f)" % (args.seed, args.cpu_seconds))
+    child = "prefill_cpu_baseline_child" if args.workload == "prefill" else "cpu_baseline_child"
+    code = ("import bench; bench.%s(%d, %f)" % (child, args.seed, args.cpu_seconds))
     try:
         r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=single_thread_env(),
                            capture_output=True, text=True, timeout=600)
@@ -778,6 +861,7 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 
 COW_METRIC = "copy-on-write block copy GB/s (bytes read + written), forked batch"
+PREFILL_METRIC = "chunked-prefill paged attention TFLOP/s, 70B shape"
 
 
 def cow_cpu_baseline(batch: int, block_elems: int, budget_s: float):

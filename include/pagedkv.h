@@ -324,10 +324,14 @@ pa_status pa_selftest_wait_timeout(int32_t limit_us, void* stream);
  *              position (a row before position 0 gives zeros).
  *   q_start    int32 [num_seqs + 1], q_start[0] = 0, q_start[num_seqs] =
  *              num_q_rows, non-decreasing.
- *   max_q_len  an upper bound of every n_b; max_q_len * (num_q_heads /
- *              num_kv_heads) <= 64, else PA_ERR_UNSUPPORTED. A sequence with
- *              more rows than max_q_len is skipped and sets bit 16 of the
- *              device error word (rejected in validating mode).
+ *   max_q_len  an upper bound of every n_b. With max_q_len * (num_q_heads /
+ *              num_kv_heads) <= 64 (drafted tokens, short chunks) one block
+ *              holds a sequence's whole query group for one KV head; above
+ *              that (long prompt chunks) blocks of 64 (token, head) rows each
+ *              run with a causal key range of their own, unsplit: split_tokens
+ *              must then be 0, else PA_ERR_UNSUPPORTED. A sequence with more
+ *              rows than max_q_len is skipped and sets bit 16 of the device
+ *              error word (rejected in validating mode).
  *   split_tokens / max_splits / part_out / part_lse: as in pa_decode, with
  *              rows in place of sequences (part_out [num_q_rows, num_q_heads,
  *              max_splits, head_dim]); split mode also writes each row's
@@ -352,7 +356,8 @@ pa_status pa_decode_multi(const void* q, const void* k_cache, const void* v_cach
  * pa_decode_multi_balanced_workspace_bytes(num_seqs, num_kv_heads, head_dim)
  * bytes, 256-byte aligned, zero-filled before its first use and left reusable
  * (too small: PA_ERR_WORKSPACE); calls sharing a workspace must not overlap.
- * Other arguments, limits and errors as pa_decode_multi. */
+ * max_q_len * (num_q_heads / num_kv_heads) must be <= 64, else
+ * PA_ERR_UNSUPPORTED. Other arguments, limits and errors as pa_decode_multi. */
 pa_status pa_decode_multi_balanced(const void* q, const void* k_cache, const void* v_cache,
                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
                                    const int32_t* context_lens, const int32_t* q_start,

@@ -314,6 +314,289 @@ pa_status launch_multi(const CUtensorMap& mk, const CUtensorMap& mv, const Multi
 }
 
 // ---------------------------------------------------------------------------
+// long query chunks: row blocks in the standard MMA form
+// ---------------------------------------------------------------------------
+// A chunk of a long prompt brings more (token, head) rows than the n side
+// holds (n_b * G > 64). Then the rows go on the MMA's m side, as in a
+// FlashAttention-2 forward pass: a block takes 64 rows (the (token, head)
+// pairs 64 rb .. 64 rb + 63 of one sequence and KV head, row = token * G +
+// head), four warps of 16 rows; per 16-key tile each warp computes
+// S[16 x 16] = Q K^T (8 k-steps x 2 key groups of m16n8k16), the online
+// softmax per row, and O[16 x D] += P V with P taken straight from the score
+// accumulators as the A operand. Every warp folds every tile of the block's
+// key range [0, last position of its last token], read through the same TMA
+// ring as the other kernels (K/V tiles are re-read from L2 by the sequence's
+// other row blocks: prefill is compute-bound).
+
+constexpr int kRowWarps = 4;   // 16 rows each
+constexpr int kRowsPerBlock = 16 * kRowWarps;
+
+template <int D>
+struct RowSmem {
+  static constexpr int kStageBytes = TileGeom<D>::kStageBytes;
+  static constexpr int kRingBytes = kMultiStages * kStageBytes;
+  static constexpr int kBarOff = kRingBytes;
+  static constexpr int kFlagOff = kBarOff + 2 * kMultiStages * 8;
+  static constexpr int kAlloc = kFlagOff + 16 + 1024;
+};
+
+template <int D, bool kTma>
+__global__ void __launch_bounds__((kRowWarps + 1) * 32, 2)
+    rowblock_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                           const __grid_constant__ CUtensorMap tmap_v, const MultiParams p) {
+  using L = RowSmem<D>;
+  using Gm = TileGeom<D>;
+  constexpr int STAGES = kMultiStages;
+  constexpr int NW = kRowWarps;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* empty = full + STAGES;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kFlagOff);
+
+  const int rb = blockIdx.x;
+  const int kvh = blockIdx.y;
+  const int b = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.group;
+  const int row0 = p.q_start[b];
+  const int n = p.q_start[b + 1] - row0;
+  const int rows = n * G;
+  if (rb * kRowsPerBlock >= rows) return;
+  if (n > p.max_q_len) {
+    if (threadIdx.x == 0) report(kErrShape);
+    return;
+  }
+  int ctx = p.context_lens[b];
+  const int cap = p.max_blocks << p.src.log2_bs;
+  ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
+  // keys the block needs: up to the last position of its last token
+  const int last_row = min(rows, (rb + 1) * kRowsPerBlock) - 1;
+  const int t_end = min(ctx, ctx - n + last_row / G + 1);
+  const int n_tiles = t_end > 0 ? (t_end + kTile - 1) / kTile : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], kTma ? 1 : 32);
+      mbar_init(&empty[s], NW);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint32_t ring = smem_u32(smem);
+
+  if (warp == NW) {
+    // ------------------------------------------------------------ loader warp
+    if (kTma && lane == 0) {
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+    }
+    const int32_t* bt = p.block_tables + (size_t)b * p.max_blocks;
+    const int n_seq_blocks = (ctx + p.src.block_size - 1) >> p.src.log2_bs;
+    int tc_base = -(1 << 30);
+    int tc_val = -1;
+    int issued = 0;
+    for (int i = 0; i < n_tiles; ++i) {
+      if (__any_sync(0xffffffffu, *abort_flag)) break;
+      const int stage = i % STAGES;
+      if (i >= STAGES &&
+          !__all_sync(0xffffffffu, mbar_wait(&empty[stage], ((i / STAGES) - 1) & 1))) {
+        if (lane == 0) report(kErrWaitEmpty);
+        *abort_flag = 1;
+        break;
+      }
+      const int t0 = i * kTile;
+      const int blk_first = t0 >> p.src.log2_bs;
+      const int blk_last = (t0 + kTile - 1) >> p.src.log2_bs;
+      if (blk_first < tc_base || blk_last >= tc_base + 32) {  // warp-uniform refill
+        tc_base = blk_first;
+        const int idx = tc_base + lane;
+        tc_val = idx < n_seq_blocks ? bt[idx] : -1;
+      }
+      issue_tile<D, kTma>(ring + stage * Gm::kStageBytes, &full[stage], &tmap_k, &tmap_v, p.src,
+                          kvh, t0, ctx, n_seq_blocks, tc_base, tc_val, lane);
+      ++issued;
+    }
+    const int first = issued > STAGES ? issued - STAGES : 0;
+    for (int i = first; i < issued; ++i) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[i % STAGES], (i / STAGES) & 1))) {
+        if (lane == 0) report(kErrDrain);
+        break;
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int gq = lane >> 2;          // this lane's rows: gq and gq + 8 of the warp
+  const int cq = lane & 3;
+  const int wrow = rb * kRowsPerBlock + warp * 16;
+  const int ra = wrow + gq, rbw = wrow + gq + 8;  // the lane's two rows
+  // the rows' query tokens, causal limits (last attended position) and q rows
+  const int lim_a = ra < rows ? ctx - n + ra / G : -1;
+  const int lim_b = rbw < rows ? ctx - n + rbw / G : -1;
+  // A operand of Q: rows gq / gq + 8, dims 16 ks + 2 cq (+1) and + 8
+  uint32_t qa[D / 16][4];
+  {
+    const unsigned int* pa_row = ra < rows ? reinterpret_cast<const unsigned int*>(
+        p.q + ((size_t)(row0 + ra / G) * p.num_q_heads + kvh * G + ra % G) * D + 2 * cq) : nullptr;
+    const unsigned int* pb_row = rbw < rows ? reinterpret_cast<const unsigned int*>(
+        p.q + ((size_t)(row0 + rbw / G) * p.num_q_heads + kvh * G + rbw % G) * D + 2 * cq) : nullptr;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      qa[ks][0] = pa_row ? __ldg(pa_row + ks * 8) : 0u;
+      qa[ks][1] = pb_row ? __ldg(pb_row + ks * 8) : 0u;
+      qa[ks][2] = pa_row ? __ldg(pa_row + ks * 8 + 4) : 0u;
+      qa[ks][3] = pb_row ? __ldg(pb_row + ks * 8 + 4) : 0u;
+    }
+  }
+  float o[D / 8][4];
+#pragma unroll
+  for (int db = 0; db < D / 8; ++db) o[db][0] = o[db][1] = o[db][2] = o[db][3] = 0.f;
+  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+  const int mi = lane >> 3;          // the 8x8 matrix this lane addresses for ldmatrix
+  for (int i = 0; i < n_tiles; ++i) {
+    if (__any_sync(0xffffffffu, *abort_flag)) break;
+    const int stage = i % STAGES;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], (i / STAGES) & 1))) {
+      if (lane == 0) report(kErrWaitFull);
+      *abort_flag = 1;
+      break;
+    }
+    const uint32_t sK = ring + stage * Gm::kStageBytes;
+    const uint32_t sV = sK + Gm::kKVBytes;
+    const int t0 = i * kTile;
+    // S = Q K^T: key groups 0-7 (s0) and 8-15 (s1)
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      const int key = 8 * (mi >> 1) + (lane & 7);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int cg = 2 * ks + (mi & 1);
+        uint32_t kb[4];  // (keys 0-7, dims lo), (keys 0-7, hi), (keys 8-15, lo), (keys 8-15, hi)
+        ldsm_x4(sK + (cg >> 3) * kHalfBytes + key * 128 + (((cg & 7) ^ (key & 7)) << 4), kb);
+        mma_bf16_16816(s0, qa[ks], kb[0], kb[1]);
+        mma_bf16_16816(s1, qa[ks], kb[2], kb[3]);
+      }
+    }
+    // causal + context masks: key t0 + k valid for a row if <= its limit
+    const int k0 = t0 + 2 * cq;
+    float y[8];  // row a: keys k0, k0+1, k0+8, k0+9; row b: the same
+    y[0] = k0 <= lim_a ? s0[0] * p.scale_log2 : -INFINITY;
+    y[1] = k0 + 1 <= lim_a ? s0[1] * p.scale_log2 : -INFINITY;
+    y[2] = k0 + 8 <= lim_a ? s1[0] * p.scale_log2 : -INFINITY;
+    y[3] = k0 + 9 <= lim_a ? s1[1] * p.scale_log2 : -INFINITY;
+    y[4] = k0 <= lim_b ? s0[2] * p.scale_log2 : -INFINITY;
+    y[5] = k0 + 1 <= lim_b ? s0[3] * p.scale_log2 : -INFINITY;
+    y[6] = k0 + 8 <= lim_b ? s1[2] * p.scale_log2 : -INFINITY;
+    y[7] = k0 + 9 <= lim_b ? s1[3] * p.scale_log2 : -INFINITY;
+    float mxa = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
+    float mxb = fmaxf(fmaxf(y[4], y[5]), fmaxf(y[6], y[7]));
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+      mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, off));
+      mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, off));
+    }
+    const float mna = fmaxf(m_a, mxa), mnb = fmaxf(m_b, mxb);
+    const float ea = mna == -INFINITY ? 0.f : mna, eb = mnb == -INFINITY ? 0.f : mnb;
+    const float aa = exp2f(m_a - ea), ab = exp2f(m_b - eb);
+    // P as the A operand of P V: rows a / b, keys 2cq (+1) and + 8
+    uint32_t pa4[4];
+    pa4[0] = pack_bf16x2(exp2f(y[0] - ea), exp2f(y[1] - ea));
+    pa4[1] = pack_bf16x2(exp2f(y[4] - eb), exp2f(y[5] - eb));
+    pa4[2] = pack_bf16x2(exp2f(y[2] - ea), exp2f(y[3] - ea));
+    pa4[3] = pack_bf16x2(exp2f(y[6] - eb), exp2f(y[7] - eb));
+    float la = (bf16_lo(pa4[0]) + bf16_hi(pa4[0])) + (bf16_lo(pa4[2]) + bf16_hi(pa4[2]));
+    float lb = (bf16_lo(pa4[1]) + bf16_hi(pa4[1])) + (bf16_lo(pa4[3]) + bf16_hi(pa4[3]));
+    l_a = l_a * aa + la;
+    l_b = l_b * ab + lb;
+    m_a = mna;
+    m_b = mnb;
+    if (__any_sync(0xffffffffu, aa != 1.f || ab != 1.f)) {
+#pragma unroll
+      for (int db = 0; db < D / 8; ++db) {
+        o[db][0] *= aa;
+        o[db][1] *= aa;
+        o[db][2] *= ab;
+        o[db][3] *= ab;
+      }
+    }
+    // V rows past the context are zeroed (stale or NaN slots)
+    const int valid = min(kTile, ctx - t0);
+    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+    const bool masked = valid < kTile;
+    if (masked) {
+      const int kr = (lane & 3) * 2;  // .trans: this lane holds keys kr, kr+1 (+8)
+      vm0 = (kr < valid ? 0x0000ffffu : 0u) | (kr + 1 < valid ? 0xffff0000u : 0u);
+      vm1 = (kr + 8 < valid ? 0x0000ffffu : 0u) | (kr + 9 < valid ? 0xffff0000u : 0u);
+    }
+    {
+      // O += P V: B operand of V via ldmatrix.trans, dim blocks 2 d2 and 2 d2 + 1
+      const int key = 8 * (mi & 1) + (lane & 7);
+#pragma unroll
+      for (int d2 = 0; d2 < D / 16; ++d2) {
+        const int cg = 2 * d2 + (mi >> 1);
+        uint32_t vb[4];  // (keys 0-7, dims 16 d2..+7), (keys 8-15, ..), (0-7, +8..), (8-15, +8..)
+        ldsm_x4_trans(sV + (cg >> 3) * kHalfBytes + key * 128 + (((cg & 7) ^ (key & 7)) << 4),
+                      vb);
+        if (masked) {
+          vb[0] &= vm0;
+          vb[1] &= vm1;
+          vb[2] &= vm0;
+          vb[3] &= vm1;
+        }
+        mma_bf16_16816(o[2 * d2], pa4, vb[0], vb[1]);
+        mma_bf16_16816(o[2 * d2 + 1], pa4, vb[2], vb[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+  }
+  if (__any_sync(0xffffffffu, *abort_flag)) return;
+
+  // ---- rows out: sum the row sums over the 4 lanes of a row, normalise ------
+#pragma unroll
+  for (int off = 1; off < 4; off <<= 1) {
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, off);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, off);
+  }
+  const float ia = l_a > 0.f ? 1.f / l_a : 0.f, ib = l_b > 0.f ? 1.f / l_b : 0.f;
+  if (ra < rows) {
+    __nv_bfloat16* dst =
+        p.out + ((size_t)(row0 + ra / G) * p.num_q_heads + kvh * G + ra % G) * D + 2 * cq;
+#pragma unroll
+    for (int db = 0; db < D / 8; ++db)
+      *reinterpret_cast<uint32_t*>(dst + 8 * db) = pack_bf16x2(o[db][0] * ia, o[db][1] * ia);
+  }
+  if (rbw < rows) {
+    __nv_bfloat16* dst =
+        p.out + ((size_t)(row0 + rbw / G) * p.num_q_heads + kvh * G + rbw % G) * D + 2 * cq;
+#pragma unroll
+    for (int db = 0; db < D / 8; ++db)
+      *reinterpret_cast<uint32_t*>(dst + 8 * db) = pack_bf16x2(o[db][2] * ib, o[db][3] * ib);
+  }
+}
+
+template <int D, bool kTma>
+pa_status launch_rowblock(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& prm,
+                          int B, int num_kv_heads, int max_rows, cudaStream_t stream) {
+  using L = RowSmem<D>;
+  auto kern = rowblock_decode_kernel<D, kTma>;
+  const int threads = (kRowWarps + 1) * 32;
+  const pa_status s = prepare_kernel(reinterpret_cast<const void*>(kern), threads, L::kAlloc,
+                                     nullptr);
+  if (s != PA_OK) return s;
+  const int nrb = (max_rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  if (nrb > 0x7fffffff / 2) return PA_ERR_UNSUPPORTED;
+  dim3 grid(nrb, num_kv_heads, B);
+  kern<<<grid, threads, L::kAlloc, stream>>>(mk, mv, prm);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
 // the work-balanced persistent schedule
 // ---------------------------------------------------------------------------
 
@@ -714,7 +997,11 @@ extern "C" pa_status pa_decode_multi(const void* q, const void* k_cache, const v
   if (s != PA_OK) return s;
   if (!q_start) return PA_ERR_INVALID_ARG;
   const int G = num_q_heads / num_kv_heads;
-  if ((long long)max_q_len * G > kMaxColumnWarps * 8) return PA_ERR_UNSUPPORTED;
+  // more (token, head) rows than the n side holds: the row-block kernel
+  // (no context split: its many row blocks fill the GPU)
+  const bool long_chunk = (long long)max_q_len * G > kMaxColumnWarps * 8;
+  if (long_chunk && split_tokens > 0) return PA_ERR_UNSUPPORTED;
+  if ((long long)max_q_len * G > (1LL << 30)) return PA_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
   if (split_tokens > 0) {
     if (split_tokens % kTile) return PA_ERR_INVALID_ARG;
@@ -764,6 +1051,14 @@ extern "C" pa_status pa_decode_multi(const void* q, const void* k_cache, const v
     if (!make_cache_map(&mk, k_cache, num_kv_heads, head_dim, rows, box_rows) ||
         !make_cache_map(&mv, v_cache, num_kv_heads, head_dim, rows, box_rows))
       return PA_ERR_CUDA;
+  }
+  if (long_chunk) {
+    const int max_rows = max_q_len * G;
+    if (head_dim == 128)
+      return tma ? launch_rowblock<128, true>(mk, mv, prm, num_seqs, num_kv_heads, max_rows, st)
+                 : launch_rowblock<128, false>(mk, mv, prm, num_seqs, num_kv_heads, max_rows, st);
+    return tma ? launch_rowblock<64, true>(mk, mv, prm, num_seqs, num_kv_heads, max_rows, st)
+               : launch_rowblock<64, false>(mk, mv, prm, num_seqs, num_kv_heads, max_rows, st);
   }
   if (head_dim == 128)
     return tma ? launch_multi<128, true>(mk, mv, prm, nc, num_seqs, num_kv_heads, st)

@@ -95,6 +95,56 @@ def test_balanced_multi_cut_units_and_sequences_without_rows(cuda_lib, lens):
     assert b.pa_last_device_error() == 0
 
 
+@pytest.mark.parametrize("qmax,hq,hkv,d,bs", [
+    (9, 8, 1, 128, 16), (40, 64, 8, 128, 16), (300, 8, 1, 128, 16), (100, 16, 4, 64, 16),
+    (70, 8, 2, 128, 8), (33, 8, 2, 128, 1), (65, 2, 2, 128, 32)])
+def test_long_chunks_match_oracle(cuda_lib, qmax, hq, hkv, d, bs):
+    # more (token, head) rows than 64: the row-block kernel, every sequence of
+    # the batch (short ones too) on it
+    rng = np.random.default_rng(qmax + hq + bs)
+    ctx0 = [0, 5, 17, 200, 1000, 3]
+    qlens = [int(x) for x in rng.integers(1, qmax + 1, len(ctx0))]
+    qlens[0] = qmax
+    case = wl.make_multi_case("long", 90 + qmax, ctx0, qlens, hq, hkv, d, bs)
+    out = run_multi(cuda_lib, case)
+    P.assert_close(P.to_f64(out), oracle_multi(case), f"chunk <= {qmax}, G={hq // hkv}")
+
+
+def test_long_prompt_in_large_chunks_equals_full_causal_attention(cuda_lib):
+    b = cuda_lib
+    n, hq, hkv, d, bs = 700, 64, 8, 128, 16
+    full = wl.make_multi_case("bigchunks", 62, [0], [n], hq, hkv, d, bs)
+    k, v = full.k_cache.cuda(), full.v_cache.cuda()
+    bt = full.block_tables.cuda()
+    kc, vc = pa.kv_append(wl.bits(full.k_cache), wl.bits(full.v_cache), wl.bits(full.k_new),
+                          wl.bits(full.v_new), full.slot_mapping.numpy())
+    sub = list(range(0, n, 7)) + [n - 1]
+    want = oracle.decode_multi(wl.bits(full.q), kc, vc, full.block_tables.numpy(),
+                               np.array([n]), np.array([0, n]), full.scale)
+    got = np.zeros_like(want)
+    a = 0
+    for c in [256, 5, 256, 183]:
+        sl = slice(a, a + c)
+        b.pa_kv_append(full.k_new[sl].cuda(), full.v_new[sl].cuda(),
+                       full.slot_mapping[sl].cuda(), k, v)
+        out = b.decode_multi(full.q[sl].cuda(), k, v, bt,
+                             torch.tensor([a + c], dtype=torch.int32, device="cuda"),
+                             torch.tensor([0, c], dtype=torch.int32, device="cuda"), c,
+                             full.scale)
+        torch.cuda.synchronize()
+        got[sl] = P.to_f64(out)
+        a += c
+    P.assert_close(got[sub], want[sub], "4 chunks of a 700-token prompt")
+
+
+def test_long_chunks_refuse_context_splits(cuda_lib):
+    b = cuda_lib
+    case = wl.make_multi_case("ls", 63, [10], [20], 64, 8, 128, 16)
+    with pytest.raises(b.PagedKVError) as e:
+        run_multi(b, case, split=64)
+    assert e.value.status == -2
+
+
 @pytest.mark.parametrize("split", [16, 64, 256])
 def test_multi_with_context_splits(cuda_lib, split):
     case = wl.make_multi_case("mqs", 50 + split, [0, 3, 60, 300, 1000, 33], [4, 2, 8, 1, 8, 5],
@@ -151,9 +201,15 @@ def test_multi_argument_checks(cuda_lib):
     q, k, v = case.q.cuda(), case.k_cache.cuda(), case.v_cache.cuda()
     bt, cl, qs = case.block_tables.cuda(), case.context_lens.cuda(), case.q_start.cuda()
     out = torch.empty_like(q)
+    ws = torch.zeros(b.pa_decode_multi_balanced_workspace_bytes(2, 2, 128), dtype=torch.uint8,
+                     device="cuda")
     with pytest.raises(b.PagedKVError) as e:       # 9 tokens x 8 heads > 64 columns
-        b.pa_decode_multi(q, k, v, bt, cl, qs, 9, case.scale, out)
+        b.pa_decode_multi_balanced(q, k, v, bt, cl, qs, 9, case.scale, ws, out)
     assert e.value.status == -2
+    b.pa_kv_append(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), k, v)
+    b.pa_decode_multi(q, k, v, bt, cl, qs, 9, case.scale, out)   # the row-block kernel
+    torch.cuda.synchronize()
+    P.assert_close(P.to_f64(out), oracle_multi(case), "max_q_len 9 on the row-block kernel")
     with pytest.raises(b.PagedKVError) as e:       # split mode without buffers
         b._check("pa_decode_multi", b._lib.pa_decode_multi(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), bt.data_ptr(), bt.shape[1], cl.data_ptr(),
