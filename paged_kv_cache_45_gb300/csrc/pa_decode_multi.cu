@@ -31,7 +31,10 @@
 
 #include <math.h>
 
+#include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <vector>
 
 #include "pa_balance.cuh"
@@ -968,6 +971,31 @@ pa_status check_q_start(const int32_t* q_start, const int32_t* context_lens, int
   return PA_OK;
 }
 
+// PA_PREFILL_KERNEL=rowblock runs long chunks on the mma.sync row-block
+// kernel instead of the tcgen05 one (read at every call).
+bool prefill_rowblock_forced() {
+  const char* v = std::getenv("PA_PREFILL_KERNEL");
+  return v && std::strcmp(v, "rowblock") == 0;
+}
+
+// Device address of this unit's error word (looked up once per device).
+unsigned int* multi_error_word() {
+  static std::mutex mu;
+  static std::map<int, unsigned int*> addr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = addr.find(dev);
+  if (it != addr.end()) return it->second;
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_multi_error) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  addr[dev] = static_cast<unsigned int*>(ptr);
+  return static_cast<unsigned int*>(ptr);
+}
+
 }  // namespace
 
 unsigned int take_multi_errors() {
@@ -1051,6 +1079,13 @@ extern "C" pa_status pa_decode_multi(const void* q, const void* k_cache, const v
     if (!make_cache_map(&mk, k_cache, num_kv_heads, head_dim, rows, box_rows) ||
         !make_cache_map(&mv, v_cache, num_kv_heads, head_dim, rows, box_rows))
       return PA_ERR_CUDA;
+  }
+  if (long_chunk && prefill_tc_supported(head_dim, block_size, G) && !prefill_rowblock_forced()) {
+    unsigned int* err = multi_error_word();
+    if (!err) return PA_ERR_CUDA;
+    return launch_prefill_tc(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                             q_start, num_seqs, max_q_len, num_q_heads, num_kv_heads, block_size,
+                             num_blocks, scale, out, err, st);
   }
   if (long_chunk) {
     const int max_rows = max_q_len * G;

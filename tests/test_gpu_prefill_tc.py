@@ -1,0 +1,110 @@
+"""GPU parity for long query chunks (chunked prefill) on the tcgen05 kernel of
+pa_decode_multi, and on the mma.sync row-block kernel it replaces
+(PA_PREFILL_KERNEL=rowblock), against the fp64 oracle's causal attention.
+
+Covers query groups that divide the 256-row block and ones that leave padding
+rows (G = 6), block sizes 8..256 (one TMA box
+per block, or a 128-key tile inside one block), chunks spanning many 128-key
+tiles with ragged tails, cached prefixes that are not tile multiples, pools
+whose unowned slots are NaN (masked keys and zeroed V rows must keep them
+out), rows before position 0, repeatability, and the chunked-prefill bench
+step (8 x 2048 new tokens after 6144 cached, 64/8 heads) on sampled rows.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import paged_attention as pa
+from paged_kv_cache_45_gb300 import workloads as wl
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = ["tcgen05", "rowblock"]
+
+
+@pytest.fixture(params=KERNELS)
+def kernel(request, monkeypatch):
+    if request.param == "rowblock":
+        monkeypatch.setenv("PA_PREFILL_KERNEL", "rowblock")
+    else:
+        monkeypatch.delenv("PA_PREFILL_KERNEL", raising=False)
+    return request.param
+
+
+def appended(case):
+    return pa.kv_append(wl.bits(case.k_cache), wl.bits(case.v_cache), wl.bits(case.k_new),
+                        wl.bits(case.v_new), case.slot_mapping.numpy())
+
+
+def run(b, case, context_lens=None):
+    k, v = case.k_cache.cuda(), case.v_cache.cuda()
+    b.pa_kv_append(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), k, v)
+    cl = case.context_lens if context_lens is None else context_lens
+    out = b.decode_multi(case.q.cuda(), k, v, case.block_tables.cuda(), cl.cuda(),
+                         case.q_start.cuda(), case.max_q_len, case.scale)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("hq,hkv,bs,ctx0,qlens", [
+    (64, 8, 16, [0, 100, 1000, 7], [300, 129, 40, 257]),      # G 8: 32 tokens a block
+    (8, 8, 16, [0, 250], [600, 513]),                          # G 1: 256 tokens a block
+    (32, 8, 32, [3, 0, 129], [130, 77, 200]),                  # G 4
+    (12, 2, 16, [50, 0], [90, 43]),                            # G 6: 42 tokens, 4 padding rows
+    (8, 1, 64, [10, 300], [5, 30]),                            # one KV head, block_size 64
+    (16, 2, 8, [0, 31], [100, 70]),                            # block_size 8
+    (16, 2, 128, [0, 200], [160, 300]),                        # one block per 128-key tile
+    (16, 2, 256, [100, 0, 600], [200, 90, 40]),                # a tile inside one block
+])
+def test_long_chunks_match_oracle(cuda_lib, kernel, hq, hkv, bs, ctx0, qlens):
+    case = wl.make_multi_case("tc", 7 + hq + bs + len(ctx0), ctx0, qlens, hq, hkv, 128, bs)
+    out = run(cuda_lib, case)
+    kc, vc = appended(case)
+    want = oracle.decode_multi(wl.bits(case.q), kc, vc, case.block_tables.numpy(),
+                               case.context_lens.numpy(), case.q_start.numpy(), case.scale)
+    P.assert_close(P.to_f64(out), want, f"{kernel} G={hq // hkv} bs={bs}")
+    assert cuda_lib.pa_last_device_error() == 0
+
+
+def test_rows_before_position_zero_are_zero(cuda_lib, kernel):
+    # a context shorter than the chunk: the first rows have no position
+    case = wl.make_multi_case("tcz", 5, [0, 40], [200, 150], 16, 2, 128, 16)
+    short = case.context_lens.clone()
+    short[0] = 130                               # tokens 0..69 of sequence 0 sit before 0
+    out = run(cuda_lib, case, context_lens=short)
+    kc, vc = appended(case)
+    want = oracle.decode_multi(wl.bits(case.q), kc, vc, case.block_tables.numpy(),
+                               short.numpy(), case.q_start.numpy(), case.scale)
+    got = P.to_f64(out)
+    assert not got[:70].any()
+    P.assert_close(got, want, f"{kernel} rows before position 0")
+
+
+def test_repeatable_bit_for_bit(cuda_lib):
+    case = wl.make_multi_case("tcr", 9, [500, 20], [400, 333], 64, 8, 128, 16)
+    a = run(cuda_lib, case)
+    b_ = run(cuda_lib, case)
+    assert torch.equal(a.view(torch.int16), b_.view(torch.int16))
+
+
+def test_prefill_bench_step_on_sampled_rows(cuda_lib):
+    # the bench's chunked-prefill step: 8 sequences, 2048 new tokens after
+    # 6144 cached, 64 q heads / 8 KV heads; rows sampled across every
+    # sequence (first, diagonal-tile and last tokens), each checked alone
+    case = wl.make_multi_case("prefill", 0, [6144] * 8, [2048] * 8, 64, 8, 128, 16)
+    out = P.to_f64(run(cuda_lib, case))
+    kc, vc = appended(case)
+    q = wl.bits(case.q)
+    bt = case.block_tables.numpy()
+    rng = np.random.default_rng(5)
+    for s in range(8):
+        picks = sorted({0, 1, 31, 32, 127, 128, 2047} | set(rng.integers(0, 2048, 3).tolist()))
+        for i in picks:
+            row = s * 2048 + i
+            want = oracle.decode_multi(q[row:row + 1], kc, vc, bt[s:s + 1],
+                                       np.array([6144 + i + 1]), np.array([0, 1]), case.scale)
+            P.assert_close(out[row:row + 1], want, f"sequence {s} token {i}")
+    assert cuda_lib.pa_last_device_error() == 0
