@@ -106,7 +106,7 @@ def describe(workload: str, batch: int = 256) -> str:
         "prefill": "chunked prefill, 70B shape: 8 sequences each bringing a 2048-token chunk "
                    "after 6144 cached tokens (causal), 64 q heads / 8 KV heads, head_dim 128, "
                    "bf16, block_size 16; pa_kv_append of the chunk + pa_decode_multi "
-                   "(row-block kernel)",
+                   "(tcgen05 kernel)",
         "spec": "speculative verification, 70B shape: B={batch} sequences, ctx log-uniform "
                 "[128, 8192], 4 new query tokens each (causal), 64 q heads / 8 KV heads, "
                 "head_dim 128, bf16, block_size 16; pa_kv_append of the 4 rows + "
@@ -283,6 +283,7 @@ KERNEL_SOURCES = {   # the files whose change invalidates a kernel's recorded DR
                               "pa_device.cuh", "pa_api.cu"),
     "rowblock_decode_kernel": ("pa_decode_multi.cu", "pa_tile.cuh", "pa_device.cuh",
                                "pa_api.cu"),
+    "prefill_tc_kernel": ("pa_prefill_tc.cu", "pa_umma.cuh", "pa_device.cuh"),
 }
 
 
@@ -627,7 +628,8 @@ def run_gpu(args):
         else (("balanced_multi_kernel" if ws.multi_balanced else "multi_decode_kernel")
               if steps.multi else "paged_decode_kernel")
     if args.workload == "prefill":
-        kernel = "rowblock_decode_kernel"
+        kernel = ("rowblock_decode_kernel" if os.environ.get("PA_PREFILL_KERNEL") == "rowblock"
+                  else "prefill_tc_kernel")
     traffic = traffic_per_launch(kernel, kv_tokens_per_launch)
     clocks = sampler.summary() if sampler else None
     prefill = args.workload == "prefill"
@@ -655,8 +657,11 @@ def run_gpu(args):
         "data": "synthetic (seeded N(0,1) bf16 q/K/V; seeded lengths and block placement)",
         "config": {"workload": describe(args.workload, args.batch) +
                    (" (e4m3 KV pool, per-KV-head scales)" if steps.fp8 else ""),
-                   "schedule": "row blocks (64 (token, head) rows x KV head x sequence per "
-                               "block, unsplit)" if args.workload == "prefill" else
+                   "schedule": ("row blocks (64 (token, head) rows x KV head x sequence per "
+                                "block, unsplit, mma.sync)"
+                                if os.environ.get("PA_PREFILL_KERNEL") == "rowblock" else
+                                "tcgen05 blocks (256 (token, head) rows x KV head x sequence, "
+                                "unsplit)") if args.workload == "prefill" else
                    "balanced" if ws.balanced else
                    (("multi, balanced persistent (pa_decode_multi_balanced)"
                      if ws.multi_balanced else
@@ -700,7 +705,7 @@ def run_gpu(args):
         line["roofline"] = {
             "bound": "tensor", "kernel": kernel, "achieved": round(kern_tflops, 2),
             "peak": tpeak, "unit": "TFLOP/s", "frac": round(kern_tflops / tpeak, 4),
-            "peak_kind": f"{tkind} bf16_tflops (cuBLAS burst; this kernel uses mma.sync)",
+            "peak_kind": f"{tkind} bf16_tflops (cuBLAS burst)",
             "traffic": None if traffic is None else int(traffic),
             "algorithmic_flops_per_launch": int(flops),
             "measured": f"CUDA events around each decode launch, {KI} steps"}

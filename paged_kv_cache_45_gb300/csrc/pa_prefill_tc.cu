@@ -11,31 +11,33 @@
 // are a dense contraction, so they run on tcgen05.mma with the accumulators
 // in tensor memory.
 //
-// One thread block per (KV head, sequence, row tile counted from the chunk's
-// end), 256 query rows = two M = 128 tiles (row = token * G + head; a tile
-// covers floor(256 / G) tokens), 10 warps:
-//   warp 0     loader: K and V tiles of 128 keys through one 3-slot ring (K_j
-//              then V_j), each block's rows fetched by two TMA boxes {64
-//              columns, rows} with the 128-byte swizzle, i.e. the K-major
-//              layout the MMA reads for K and the MN-major one for V;
+// One thread block per (row tile counted from the chunk's end, KV head,
+// sequence), 256 query rows = two M = 128 tiles (row = token * G + head; a
+// block covers floor(256 / G) tokens), 10 warps:
+//   warp 0     loader: K_j and V_j tiles of 128 keys through a 5-slot ring;
+//              a paged block's rows of one head land with ONE 4-D TMA box
+//              (64 columns x 8 rows x both 128-byte halves x block_size / 8
+//              row groups, 128-byte swizzle), lane i issuing box i so that
+//              the boxes' issue costs overlap;
 //   warp 1     allocates 512 TMEM columns (S_0, S_1 scores, O_0, O_1 outputs)
-//              and one lane issues every MMA:
-//                S_w = Q_w K_j^T  (M 128, N 128 keys, K 128 = head_dim)
-//                O_w += P_w V_j   (M 128, N 128 = head_dim, K 128 keys)
-//              in the order S_0(j), S_1(j), PV_0(j), S_0(j+1), PV_1(j),
-//              S_1(j+1), ... so that the tensor cores work on one tile's
-//              products while the other tile's softmax runs;
+//              and one lane issues every MMA, descriptors built once:
+//                S_w = Q_w K_j^T  (SS: M 128, N 128 keys, K 128 = head_dim)
+//                O_w += P_w V_j   (TS: P_w from TMEM, M 128, N 128, K 128 keys)
+//              in the order P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1), ... so the
+//              tensor cores work on one tile's products while the other
+//              tile's softmax runs;
 //   warps 2-9  two softmax warpgroups, one per Q tile, one thread per row:
 //              read the row's 128 scores from TMEM, apply the causal limit,
 //              take the online softmax in base 2 (the running output is
 //              rescaled only when the running max grew by more than 2^8 --
 //              exact, as the final division uses the same stale max), write
-//              P as bf16 into shared memory in the K-major swizzled layout,
-//              and after the last tile divide O by the row sum and store bf16.
-// The key range of a block is [0, last position of its last token]; the
-// rows past a row's own position in the diagonal tiles are masked, and V
-// rows past the block's last position are zeroed before the last P.V (they
-// may be unwritten slots).
+//              P as bf16 pairs into the first 64 columns of S_w (the next
+//              S_w is issued after P_w V_j, and the pipe runs in order), and
+//              after the last tile divide O by the row sum and store bf16.
+// The key range of a block is [0, last position of its last token]; blocks
+// of one sequence and head fold its tiles in rotated orders. Keys past a
+// row's own position are masked, and V rows past the block's last position
+// are zeroed before their P.V (they may be unwritten slots).
 
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -55,8 +57,13 @@ constexpr int kTcD = 128;                          // head_dim
 constexpr int kTcRows = 128;                       // rows per Q tile (MMA M)
 constexpr int kTcQTiles = 2;                       // Q tiles per block
 constexpr int kTcKeys = 128;                       // keys per K/V tile
-constexpr int kTcSlots = 3;                        // K/V ring slots
-constexpr int kTcPanel = kTcRows * 128;            // one 64-column panel: 16 KB
+constexpr int kTcSlots = 5;                        // K/V ring slots
+constexpr int kTcPanel = kTcRows * 128;            // Q: one 64-column panel, 16 KB
+// K/V slots hold 8-row groups of both 64-column halves: group g, half h at
+// g * kKvGroup + h * kKvHalf (each 1 KB = 8 rows of 128 bytes, swizzled), the
+// layout one 4-D TMA box per paged block writes.
+constexpr int kKvHalf = 1024;
+constexpr int kKvGroup = 2048;
 constexpr int kTcTileBytes = 2 * kTcPanel;         // 128 rows x 256 B: 32 KB
 constexpr int kTcSoftmaxWarps = 4 * kTcQTiles;
 constexpr int kTcThreads = (2 + kTcSoftmaxWarps) * 32;
@@ -65,11 +72,10 @@ constexpr float kRescaleLog2 = 8.0f;               // rescale O when the max gro
 
 struct TcSmem {
   static constexpr int kQ = 0;                                   // Q_0, Q_1
-  static constexpr int kP = kQ + kTcQTiles * kTcTileBytes;       // P_0, P_1
-  static constexpr int kRing = kP + kTcQTiles * kTcTileBytes;    // 3 K/V slots
+  static constexpr int kRing = kQ + kTcQTiles * kTcTileBytes;    // K/V slots
   static constexpr int kBar = kRing + kTcSlots * kTcTileBytes;
-  // barriers: full[3], empty[3], s_full[2], p_full[2], o_done[2], q_ready, drain
-  static constexpr int kNumBars = 2 * kTcSlots + 3 * kTcQTiles + 2;
+  // barriers: full[5], empty[5], s_full[2], p_full[2], q_ready, o_final
+  static constexpr int kNumBars = 2 * kTcSlots + 2 * kTcQTiles + 2;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kFlag = kTmemSlot + 8;
   static constexpr int kAlloc = kFlag + 8 + 1024;                // + 1024-byte alignment
@@ -122,6 +128,16 @@ __device__ __forceinline__ uint32_t sw_chunk(int r, int c) {
   return (uint32_t)((c >> 3) * kTcPanel + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+// 4-D TMA tile load (coordinates innermost first), completion on `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -137,24 +153,31 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
   return v;
 }
 
+// Ring position of K_i and V_i: K0 V0 K1 V1 ..., the order the MMAs consume them in.
+__device__ __forceinline__ int k_seq(int i) { return 2 * i; }
+__device__ __forceinline__ int v_seq(int i) { return 2 * i + 1; }
+
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const TcParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int kvh = blockIdx.x;
-  const int b = blockIdx.y;
+  // blockIdx.x counts row tiles from the chunk's end (longest key range
+  // first); a sequence's row tiles are neighbours in launch order, so the
+  // blocks running together share its K/V in L2.
+  const int kvh = blockIdx.y;
+  const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.group;
   const int TPB = p.tokens_per_block;
   const int row0 = p.q_start[b];
   const int n = p.q_start[b + 1] - row0;
-  const int tok_hi = n - (int)blockIdx.z * TPB;  // this block: chunk tokens [tok_lo, tok_hi)
+  const int tok_hi = n - (int)blockIdx.x * TPB;  // this block: chunk tokens [tok_lo, tok_hi)
   if (tok_hi <= 0) return;
   if (n > p.max_q_len) {
-    if (threadIdx.x == 0 && blockIdx.z == 0) atomicOr(p.err, kErrShape);
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.err, kErrShape);
     return;
   }
   const int tok_lo = tok_hi - TPB > 0 ? tok_hi - TPB : 0;
@@ -164,6 +187,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int pos_base = ctx - n;                 // position of the chunk's token 0
   const int pos_last = pos_base + tok_hi - 1;   // the block's last attended position
   const int n_tiles = pos_last >= 0 ? pos_last / kTcKeys + 1 : 0;
+  // Iteration i folds key tile (i + rot) mod n_tiles: the blocks of one
+  // sequence and KV head run together, and a rotation of their order keeps
+  // them from all reading the same tile (the same L2 lines) at the same time.
+  const int rot = n_tiles > 0 ? (int)((blockIdx.x * 7u) % (unsigned)n_tiles) : 0;
+  auto tile_of = [&](int i) { return i + rot < n_tiles ? i + rot : i + rot - n_tiles; };
 
   // softmax thread -> (Q tile, row); rows past the block's tokens are padding
   const int sw = warp - 2;                      // softmax warp 0..7
@@ -189,13 +217,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* empty = full + kTcSlots;
   uint64_t* s_full = empty + kTcSlots;
   uint64_t* p_full = s_full + kTcQTiles;
-  uint64_t* o_done = p_full + kTcQTiles;
-  uint64_t* q_ready = o_done + kTcQTiles;
-  uint64_t* drain = q_ready + 1;
+  uint64_t* q_ready = p_full + kTcQTiles;
+  uint64_t* o_final = q_ready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TcSmem::kTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + TcSmem::kFlag);
   const uint32_t sQ = smem_u32(smem + TcSmem::kQ);
-  const uint32_t sP = smem_u32(smem + TcSmem::kP);
   const uint32_t ring = smem_u32(smem + TcSmem::kRing);
 
   if (threadIdx.x == 0) {
@@ -205,11 +231,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int w = 0; w < kTcQTiles; ++w) {
       mbar_init(&s_full[w], 1);
-      mbar_init(&p_full[w], kTcRows);
-      mbar_init(&o_done[w], 1);
+      mbar_init(&p_full[w], kTcRows / 32);  // one arrival per softmax warp
     }
-    mbar_init(q_ready, kTcQTiles * kTcRows);
-    mbar_init(drain, 1);
+    mbar_init(q_ready, kTcSoftmaxWarps);
+    mbar_init(o_final, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -224,37 +249,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ loader
+    // The whole warp holds 32 consecutive block-table entries (one coalesced
+    // read per refill, bt[ent_base + lane]); lane i issues the tile's box i.
     if (lane == 0) {
       prefetch_tensormap(&tmap_k);
       prefetch_tensormap(&tmap_v);
-      const int32_t* bt = p.block_tables + (size_t)b * p.max_blocks;
-      const int rb = p.box_rows;
-      const int boxes = kTcKeys / rb;
-      int L = 0;
-      for (; L < 2 * n_tiles; ++L) {
-        const int slot = L % kTcSlots;
-        if (L >= kTcSlots &&
-            !wait_or_abort(&empty[slot], ((L / kTcSlots) - 1) & 1, abort_flag)) {
-          give_up(abort_flag, p.err, kErrWaitEmpty);
-          break;
-        }
-        const int j = L >> 1;
-        const CUtensorMap* map = (L & 1) ? &tmap_v : &tmap_k;
-        const int nbox = min(boxes, (pos_last - j * kTcKeys) / rb + 1);
-        mbar_arrive_expect_tx(&full[slot], (uint32_t)(nbox * rb * 256));
-        const uint32_t dst = ring + slot * kTcTileBytes;
-        for (int i = 0; i < nbox; ++i) {
-          const int key0 = j * kTcKeys + i * rb;
-          const int blk = bt[key0 >> p.log2_bs];
-          // a block id outside the pool reads zeros (a box wholly out of range)
-          const int y = (blk >= 0 && blk < p.num_blocks)
-                            ? blk * p.block_size + (key0 & (p.block_size - 1))
-                            : -rb;
-          tma_load_2d(dst + i * rb * 128, map, kvh * kTcD, y, &full[slot]);
-          tma_load_2d(dst + kTcPanel + i * rb * 128, map, kvh * kTcD + 64, y, &full[slot]);
-        }
+    }
+    const int32_t* bt = p.block_tables + (size_t)b * p.max_blocks;
+    const int rb = p.box_rows;
+    const int boxes = kTcKeys / rb;
+    const int n_entries = (pos_last >> p.log2_bs) + 1;      // entries the block reads
+    int ent_base = -(1 << 30);
+    int ent_val = -1;
+    int L = 0;
+    for (; L < 2 * n_tiles; ++L) {
+      const int slot = L % kTcSlots;
+      if (L >= kTcSlots &&
+          !__all_sync(0xffffffffu, wait_or_abort(&empty[slot], ((L / kTcSlots) - 1) & 1,
+                                                 abort_flag))) {
+        if (lane == 0) give_up(abort_flag, p.err, kErrWaitEmpty);
+        break;
       }
-      // every copy issued must land before the block ends
+      const bool is_v = (L & 1) != 0;  // L = 2 j: K_j, L = 2 j + 1: V_j
+      const int j = tile_of(L >> 1);
+      const CUtensorMap* map = is_v ? &tmap_v : &tmap_k;
+      const int nbox = min(boxes, (pos_last - j * kTcKeys) / rb + 1);
+      const int e_first = (j * kTcKeys) >> p.log2_bs;
+      const int e_last = (j * kTcKeys + nbox * rb - 1) >> p.log2_bs;
+      if (e_first < ent_base || e_last >= ent_base + 32) {  // warp-uniform refill
+        ent_base = e_first;
+        const int idx = ent_base + lane;
+        ent_val = idx < n_entries ? bt[idx] : -1;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(nbox * rb * 256));
+      // one box per lane, issued together: a TMA instruction costs a lane a
+      // few hundred cycles, and lanes overlap them
+      const uint32_t dst = ring + slot * kTcTileBytes;
+      const int i = lane < nbox ? lane : 0;
+      const int key0 = j * kTcKeys + i * rb;
+      const int blk = __shfl_sync(0xffffffffu, ent_val, (key0 >> p.log2_bs) - ent_base);
+      if (lane < nbox) {
+        // rb rows (rb / 8 groups) x both halves of this head; a block id
+        // outside the pool reads zeros (a box wholly out of range)
+        const int grp = (blk >= 0 && blk < p.num_blocks)
+                            ? (blk * p.block_size + (key0 & (p.block_size - 1))) >> 3
+                            : -(rb >> 3);
+        tma_load_4d(dst + (i * rb >> 3) * kKvGroup, map, 0, 0, 2 * kvh, grp, &full[slot]);
+      }
+    }
+    // every copy issued must land before the block ends
+    if (lane == 0) {
       for (int s = 0; s < kTcSlots; ++s) {
         if (L <= s) continue;
         const int last = s + ((L - 1 - s) / kTcSlots) * kTcSlots;
@@ -266,73 +310,77 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = umma_idesc_bf16(kTcRows, kTcKeys, false);
       constexpr uint32_t kIdO = umma_idesc_bf16(kTcRows, kTcD, true);
-      auto issue_s = [&](int w, int L) {  // S_w = Q_w K^T, K in slot L % 3
-        const uint32_t qa = sQ + w * kTcTileBytes;
-        const uint32_t kb = ring + (L % kTcSlots) * kTcTileBytes;
+      // Descriptors are built once; a k-step or a slot moves only the start
+      // address (bits 0-13, address >> 4), so each MMA costs one 64-bit add.
+      // (Building them per MMA made the issuing thread, not the tensor pipe,
+      // the bottleneck.)
+      constexpr uint64_t kTileStep = kTcTileBytes >> 4;
+      const uint64_t d_q = umma_desc_sw128(sQ, 16, 1024);             // Q_0, K-major
+      const uint64_t d_k = umma_desc_sw128(ring, 16, kKvGroup);          // slot 0, K-major
+      const uint64_t d_v = umma_desc_sw128(ring, kKvHalf, kKvGroup);     // slot 0, MN-major
+      auto issue_s = [&](int w, int L) {  // S_w = Q_w K^T, K in slot L % kTcSlots
+        const uint64_t qd = d_q + (uint64_t)w * kTileStep;
+        const uint64_t kd = d_k + (uint64_t)(L % kTcSlots) * kTileStep;
+        const uint32_t dst = tmem + w * kTcKeys;
 #pragma unroll
         for (int kk = 0; kk < kTcD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kTcPanel + (kk & 3) * 32;
-          umma_bf16_ss(tmem + w * kTcKeys, umma_desc_sw128(qa + off, 16, 1024),
-                       umma_desc_sw128(kb + off, 16, 1024), kIdS, kk > 0);
+          const uint64_t qoff = (uint64_t)(((kk >> 2) * kTcPanel + (kk & 3) * 32) >> 4);
+          const uint64_t koff = (uint64_t)(((kk >> 2) * kKvHalf + (kk & 3) * 32) >> 4);
+          umma_bf16_ss(dst, qd + qoff, kd + koff, kIdS, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int w, int L, int j) {  // O_w += P_w V, V in slot L % 3
-        const uint32_t pa_ = sP + w * kTcTileBytes;
-        const uint32_t vb = ring + (L % kTcSlots) * kTcTileBytes;
+      auto issue_pv = [&](int w, int L, int j) {  // O_w += P_w V; P_w in TMEM, V in a slot
+        const uint64_t vd = d_v + (uint64_t)(L % kTcSlots) * kTileStep;
+        const uint32_t dst = tmem + 2 * kTcKeys + w * kTcD;
+        const uint32_t pa_ = tmem + w * kTcKeys;
 #pragma unroll
-        for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kTcPanel + (kk & 3) * 32;
-          umma_bf16_ss(tmem + 2 * kTcKeys + w * kTcD, umma_desc_sw128(pa_ + off, 16, 1024),
-                       umma_desc_sw128(vb + kk * 2048, kTcPanel, 1024), kIdO,
+        for (int kk = 0; kk < kTcKeys / 16; ++kk)
+          umma_bf16_ts(dst, pa_ + kk * 8, vd + (uint64_t)(kk * ((2 * kKvGroup) >> 4)), kIdO,
                        (j > 0 || kk > 0) ? 1u : 0u);
-        }
       };
       auto landed = [&](int L) {
         return wait_or_abort(&full[L % kTcSlots], (L / kTcSlots) & 1, abort_flag);
       };
-      bool ok = wait_or_abort(q_ready, 0, abort_flag) && landed(0);
+      // Tensor-pipe order: P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1), ...: while
+      // one warpgroup's softmax runs, the other's products are computed. P_w
+      // lives in S_w's columns, so S_w(j+1) follows P_w V_j (the pipe runs
+      // in issue order).
+      bool ok = wait_or_abort(q_ready, 0, abort_flag) && landed(k_seq(0));
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
+        issue_s(0, k_seq(0));
         umma_commit(&s_full[0]);
-        issue_s(1, 0);
+        issue_s(1, k_seq(0));
         umma_commit(&s_full[1]);
-        umma_commit(&empty[0]);
+        umma_commit(&empty[k_seq(0) % kTcSlots]);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int LV = 2 * j + 1, LK1 = 2 * j + 2;
         const bool more = j + 1 < n_tiles;
-        if (!(ok = landed(LV) && wait_or_abort(&p_full[0], j & 1, abort_flag))) break;
-        tc_fence_after();
-        issue_pv(0, LV, j);
-        umma_commit(&o_done[0]);
-        if (more) {
-          if (!(ok = landed(LK1))) break;
-          issue_s(0, LK1);
-          umma_commit(&s_full[0]);
-        }
-        if (!(ok = wait_or_abort(&p_full[1], j & 1, abort_flag))) break;
-        tc_fence_after();
-        issue_pv(1, LV, j);
-        umma_commit(&o_done[1]);
-        umma_commit(&empty[LV % kTcSlots]);
-        if (more) {
-          issue_s(1, LK1);
-          umma_commit(&s_full[1]);
-          umma_commit(&empty[LK1 % kTcSlots]);
+        const int LV = v_seq(j), LK = k_seq(j + 1);
+        if (!(ok = landed(LV))) break;
+        for (int w = 0; w < kTcQTiles; ++w) {
+          if (!(ok = wait_or_abort(&p_full[w], j & 1, abort_flag))) break;
+          tc_fence_after();
+          issue_pv(w, LV, j);
+          if (w == kTcQTiles - 1) umma_commit(&empty[LV % kTcSlots]);
+          if (more) {
+            if (w == 0 && !(ok = landed(LK))) break;
+            issue_s(w, LK);
+            umma_commit(&s_full[w]);
+            if (w == kTcQTiles - 1) umma_commit(&empty[LK % kTcSlots]);
+          }
         }
       }
       if (!ok) give_up(abort_flag, p.err, kErrWaitFull);
-      umma_commit(drain);  // every MMA issued is done before TMEM is freed
-      if (!mbar_wait(drain, 0)) atomicOr(p.err, kErrDrain);
+      umma_commit(o_final);  // every MMA issued is done: outputs final, TMEM free to go
+      if (!mbar_wait(o_final, 0)) atomicOr(p.err, kErrDrain);
     }
   } else {
     // ------------------------------------------------------------ softmax
     const uint32_t lanes = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t t_s = lanes + qt * kTcKeys;               // S of this tile
+    const uint32_t t_s = lanes + qt * kTcKeys;               // S of this tile; P in its first half
     const uint32_t t_o = lanes + 2 * kTcKeys + qt * kTcD;    // O of this tile
     const uint32_t my_q = sQ + qt * kTcTileBytes;
-    const uint32_t my_p = sP + qt * kTcTileBytes;
     {  // this row of Q into the K-major swizzled tile (zeros for padding rows)
       const __nv_bfloat16* src = p.q + out_off;
 #pragma unroll 4
@@ -341,47 +389,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         st_shared_v4(my_q + sw_chunk(r, c), v.x, v.y, v.z, v.w);
       }
       fence_proxy_async_smem();
-      mbar_arrive(q_ready);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
     }
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY;  // running max, log2 units (the one P and O use)
     float l_run = 0.f;        // running row sum of P
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
+      // S_w(j) done implies P_w V_{j-1} done (issued before it): O is current
+      // and S's columns may take P
       ok = __all_sync(0xffffffffu, wait_or_abort(&s_full[qt], j & 1, abort_flag));
-      if (ok && j > 0)  // PV of tile j-1 is done: its P buffer is free, O is current
-        ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[qt], (j - 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       float s[kTcKeys];
-      tmem_ld64_sync(t_s, *reinterpret_cast<float(*)[64]>(&s[0]));
-      tmem_ld64_sync(t_s + 64, *reinterpret_cast<float(*)[64]>(&s[64]));
-      const int lim = pos - j * kTcKeys;  // keys 0 .. lim of the tile are visible
+      tmem_ld128_sync(t_s, s);
+      const int tile = tile_of(j);
+      const int lim = pos - tile * kTcKeys;  // keys 0 .. lim of the tile are visible
       if (lim < kTcKeys - 1) {
 #pragma unroll
         for (int c = 0; c < kTcKeys; ++c) s[c] = c <= lim ? s[c] : -INFINITY;
       }
-      float mx = -INFINITY;
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < kTcKeys; ++c) mx = fmaxf(mx, s[c]);
+      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < kTcKeys; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_tile = mx * sl2;
       const bool grow = m_tile > m_run + kRescaleLog2;  // also the first finite max
       const float m_use = grow ? m_tile : m_run;
       const float alpha = grow ? ex2_approx(m_run - m_use) : 1.f;  // 0 when m_run = -inf
       const float ms = m_use == -INFINITY ? 0.f : m_use;
-      float sum = 0.f;
+      uint32_t pk[kTcKeys / 2];  // P row as bf16 pairs
+      float sum8[8];
 #pragma unroll
-      for (int c = 0; c < kTcKeys / 8; ++c) {
-        uint32_t w4[4];
+      for (int i = 0; i < 8; ++i) sum8[i] = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float e0 = ex2_approx(fmaf(s[8 * c + 2 * i], sl2, -ms));
-          const float e1 = ex2_approx(fmaf(s[8 * c + 2 * i + 1], sl2, -ms));
-          sum += e0 + e1;
-          w4[i] = pack_bf16x2(e0, e1);
-        }
-        st_shared_v4(my_p + sw_chunk(r, c), w4[0], w4[1], w4[2], w4[3]);
+      for (int c = 0; c < kTcKeys; c += 2) {
+        const float e0 = ex2_approx(fmaf(s[c], sl2, -ms));
+        const float e1 = ex2_approx(fmaf(s[c + 1], sl2, -ms));
+        sum8[(c >> 1) & 7] += e0 + e1;
+        pk[c >> 1] = pack_bf16x2(e0, e1);
       }
+      tmem_st64_sync(t_s, pk);
+      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                        ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       l_run = l_run * alpha + sum;
       m_run = m_use;
       if (j > 0 && __any_sync(0xffffffffu, grow)) {  // rescale the running output
@@ -394,30 +448,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tmem_st32_sync(t_o + c, o);
         }
       }
-      if (qt == 0 && j == n_tiles - 1) {
+      if (qt == 0 && tile == n_tiles - 1) {
         // the last V tile: zero its rows past the block's last position
-        const int first = pos_last - j * kTcKeys + 1;
+        const int first = pos_last - tile * kTcKeys + 1;
         if (first < kTcKeys) {
-          const int LV = 2 * j + 1;
+          const int LV = v_seq(j);
           ok = __all_sync(0xffffffffu, wait_or_abort(&full[LV % kTcSlots],
                                                       (LV / kTcSlots) & 1, abort_flag));
           if (ok) {
             const uint32_t vt = ring + (LV % kTcSlots) * kTcTileBytes;
             for (int i = r; i < (kTcKeys - first) * 16; i += kTcRows) {
               const int row = first + (i >> 4), c = i & 15;
-              st_shared_v4(vt + (c >> 3) * kTcPanel + row * 128 + (c & 7) * 16, 0, 0, 0, 0);
+              st_shared_v4(vt + (row >> 3) * kKvGroup + (c >> 3) * kKvHalf + (row & 7) * 128 +
+                               (c & 7) * 16,
+                           0, 0, 0, 0);
             }
+            fence_proxy_async_smem();
           }
         }
       }
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full[qt]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[qt]);
       if (!ok) break;
     }
-    if (ok)
-      ok = __all_sync(0xffffffffu,
-                      wait_or_abort(&o_done[qt], (n_tiles - 1) & 1, abort_flag));
+    if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(o_final, 0, abort_flag));
     if (!ok) {
       give_up(abort_flag, p.err, kErrWaitFull);
     } else {
@@ -462,16 +517,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tc_map_encoder() {
   return fn;
 }
 
-// 2-D map over a bf16 cache as [num_blocks * block_size rows, Hkv * 128
-// columns], box {64 columns, box_rows rows}, 128-byte swizzle.
+// 4-D map over a bf16 cache [rows = num_blocks * block_size, Hkv, 128]:
+// (64 columns, 8 rows of a group, 128-byte column halves of all heads, 8-row
+// groups), box {64, 8, 2, box_rows / 8}: one box lands box_rows rows of one
+// head, both halves, as [group][half][row] 1 KB swizzled atoms. (The halves'
+// stride, 128 B, is below the rows'.)
 bool make_tc_map(CUtensorMap* map, const void* base, int hkv, long long rows, int box_rows) {
   auto enc = tc_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)hkv * kTcD, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)hkv * kTcD * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  if (!enc || rows % 8 != 0 || box_rows % 8 != 0) return false;
+  const cuuint64_t row_bytes = (cuuint64_t)hkv * kTcD * 2;
+  cuuint64_t dims[4] = {64, 8, (cuuint64_t)hkv * 2, (cuuint64_t)(rows / 8)};
+  cuuint64_t strides[3] = {row_bytes, 128, 8 * row_bytes};
+  cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)(box_rows / 8)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
@@ -509,7 +568,7 @@ pa_status launch_prefill_tc(const void* q, const void* k_cache, const void* v_ca
   prm.num_blocks = num_blocks;
   prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
   const long long tiles = ((long long)max_q_len + prm.tokens_per_block - 1) / prm.tokens_per_block;
-  if (tiles > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+  if (tiles > 0x7fffffffLL || num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
   CUtensorMap mk, mv;
   std::memset(&mk, 0, sizeof(mk));
   std::memset(&mv, 0, sizeof(mv));
@@ -520,7 +579,7 @@ pa_status launch_prefill_tc(const void* q, const void* k_cache, const void* v_ca
   const pa_status s = prepare_kernel(reinterpret_cast<const void*>(prefill_tc_kernel),
                                      kTcThreads, TcSmem::kAlloc, nullptr);
   if (s != PA_OK) return s;
-  const dim3 grid(num_kv_heads, num_seqs, (unsigned)tiles);
+  const dim3 grid((unsigned)tiles, num_kv_heads, num_seqs);
   prefill_tc_kernel<<<grid, kTcThreads, TcSmem::kAlloc, stream>>>(mk, mv, prm);
   return launch_status();
 }
