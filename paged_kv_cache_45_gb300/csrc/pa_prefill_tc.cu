@@ -145,6 +145,37 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (v, v) as one 64-bit register pair.
+__device__ __forceinline__ uint64_t splat2(float v) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(v));
+  return r;
+}
+
+// (d0, d1) = (a0, a1) * b2 + c2 (b2, c2 packed pairs), one packed instruction.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, uint64_t b2,
+                                     uint64_t c2) {
+  asm("{\n\t.reg .b64 x, w;\n\tmov.b64 x, {%2, %3};\n\t"
+      "fma.rn.f32x2 w, x, %4, %5;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "l"(b2), "l"(c2));
+}
+
+// (s0, s1) += (a0, a1), one packed instruction.
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
+  asm("{\n\t.reg .b64 x, y, w;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+      "add.rn.f32x2 w, x, y;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+
 __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -410,27 +441,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int c = 0; c < kTcKeys; ++c) s[c] = c <= lim ? s[c] : -INFINITY;
       }
-      float mx8[8];
+      float mx8[8];  // 8 independent chains of three-input maxes
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[i + 8]);
 #pragma unroll
-      for (int c = 8; c < kTcKeys; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int c = 16; c < kTcKeys; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = max3(mx8[i], s[c + i], s[c + 8 + i]);
+      const float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]),
+                            fmaxf(mx8[6], mx8[7]));
       const float m_tile = mx * sl2;
       const bool grow = m_tile > m_run + kRescaleLog2;  // also the first finite max
       const float m_use = grow ? m_tile : m_run;
       const float alpha = grow ? ex2_approx(m_run - m_use) : 1.f;  // 0 when m_run = -inf
       const float ms = m_use == -INFINITY ? 0.f : m_use;
       uint32_t pk[kTcKeys / 2];  // P row as bf16 pairs
-      float sum8[8];
+      float sum8[8];             // 4 packed (even, odd) running sums
 #pragma unroll
       for (int i = 0; i < 8; ++i) sum8[i] = 0.f;
+      const uint64_t sl2x2 = splat2(sl2), negms2 = splat2(-ms);
 #pragma unroll
       for (int c = 0; c < kTcKeys; c += 2) {
-        const float e0 = ex2_approx(fmaf(s[c], sl2, -ms));
-        const float e1 = ex2_approx(fmaf(s[c + 1], sl2, -ms));
-        sum8[(c >> 1) & 7] += e0 + e1;
+        float x0, x1;
+        fma2(x0, x1, s[c], s[c + 1], sl2x2, negms2);
+        const float e0 = ex2_approx(x0);
+        const float e1 = ex2_approx(x1);
+        const int a = (c >> 1) & 3;
+        add2(sum8[2 * a], sum8[2 * a + 1], e0, e1);
         pk[c >> 1] = pack_bf16x2(e0, e1);
       }
       tmem_st64_sync(t_s, pk);
