@@ -118,6 +118,18 @@ def describe(workload: str, batch: int = 256) -> str:
     }[workload].replace("{batch}", str(batch))
 
 
+def attended_pairs(q_start, context_lens) -> int:
+    """(query row, key) pairs a causal multi-token step attends: sequence b's
+    n_b rows sit at positions ctx_b - n_b .. ctx_b - 1 and row p sees keys
+    0..p (none when p < 0): T(ctx_b) - T(max(ctx_b - n_b, 0)), T(x) = x(x+1)/2."""
+    total = 0
+    for b in range(len(context_lens)):
+        n, c = int(q_start[b + 1]) - int(q_start[b]), int(context_lens[b])
+        lo = max(c - n, 0)
+        total += c * (c + 1) // 2 - lo * (lo + 1) // 2
+    return total
+
+
 class Steps:
     """Device-resident inputs of a workload's steps, cycled by index."""
 
@@ -141,9 +153,7 @@ class Steps:
                                    slots=case.slot_mapping, tables=case.block_tables,
                                    lens=case.context_lens, qstart=case.q_start))
             # attention FLOPs: 2 products x 2 FLOP x D per (row, attended key)
-            qs, cl = case.q_start.numpy().astype(np.int64), case.context_lens.numpy()
-            attended = sum(int((cl[i] - (qs[i + 1] - qs[i]) + 1 + cl[i]) * (qs[i + 1] - qs[i])) // 2
-                           for i in range(len(cl)))
+            attended = attended_pairs(case.q_start.numpy(), case.context_lens.numpy())
             self.items[-1]["flops"] = 4 * self.d * self.hq * attended
         elif workload == "cb70b":
             cb = wl.ContinuousBatching(seed=seed, batch=batch)
