@@ -85,6 +85,8 @@ def parse_args():
                     help="budget of the oracle's CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the pass that replays the timed steps from CUDA graphs")
     return ap.parse_args()
 
 
@@ -532,6 +534,29 @@ def run_gpu(args):
     total_s = t_ev[0].elapsed_time(t_ev[1]) / 1e3
     alg_bytes = sum(steps.items[i]["kv_bytes"] + steps.items[i]["qo_bytes"] for i in idx)
 
+    # ------------------ the same K steps replayed from CUDA graphs (one graph
+    # per distinct step input, captured after the warm-up: a warmed entry point
+    # issues only its launches)
+    graph_s = None
+    if not args.no_graph:
+        graphs = []
+        for it in steps.items:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(it["dev"])
+            graphs.append(g)
+        for w in range(3):
+            graphs[w % n].replay()
+        g_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        torch.cuda.synchronize()
+        g_ev[0].record(stream)
+        for k in range(K):
+            graphs[idx[k]].replay()
+        g_ev[1].record(stream)
+        torch.cuda.synchronize()
+        graph_s = g_ev[0].elapsed_time(g_ev[1]) / 1e3
+        del graphs
+
     # ---------- an instrumented pass: events around every launch of the step
     # (the per-kernel breakdown and the decode kernel's own duration; an event
     # pair costs ~2 us of device time, so these steps are not the headline)
@@ -621,6 +646,12 @@ def run_gpu(args):
     e2e_s = e2e_ev[0].elapsed_time(e2e_ev[1]) / 1e3
 
     # ------------------------------------------------------------ across ranks
+    graph_line = None
+    if graph_s is not None:
+        graph_line = {"ms_per_step": round(graph_s / K * 1e3, 5),
+                      "value": round(alg_bytes / world / graph_s / 1e9, 2), "unit": "GB/s",
+                      "graphs": n, "note": "the same K steps replayed from CUDA graphs "
+                                           "(one per distinct step input), rank 0"}
     stats = torch.tensor([total_s, alg_bytes, e2e_s, e2e_bytes, dec_s, dec_bytes],
                          dtype=torch.float64, device=device)
     if world > 1:
@@ -725,6 +756,11 @@ def run_gpu(args):
         line["config"]["l2"] = "inputs larger than L2: 268 MB of K/V read every step"
         line.pop("pct_of_hbm_peak", None)
         line.pop("pct_of_datasheet_8tbs", None)
+    if graph_line is not None:
+        if prefill:
+            graph_line["value"] = round(steps.items[0]["flops"] * K / graph_s / 1e12, 2)
+            graph_line["unit"] = "TFLOP/s"
+        line["graph"] = graph_line
     if clocks is not None:
         line["clocks"] = clocks
     if cpu is not None:
@@ -769,8 +805,8 @@ def prefill_cpu_baseline(seed: int, budget_s: float):
     return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
             "kind": "oracle",
             "sample": f"the first {rows} rows of one sequence's 2048-token chunk (each at its "
-                      f"causal context, 6145.. keys, 64 heads), fp64 oracle decode_multi, one "
-                      f"BLAS thread, {secs:.1f} s"}
+                      f"causal context, 6145.. keys, 64 heads), fp64 oracle decode_multi, "
+                      f"{blas_threads()} BLAS thread(s), {secs:.1f} s"}
 
 
 def oracle_sample_case(seed: int, n_seqs: int = 48):
@@ -816,15 +852,19 @@ def cpu_baseline_child(seed: int, budget_s: float) -> None:
                       "cores": 1, "kind": "oracle",
                       "sample": f"{len(times)} sequences of a 48-sequence sample of the 70B-shape "
                                 f"batch (log-uniform [128, 8192] tokens), fp64 oracle append + "
-                                f"decode, one BLAS thread, {sum(times):.1f} s",
+                                f"decode, {blas_threads()} BLAS thread(s), {sum(times):.1f} s",
                       "seconds": round(sum(times), 2), "host_cpus": os.cpu_count()}))
 
 
-def single_thread_env():
+def blas_threads() -> str:
+    return os.environ.get("OPENBLAS_NUM_THREADS", "default")
+
+
+def single_thread_env(threads: int = 1):
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
               "NUMEXPR_NUM_THREADS"):
-        env[k] = "1"
+        env[k] = str(threads)
     env["CUDA_VISIBLE_DEVICES"] = ""
     return env
 
@@ -834,15 +874,30 @@ def prefill_cpu_baseline_child(seed: int, budget_s: float) -> None:
 
 
 def cpu_baseline_subprocess(args):
+    """The oracle with one BLAS thread (the reported value), and again with a
+    BLAS thread per host core (reported beside it)."""
     child = "prefill_cpu_baseline_child" if args.workload == "prefill" else "cpu_baseline_child"
     code = ("import bench; bench.%s(%d, %f)" % (child, args.seed, args.cpu_seconds))
-    try:
-        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=single_thread_env(),
-                           capture_output=True, text=True, timeout=600)
+
+    def run(threads):
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT,
+                           env=single_thread_env(threads), capture_output=True, text=True,
+                           timeout=600)
         return json.loads(r.stdout.strip().splitlines()[-1])
+    try:
+        out = run(1)
     except Exception as e:  # reported, not fatal: the GPU number stands on its own
         return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
                 "sample": f"failed: {type(e).__name__}: {e}"}
+    threads = os.cpu_count() or 1
+    try:
+        allc = run(threads)
+        out["all_threads"] = {"value": allc["value"], "threads": threads,
+                              "sample": allc["sample"]}
+    except Exception as e:
+        out["all_threads"] = {"value": None, "threads": threads,
+                              "sample": f"failed: {type(e).__name__}: {e}"}
+    return out
 
 
 def run_reference(args):
