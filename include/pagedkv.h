@@ -327,11 +327,15 @@ pa_status pa_selftest_wait_timeout(int32_t limit_us, void* stream);
  *   max_q_len  an upper bound of every n_b. With max_q_len * (num_q_heads /
  *              num_kv_heads) <= 64 (drafted tokens, short chunks) one block
  *              holds a sequence's whole query group for one KV head; above
- *              that (long prompt chunks) blocks of 64 (token, head) rows each
- *              run with a causal key range of their own, unsplit: split_tokens
- *              must then be 0, else PA_ERR_UNSUPPORTED. A sequence with more
- *              rows than max_q_len is skipped and sets bit 16 of the device
- *              error word (rejected in validating mode).
+ *              that (long prompt chunks) the rows are tiled, unsplit, each
+ *              tile with a causal key range of its own: 256 (token, head)
+ *              rows a block on the tcgen05 tensor cores (scores and outputs
+ *              in tensor memory) for head_dim 128 and block_size >= 8, 64
+ *              rows a block on warp MMAs otherwise (or when the environment
+ *              sets PA_PREFILL_KERNEL=rowblock); split_tokens must then be 0,
+ *              else PA_ERR_UNSUPPORTED. A sequence with more rows than
+ *              max_q_len is skipped and sets bit 16 of the device error word
+ *              (rejected in validating mode).
  *   split_tokens / max_splits / part_out / part_lse: as in pa_decode, with
  *              rows in place of sequences (part_out [num_q_rows, num_q_heads,
  *              max_splits, head_dim]); split mode also writes each row's
