@@ -108,3 +108,48 @@ def test_prefill_bench_step_on_sampled_rows(cuda_lib):
                                        np.array([6144 + i + 1]), np.array([0, 1]), case.scale)
             P.assert_close(out[row:row + 1], want, f"sequence {s} token {i}")
     assert cuda_lib.pa_last_device_error() == 0
+
+
+def test_rows_above_max_q_len_set_the_shape_bit(cuda_lib, kernel):
+    # long-chunk launch (max_q_len 20 x G 8 > 64 rows) with a sequence of 40
+    # tokens: that sequence is skipped, the device error word gets bit 16
+    b = cuda_lib
+    case = wl.make_multi_case("tcshape", 13, [10, 100], [40, 12], 16, 2, 128, 16)
+    k, v = case.k_cache.cuda(), case.v_cache.cuda()
+    b.pa_kv_append(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), k, v)
+    out = torch.zeros_like(case.q).cuda()
+    b.pa_decode_multi(case.q.cuda(), k, v, case.block_tables.cuda(), case.context_lens.cuda(),
+                      case.q_start.cuda(), 20, case.scale, out)
+    torch.cuda.synchronize()
+    assert b.pa_last_device_error() & 16
+    got = P.to_f64(out)
+    assert not got[:40].any()                    # the skipped sequence: untouched
+    kc, vc = appended(case)
+    want = oracle.decode_multi(wl.bits(case.q), kc, vc, case.block_tables.numpy(),
+                               case.context_lens.numpy(), case.q_start.numpy(), case.scale)
+    P.assert_close(got[40:], want[40:], f"{kernel} the other sequence")
+
+
+def test_block_ids_outside_the_pool_read_zeros(cuda_lib):
+    # a table entry inside the context that points past the pool: the kernel
+    # reads zero K/V rows there (a TMA box wholly out of range) and faults
+    # nothing; the oracle sees the same once that entry names a zero block
+    b = cuda_lib
+    case = wl.make_multi_case("tcoob", 17, [100, 40], [300, 90], 16, 2, 128, 16)
+    nb = case.k_cache.shape[0]
+    k, v = case.k_cache.cuda(), case.v_cache.cuda()
+    b.pa_kv_append(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), k, v)
+    kc, vc = appended(case)
+    bt = case.block_tables.clone()
+    bt[0, 3] = nb + 7                            # keys 48..63 of sequence 0
+    out = b.decode_multi(case.q.cuda(), k, v, bt.cuda(), case.context_lens.cuda(),
+                         case.q_start.cuda(), case.max_q_len, case.scale)
+    torch.cuda.synchronize()
+    assert b.pa_last_device_error() == 0
+    kz = np.concatenate([kc, np.zeros_like(kc[:1])])   # block nb: all zeros
+    vz = np.concatenate([vc, np.zeros_like(vc[:1])])
+    bt_ref = bt.numpy().copy()
+    bt_ref[0, 3] = nb
+    want = oracle.decode_multi(wl.bits(case.q), kz, vz, bt_ref, case.context_lens.numpy(),
+                               case.q_start.numpy(), case.scale)
+    P.assert_close(P.to_f64(out), want, "block id outside the pool")
