@@ -392,7 +392,7 @@ def run_gpu(args):
         split = -1 if args.multi_schedule == "balanced" else (args.split if args.split >= 0
                                                               else 1024)
         if args.workload == "prefill":
-            split = 0     # long chunks run on the row-block kernel, unsplit
+            split = 0     # long chunks run unsplit (the tcgen05 kernel)
     elif args.schedule == "balanced":
         split = b.BALANCED
     elif args.split >= 0:

@@ -330,7 +330,7 @@ pa_status pa_selftest_wait_timeout(int32_t limit_us, void* stream);
  *              that (long prompt chunks) the rows are tiled, unsplit, each
  *              tile with a causal key range of its own: 256 (token, head)
  *              rows a block on the tcgen05 tensor cores (scores and outputs
- *              in tensor memory) for head_dim 128 and block_size >= 8, 64
+ *              in tensor memory) for block_size >= 8, 64
  *              rows a block on warp MMAs otherwise (or when the environment
  *              sets PA_PREFILL_KERNEL=rowblock); split_tokens must then be 0,
  *              else PA_ERR_UNSUPPORTED. A sequence with more rows than

@@ -28,7 +28,6 @@ pa_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-namespace {
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -42,7 +41,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   });
   return fn;
 }
-}  // namespace
 
 pa_status prepare_kernel(const void* func, int threads, int smem_bytes, int* blocks_per_sm) {
   static std::mutex mu;

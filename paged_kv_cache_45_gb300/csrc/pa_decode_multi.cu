@@ -1084,8 +1084,8 @@ extern "C" pa_status pa_decode_multi(const void* q, const void* k_cache, const v
     unsigned int* err = multi_error_word();
     if (!err) return PA_ERR_CUDA;
     return launch_prefill_tc(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                             q_start, num_seqs, max_q_len, num_q_heads, num_kv_heads, block_size,
-                             num_blocks, scale, out, err, st);
+                             q_start, num_seqs, max_q_len, num_q_heads, num_kv_heads, head_dim,
+                             block_size, num_blocks, scale, out, err, st);
   }
   if (long_chunk) {
     const int max_rows = max_q_len * G;

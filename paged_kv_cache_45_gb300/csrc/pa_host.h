@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,6 +27,10 @@ bool validating();
 
 // Maps the last launch error to a status, clearing it.
 pa_status launch_status();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (looked up
+// once); null when the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Tensor map over a cache viewed as [rows = num_blocks*block_size,
 // cols = num_kv_heads*head_dim] elements of elem_bytes (2: bf16, 1: e4m3
@@ -59,16 +64,16 @@ pa_status check_decode_args(const void* q, const void* k_cache, const void* v_ca
 pa_status prepare_kernel(const void* func, int threads, int smem_bytes, int* blocks_per_sm);
 
 // Long query chunks on the tcgen05 tensor cores (pa_prefill_tc.cu): supported
-// for head_dim 128, block_size >= 8 and a query group of at most 256 heads.
-// Runs pa_decode_multi's unsplit causal attention with the same arguments;
-// device errors are ORed into *err.
+// for head_dim 64 or 128, block_size >= 8 and a query group of at most 256
+// heads. Runs pa_decode_multi's unsplit causal attention with the same
+// arguments; device errors are ORed into *err.
 bool prefill_tc_supported(int head_dim, int block_size, int group);
 pa_status launch_prefill_tc(const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_tables, int max_blocks,
                             const int32_t* context_lens, const int32_t* q_start, int num_seqs,
-                            int max_q_len, int num_q_heads, int num_kv_heads, int block_size,
-                            int num_blocks, float scale, void* out, unsigned int* err,
-                            cudaStream_t stream);
+                            int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int num_blocks, float scale, void* out,
+                            unsigned int* err, cudaStream_t stream);
 
 // Reads and clears a translation unit's device error word (synchronous).
 unsigned int take_decode_errors();

@@ -43,7 +43,6 @@
 #include <math.h>
 
 #include <cstring>
-#include <mutex>
 
 #include "pa_device.cuh"
 #include "pa_host.h"
@@ -53,34 +52,44 @@
 namespace pa {
 namespace {
 
-constexpr int kTcD = 128;                          // head_dim
 constexpr int kTcRows = 128;                       // rows per Q tile (MMA M)
 constexpr int kTcQTiles = 2;                       // Q tiles per block
 constexpr int kTcKeys = 128;                       // keys per K/V tile
-constexpr int kTcSlots = 5;                        // K/V ring slots
 constexpr int kTcPanel = kTcRows * 128;            // Q: one 64-column panel, 16 KB
-// K/V slots hold 8-row groups of both 64-column halves: group g, half h at
-// g * kKvGroup + h * kKvHalf (each 1 KB = 8 rows of 128 bytes, swizzled), the
-// layout one 4-D TMA box per paged block writes.
-constexpr int kKvHalf = 1024;
-constexpr int kKvGroup = 2048;
-constexpr int kTcTileBytes = 2 * kTcPanel;         // 128 rows x 256 B: 32 KB
+constexpr int kKvHalf = 1024;                      // 8 rows of one 64-column panel
+constexpr int kRingBudget = 5 * 32768;             // shared memory of the K/V ring
+
+// Sizes that follow head_dim (64 or 128): a row is D / 64 panels of 64
+// columns (128 bytes). K/V slots hold 8-row groups of all panels: group g,
+// panel h at g * kKvGroup + h * kKvHalf (each 1 KB = 8 rows of 128 bytes,
+// swizzled), the layout one 4-D TMA box per paged block writes.
+template <int D>
+struct TcShape {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kQBytes = kTcRows * D * 2;     // one Q tile
+  static constexpr int kKvBytes = kTcKeys * D * 2;    // one K or V tile: a ring slot
+  static constexpr int kKvGroup = kHalves * kKvHalf;
+  static constexpr int kSlots = kRingBudget / kKvBytes;  // 5 at D 128, 10 at D 64
+};
 constexpr int kTcSoftmaxWarps = 4 * kTcQTiles;
 constexpr int kTcThreads = (2 + kTcSoftmaxWarps) * 32;
 constexpr uint32_t kTcCols = 512;                  // TMEM columns
 constexpr float kRescaleLog2 = 8.0f;               // rescale O when the max grows by > 2^8
 
+template <int D>
 struct TcSmem {
+  using S = TcShape<D>;
   static constexpr int kQ = 0;                                   // Q_0, Q_1
-  static constexpr int kRing = kQ + kTcQTiles * kTcTileBytes;    // K/V slots
-  static constexpr int kBar = kRing + kTcSlots * kTcTileBytes;
+  static constexpr int kRing = kQ + kTcQTiles * S::kQBytes;      // K/V slots
+  static constexpr int kBar = kRing + S::kSlots * S::kKvBytes;
   // barriers: full[5], empty[5], s_full[2], p_full[2], q_ready, o_final
-  static constexpr int kNumBars = 2 * kTcSlots + 2 * kTcQTiles + 2;
+  static constexpr int kNumBars = 2 * S::kSlots + 2 * kTcQTiles + 2;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kFlag = kTmemSlot + 8;
   static constexpr int kAlloc = kFlag + 8 + 1024;                // + 1024-byte alignment
 };
-static_assert(TcSmem::kAlloc <= 232448, "over the 227 KB of shared memory per block");
+static_assert(TcSmem<128>::kAlloc <= 232448, "over the 227 KB of shared memory per block");
+static_assert(TcSmem<64>::kAlloc <= 232448, "over the 227 KB of shared memory per block");
 
 struct TcParams {
   const __nv_bfloat16* q;       // [R, Hq, D]
@@ -188,9 +197,13 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
 __device__ __forceinline__ int k_seq(int i) { return 2 * i; }
 __device__ __forceinline__ int v_seq(int i) { return 2 * i + 1; }
 
+template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const TcParams p) {
+  using Sh = TcShape<D>;
+  using L = TcSmem<D>;
+  constexpr int kSlots = Sh::kSlots;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -234,29 +247,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int tok = tok_lo + R / G;
   const int pos = row_valid ? pos_base + tok : -1;
   const size_t out_off =
-      ((size_t)(row0 + tok) * p.num_q_heads + (size_t)kvh * G + (R % G)) * kTcD;
+      ((size_t)(row0 + tok) * p.num_q_heads + (size_t)kvh * G + (R % G)) * D;
 
   if (n_tiles == 0) {  // no position to attend: zero rows, nothing else
     if (row_valid) {
       uint4* o = reinterpret_cast<uint4*>(p.out + out_off);
-      for (int c = 0; c < kTcD / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
+      for (int c = 0; c < D / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
     }
     return;
   }
 
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TcSmem::kBar);
-  uint64_t* empty = full + kTcSlots;
-  uint64_t* s_full = empty + kTcSlots;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* empty = full + kSlots;
+  uint64_t* s_full = empty + kSlots;
   uint64_t* p_full = s_full + kTcQTiles;
   uint64_t* q_ready = p_full + kTcQTiles;
   uint64_t* o_final = q_ready + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TcSmem::kTmemSlot);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + TcSmem::kFlag);
-  const uint32_t sQ = smem_u32(smem + TcSmem::kQ);
-  const uint32_t ring = smem_u32(smem + TcSmem::kRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kFlag);
+  const uint32_t sQ = smem_u32(smem + L::kQ);
+  const uint32_t ring = smem_u32(smem + L::kRing);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kTcSlots; ++s) {
+    for (int s = 0; s < kSlots; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -294,9 +307,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int ent_val = -1;
     int L = 0;
     for (; L < 2 * n_tiles; ++L) {
-      const int slot = L % kTcSlots;
-      if (L >= kTcSlots &&
-          !__all_sync(0xffffffffu, wait_or_abort(&empty[slot], ((L / kTcSlots) - 1) & 1,
+      const int slot = L % kSlots;
+      if (L >= kSlots &&
+          !__all_sync(0xffffffffu, wait_or_abort(&empty[slot], ((L / kSlots) - 1) & 1,
                                                  abort_flag))) {
         if (lane == 0) give_up(abort_flag, p.err, kErrWaitEmpty);
         break;
@@ -312,65 +325,67 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int idx = ent_base + lane;
         ent_val = idx < n_entries ? bt[idx] : -1;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(nbox * rb * 256));
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(nbox * rb * D * 2));
       // one box per lane, issued together: a TMA instruction costs a lane a
       // few hundred cycles, and lanes overlap them
-      const uint32_t dst = ring + slot * kTcTileBytes;
+      const uint32_t dst = ring + slot * Sh::kKvBytes;
       const int i = lane < nbox ? lane : 0;
       const int key0 = j * kTcKeys + i * rb;
       const int blk = __shfl_sync(0xffffffffu, ent_val, (key0 >> p.log2_bs) - ent_base);
       if (lane < nbox) {
-        // rb rows (rb / 8 groups) x both halves of this head; a block id
+        // rb rows (rb / 8 groups) x all panels of this head; a block id
         // outside the pool reads zeros (a box wholly out of range)
         const int grp = (blk >= 0 && blk < p.num_blocks)
                             ? (blk * p.block_size + (key0 & (p.block_size - 1))) >> 3
                             : -(rb >> 3);
-        tma_load_4d(dst + (i * rb >> 3) * kKvGroup, map, 0, 0, 2 * kvh, grp, &full[slot]);
+        tma_load_4d(dst + (i * rb >> 3) * Sh::kKvGroup, map, 0, 0, Sh::kHalves * kvh, grp,
+                    &full[slot]);
       }
     }
     // every copy issued must land before the block ends
     if (lane == 0) {
-      for (int s = 0; s < kTcSlots; ++s) {
+      for (int s = 0; s < kSlots; ++s) {
         if (L <= s) continue;
-        const int last = s + ((L - 1 - s) / kTcSlots) * kTcSlots;
-        if (!mbar_wait(&full[s], (last / kTcSlots) & 1)) atomicOr(p.err, kErrDrain);
+        const int last = s + ((L - 1 - s) / kSlots) * kSlots;
+        if (!mbar_wait(&full[s], (last / kSlots) & 1)) atomicOr(p.err, kErrDrain);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = umma_idesc_bf16(kTcRows, kTcKeys, false);
-      constexpr uint32_t kIdO = umma_idesc_bf16(kTcRows, kTcD, true);
+      constexpr uint32_t kIdO = umma_idesc_bf16(kTcRows, D, true);
       // Descriptors are built once; a k-step or a slot moves only the start
       // address (bits 0-13, address >> 4), so each MMA costs one 64-bit add.
       // (Building them per MMA made the issuing thread, not the tensor pipe,
       // the bottleneck.)
-      constexpr uint64_t kTileStep = kTcTileBytes >> 4;
+      constexpr uint64_t kQStep = Sh::kQBytes >> 4;
+      constexpr uint64_t kSlotStep = Sh::kKvBytes >> 4;
       const uint64_t d_q = umma_desc_sw128(sQ, 16, 1024);             // Q_0, K-major
-      const uint64_t d_k = umma_desc_sw128(ring, 16, kKvGroup);          // slot 0, K-major
-      const uint64_t d_v = umma_desc_sw128(ring, kKvHalf, kKvGroup);     // slot 0, MN-major
-      auto issue_s = [&](int w, int L) {  // S_w = Q_w K^T, K in slot L % kTcSlots
-        const uint64_t qd = d_q + (uint64_t)w * kTileStep;
-        const uint64_t kd = d_k + (uint64_t)(L % kTcSlots) * kTileStep;
+      const uint64_t d_k = umma_desc_sw128(ring, 16, Sh::kKvGroup);          // slot 0, K-major
+      const uint64_t d_v = umma_desc_sw128(ring, kKvHalf, Sh::kKvGroup);     // slot 0, MN-major
+      auto issue_s = [&](int w, int L) {  // S_w = Q_w K^T, K in slot L % kSlots
+        const uint64_t qd = d_q + (uint64_t)w * kQStep;
+        const uint64_t kd = d_k + (uint64_t)(L % kSlots) * kSlotStep;
         const uint32_t dst = tmem + w * kTcKeys;
 #pragma unroll
-        for (int kk = 0; kk < kTcD / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t qoff = (uint64_t)(((kk >> 2) * kTcPanel + (kk & 3) * 32) >> 4);
           const uint64_t koff = (uint64_t)(((kk >> 2) * kKvHalf + (kk & 3) * 32) >> 4);
           umma_bf16_ss(dst, qd + qoff, kd + koff, kIdS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int w, int L, int j) {  // O_w += P_w V; P_w in TMEM, V in a slot
-        const uint64_t vd = d_v + (uint64_t)(L % kTcSlots) * kTileStep;
-        const uint32_t dst = tmem + 2 * kTcKeys + w * kTcD;
+        const uint64_t vd = d_v + (uint64_t)(L % kSlots) * kSlotStep;
+        const uint32_t dst = tmem + 2 * kTcKeys + w * D;
         const uint32_t pa_ = tmem + w * kTcKeys;
 #pragma unroll
         for (int kk = 0; kk < kTcKeys / 16; ++kk)
-          umma_bf16_ts(dst, pa_ + kk * 8, vd + (uint64_t)(kk * ((2 * kKvGroup) >> 4)), kIdO,
+          umma_bf16_ts(dst, pa_ + kk * 8, vd + (uint64_t)(kk * ((2 * Sh::kKvGroup) >> 4)), kIdO,
                        (j > 0 || kk > 0) ? 1u : 0u);
       };
       auto landed = [&](int L) {
-        return wait_or_abort(&full[L % kTcSlots], (L / kTcSlots) & 1, abort_flag);
+        return wait_or_abort(&full[L % kSlots], (L / kSlots) & 1, abort_flag);
       };
       // Tensor-pipe order: P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1), ...: while
       // one warpgroup's softmax runs, the other's products are computed. P_w
@@ -383,7 +398,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         umma_commit(&s_full[0]);
         issue_s(1, k_seq(0));
         umma_commit(&s_full[1]);
-        umma_commit(&empty[k_seq(0) % kTcSlots]);
+        umma_commit(&empty[k_seq(0) % kSlots]);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         const bool more = j + 1 < n_tiles;
@@ -393,12 +408,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!(ok = wait_or_abort(&p_full[w], j & 1, abort_flag))) break;
           tc_fence_after();
           issue_pv(w, LV, j);
-          if (w == kTcQTiles - 1) umma_commit(&empty[LV % kTcSlots]);
+          if (w == kTcQTiles - 1) umma_commit(&empty[LV % kSlots]);
           if (more) {
             if (w == 0 && !(ok = landed(LK))) break;
             issue_s(w, LK);
             umma_commit(&s_full[w]);
-            if (w == kTcQTiles - 1) umma_commit(&empty[LK % kTcSlots]);
+            if (w == kTcQTiles - 1) umma_commit(&empty[LK % kSlots]);
           }
         }
       }
@@ -410,12 +425,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------------------ softmax
     const uint32_t lanes = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t t_s = lanes + qt * kTcKeys;               // S of this tile; P in its first half
-    const uint32_t t_o = lanes + 2 * kTcKeys + qt * kTcD;    // O of this tile
-    const uint32_t my_q = sQ + qt * kTcTileBytes;
+    const uint32_t t_o = lanes + 2 * kTcKeys + qt * D;       // O of this tile
+    const uint32_t my_q = sQ + qt * Sh::kQBytes;
     {  // this row of Q into the K-major swizzled tile (zeros for padding rows)
       const __nv_bfloat16* src = p.q + out_off;
 #pragma unroll 4
-      for (int c = 0; c < kTcD / 8; ++c) {
+      for (int c = 0; c < D / 8; ++c) {
         const uint4 v = row_valid ? ld_global_nc_v4(src + 8 * c) : make_uint4(0, 0, 0, 0);
         st_shared_v4(my_q + sw_chunk(r, c), v.x, v.y, v.z, v.w);
       }
@@ -477,7 +492,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       m_run = m_use;
       if (j > 0 && __any_sync(0xffffffffu, grow)) {  // rescale the running output
 #pragma unroll 1
-        for (int c = 0; c < kTcD; c += 32) {
+        for (int c = 0; c < D; c += 32) {
           float o[32];
           tmem_ld32_sync(t_o + c, o);
 #pragma unroll
@@ -490,13 +505,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int first = pos_last - tile * kTcKeys + 1;
         if (first < kTcKeys) {
           const int LV = v_seq(j);
-          ok = __all_sync(0xffffffffu, wait_or_abort(&full[LV % kTcSlots],
-                                                      (LV / kTcSlots) & 1, abort_flag));
+          ok = __all_sync(0xffffffffu, wait_or_abort(&full[LV % kSlots],
+                                                      (LV / kSlots) & 1, abort_flag));
           if (ok) {
-            const uint32_t vt = ring + (LV % kTcSlots) * kTcTileBytes;
-            for (int i = r; i < (kTcKeys - first) * 16; i += kTcRows) {
-              const int row = first + (i >> 4), c = i & 15;
-              st_shared_v4(vt + (row >> 3) * kKvGroup + (c >> 3) * kKvHalf + (row & 7) * 128 +
+            const uint32_t vt = ring + (LV % kSlots) * Sh::kKvBytes;
+            for (int i = r; i < (kTcKeys - first) * (D / 8); i += kTcRows) {
+              const int row = first + i / (D / 8), c = i % (D / 8);
+              st_shared_v4(vt + (row >> 3) * Sh::kKvGroup + (c >> 3) * kKvHalf + (row & 7) * 128 +
                                (c & 7) * 16,
                            0, 0, 0, 0);
             }
@@ -517,7 +532,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(p.out + out_off);
 #pragma unroll 1
-      for (int c = 0; c < kTcD; c += 32) {
+      for (int c = 0; c < D; c += 32) {
         float o[32];
         tmem_ld32_sync(t_o + c, o);
         if (row_valid) {
@@ -539,33 +554,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point.
-PFN_cuTensorMapEncodeTiled_v12000 tc_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// 4-D map over a bf16 cache [rows = num_blocks * block_size, Hkv, 128]:
-// (64 columns, 8 rows of a group, 128-byte column halves of all heads, 8-row
-// groups), box {64, 8, 2, box_rows / 8}: one box lands box_rows rows of one
-// head, both halves, as [group][half][row] 1 KB swizzled atoms. (The halves'
-// stride, 128 B, is below the rows'.)
+// 4-D map over a bf16 cache [rows = num_blocks * block_size, Hkv, D]:
+// (64 columns, 8 rows of a group, the 128-byte column panels of all heads,
+// 8-row groups), box {64, 8, D / 64, box_rows / 8}: one box lands box_rows rows
+// of one head, all its panels, as [group][panel][row] 1 KB swizzled atoms.
+// (The panels' stride, 128 B, is below the rows'.)
+template <int D>
 bool make_tc_map(CUtensorMap* map, const void* base, int hkv, long long rows, int box_rows) {
-  auto enc = tc_map_encoder();
+  auto enc = tensor_map_encoder();
   if (!enc || rows % 8 != 0 || box_rows % 8 != 0) return false;
-  const cuuint64_t row_bytes = (cuuint64_t)hkv * kTcD * 2;
-  cuuint64_t dims[4] = {64, 8, (cuuint64_t)hkv * 2, (cuuint64_t)(rows / 8)};
+  const cuuint64_t row_bytes = (cuuint64_t)hkv * D * 2;
+  cuuint64_t dims[4] = {64, 8, (cuuint64_t)hkv * TcShape<D>::kHalves, (cuuint64_t)(rows / 8)};
   cuuint64_t strides[3] = {row_bytes, 128, 8 * row_bytes};
-  cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)(box_rows / 8)};
+  cuuint32_t box[4] = {64, 8, (cuuint32_t)TcShape<D>::kHalves, (cuuint32_t)(box_rows / 8)};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -573,20 +574,33 @@ bool make_tc_map(CUtensorMap* map, const void* base, int hkv, long long rows, in
          CUDA_SUCCESS;
 }
 
+template <int D>
+pa_status launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const TcParams& prm,
+                    long long tiles, int num_kv_heads, int num_seqs, cudaStream_t stream) {
+  using L = TcSmem<D>;
+  const pa_status s = prepare_kernel(reinterpret_cast<const void*>(prefill_tc_kernel<D>),
+                                     kTcThreads, L::kAlloc, nullptr);
+  if (s != PA_OK) return s;
+  const dim3 grid((unsigned)tiles, num_kv_heads, num_seqs);
+  prefill_tc_kernel<D><<<grid, kTcThreads, L::kAlloc, stream>>>(mk, mv, prm);
+  return launch_status();
+}
+
 }  // namespace
 
 bool prefill_tc_supported(int head_dim, int block_size, int group) {
-  return head_dim == kTcD && block_size >= 8 && group >= 1 && group <= kTcQTiles * kTcRows;
+  return (head_dim == 64 || head_dim == 128) && block_size >= 8 && group >= 1 &&
+         group <= kTcQTiles * kTcRows;
 }
 
 pa_status launch_prefill_tc(const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_tables, int max_blocks,
                             const int32_t* context_lens, const int32_t* q_start, int num_seqs,
-                            int max_q_len, int num_q_heads, int num_kv_heads, int block_size,
-                            int num_blocks, float scale, void* out, unsigned int* err,
-                            cudaStream_t stream) {
+                            int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int num_blocks, float scale, void* out,
+                            unsigned int* err, cudaStream_t stream) {
   const int G = num_q_heads / num_kv_heads;
-  if (!prefill_tc_supported(kTcD, block_size, G)) return PA_ERR_UNSUPPORTED;
+  if (!prefill_tc_supported(head_dim, block_size, G)) return PA_ERR_UNSUPPORTED;
   TcParams prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.q_start = q_start;
@@ -610,15 +624,16 @@ pa_status launch_prefill_tc(const void* q, const void* k_cache, const void* v_ca
   std::memset(&mk, 0, sizeof(mk));
   std::memset(&mv, 0, sizeof(mv));
   const long long rows = (long long)num_blocks * block_size;
-  if (!make_tc_map(&mk, k_cache, num_kv_heads, rows, prm.box_rows) ||
-      !make_tc_map(&mv, v_cache, num_kv_heads, rows, prm.box_rows))
+  if (head_dim == 128) {
+    if (!make_tc_map<128>(&mk, k_cache, num_kv_heads, rows, prm.box_rows) ||
+        !make_tc_map<128>(&mv, v_cache, num_kv_heads, rows, prm.box_rows))
+      return PA_ERR_CUDA;
+    return launch_tc<128>(mk, mv, prm, tiles, num_kv_heads, num_seqs, stream);
+  }
+  if (!make_tc_map<64>(&mk, k_cache, num_kv_heads, rows, prm.box_rows) ||
+      !make_tc_map<64>(&mv, v_cache, num_kv_heads, rows, prm.box_rows))
     return PA_ERR_CUDA;
-  const pa_status s = prepare_kernel(reinterpret_cast<const void*>(prefill_tc_kernel),
-                                     kTcThreads, TcSmem::kAlloc, nullptr);
-  if (s != PA_OK) return s;
-  const dim3 grid((unsigned)tiles, num_kv_heads, num_seqs);
-  prefill_tc_kernel<<<grid, kTcThreads, TcSmem::kAlloc, stream>>>(mk, mv, prm);
-  return launch_status();
+  return launch_tc<64>(mk, mv, prm, tiles, num_kv_heads, num_seqs, stream);
 }
 
 }  // namespace pa

@@ -2,8 +2,8 @@
 pa_decode_multi, and on the mma.sync row-block kernel it replaces
 (PA_PREFILL_KERNEL=rowblock), against the fp64 oracle's causal attention.
 
-Covers query groups that divide the 256-row block and ones that leave padding
-rows (G = 6), block sizes 8..256 (one TMA box
+Covers head_dim 128 and 64, query groups that divide the 256-row block and
+ones that leave padding rows (G = 6), block sizes 8..256 (one TMA box
 per block, or a 128-key tile inside one block), chunks spanning many 128-key
 tiles with ragged tails, cached prefixes that are not tile multiples, pools
 whose unowned slots are NaN (masked keys and zeroed V rows must keep them
@@ -66,6 +66,22 @@ def test_long_chunks_match_oracle(cuda_lib, kernel, hq, hkv, bs, ctx0, qlens):
     want = oracle.decode_multi(wl.bits(case.q), kc, vc, case.block_tables.numpy(),
                                case.context_lens.numpy(), case.q_start.numpy(), case.scale)
     P.assert_close(P.to_f64(out), want, f"{kernel} G={hq // hkv} bs={bs}")
+    assert cuda_lib.pa_last_device_error() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,bs,ctx0,qlens", [
+    (32, 4, 16, [0, 100, 1000, 7], [300, 129, 40, 257]),      # G 8
+    (8, 8, 8, [0, 250], [600, 513]),                           # G 1, block_size 8
+    (12, 2, 64, [50, 0], [90, 43]),                            # G 6, padding rows
+    (16, 2, 256, [100, 0, 600], [200, 90, 40]),                # a tile inside one block
+])
+def test_head_dim_64_long_chunks_match_oracle(cuda_lib, kernel, hq, hkv, bs, ctx0, qlens):
+    case = wl.make_multi_case("tc64", 11 + hq + bs, ctx0, qlens, hq, hkv, 64, bs)
+    out = run(cuda_lib, case)
+    kc, vc = appended(case)
+    want = oracle.decode_multi(wl.bits(case.q), kc, vc, case.block_tables.numpy(),
+                               case.context_lens.numpy(), case.q_start.numpy(), case.scale)
+    P.assert_close(P.to_f64(out), want, f"{kernel} D=64 G={hq // hkv} bs={bs}")
     assert cuda_lib.pa_last_device_error() == 0
 
 
