@@ -169,3 +169,30 @@ def test_block_ids_outside_the_pool_read_zeros(cuda_lib):
     want = oracle.decode_multi(wl.bits(case.q), kz, vz, bt_ref, case.context_lens.numpy(),
                                case.q_start.numpy(), case.scale)
     P.assert_close(P.to_f64(out), want, "block id outside the pool")
+
+
+def _random_shapes(n):
+    rng = np.random.default_rng(2024)
+    out = []
+    for i in range(n):
+        hkv = int(rng.choice([1, 2, 4, 8]))
+        g = int(rng.integers(1, 9))
+        d = int(rng.choice([64, 128]))
+        bs = int(rng.choice([8, 16, 32, 64, 128, 256]))
+        B = int(rng.integers(1, 5))
+        ctx0 = [int(x) for x in rng.integers(0, 900, B)]
+        qlens = [int(x) for x in rng.integers(1, 400, B)]
+        qlens[0] = max(qlens[0], 80 // g + 1)      # at least one long chunk: > 64 rows
+        out.append((i, g * hkv, hkv, d, bs, ctx0, qlens))
+    return out
+
+
+@pytest.mark.parametrize("i,hq,hkv,d,bs,ctx0,qlens", _random_shapes(12))
+def test_random_shapes_match_oracle(cuda_lib, i, hq, hkv, d, bs, ctx0, qlens):
+    case = wl.make_multi_case("tcrand", 500 + i, ctx0, qlens, hq, hkv, d, bs)
+    out = run(cuda_lib, case)
+    kc, vc = appended(case)
+    want = oracle.decode_multi(wl.bits(case.q), kc, vc, case.block_tables.numpy(),
+                               case.context_lens.numpy(), case.q_start.numpy(), case.scale)
+    P.assert_close(P.to_f64(out), want, f"random shape {i}: G={hq // hkv} D={d} bs={bs}")
+    assert cuda_lib.pa_last_device_error() == 0
