@@ -37,6 +37,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -322,11 +323,19 @@ class MultiWorkspace:
         self.row_lens = torch.empty(R, dtype=torch.int32, device=device) if split else None
 
 
+def code_of(text: str) -> str:
+    """C/CUDA source with comments, trailing spaces and blank lines removed:
+    what the compiler sees, so that editing a comment keeps a capture valid."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "paged_kv_cache_45_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_45_gb300", "csrc", name)) as fh:
+            h.update(code_of(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -14,15 +14,17 @@
 // One thread block per (row tile counted from the chunk's end, KV head,
 // sequence), 256 query rows = two M = 128 tiles (row = token * G + head; a
 // block covers floor(256 / G) tokens), 10 warps:
-//   warp 0     loader: K_j and V_j tiles of 128 keys through a 5-slot ring;
-//              a paged block's rows of one head land with ONE 4-D TMA box
-//              (64 columns x 8 rows x both 128-byte halves x block_size / 8
-//              row groups, 128-byte swizzle), lane i issuing box i so that
-//              the boxes' issue costs overlap;
+//   warp 0     loader: K_j and V_j tiles of 128 keys through a 160 KB ring
+//              (5 slots at head_dim 128, 10 at 64); a paged block's rows of
+//              one head land with ONE 4-D TMA box (64 columns x 8 rows x the
+//              head's 128-byte panels x block_size / 8 row groups, 128-byte
+//              swizzle), lane i issuing box i so that the boxes' issue costs
+//              overlap;
 //   warp 1     allocates 512 TMEM columns (S_0, S_1 scores, O_0, O_1 outputs)
 //              and one lane issues every MMA, descriptors built once:
-//                S_w = Q_w K_j^T  (SS: M 128, N 128 keys, K 128 = head_dim)
-//                O_w += P_w V_j   (TS: P_w from TMEM, M 128, N 128, K 128 keys)
+//                S_w = Q_w K_j^T  (SS: M 128, N 128 keys, K = head_dim)
+//                O_w += P_w V_j   (TS: P_w from TMEM, M 128, N head_dim,
+//                                  K 128 keys)
 //              in the order P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1), ... so the
 //              tensor cores work on one tile's products while the other
 //              tile's softmax runs;

@@ -34,3 +34,11 @@ def test_prefill_step_flops():
     pairs = bench.attended_pairs(qs, ctx)
     assert pairs == 8 * sum(range(6145, 8193))
     assert 4 * 128 * 64 * pairs == 3848559132672   # the bench line's FLOPs per launch
+
+
+def test_source_hash_ignores_comments_only():
+    a = "int f(int x) {  // doubles\n  /* the rest\n     of it */ return 2 * x;\n}\n"
+    b = "int f(int x) {\n\n  return 2 * x;   \n}\n"
+    c = "int f(int x) {\n  return 3 * x;\n}\n"
+    assert bench.code_of(a) == bench.code_of(b)
+    assert bench.code_of(a) != bench.code_of(c)
