@@ -324,11 +324,13 @@ class MultiWorkspace:
 
 
 def code_of(text: str) -> str:
-    """C/CUDA source with comments, trailing spaces and blank lines removed:
-    what the compiler sees, so that editing a comment keeps a capture valid."""
+    """C/CUDA source with comments and blank lines removed and each line's
+    whitespace collapsed: what the compiler sees, so that editing a comment
+    keeps a capture valid."""
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     text = re.sub(r"//[^\n]*", "", text)
-    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+    return "\n".join(re.sub(r"\s+", " ", line.strip()) for line in text.splitlines()
+                     if line.strip())
 
 
 def kernel_source_hash(kernel: str) -> str:
