@@ -36,5 +36,6 @@ from .paged_attention import (  # noqa: F401
     kv_append_fp8_inplace,
     dequantize_pool,
     decode_fp8,
+    decode_multi_fp8,
 )
 from .prefix_cache import PrefixCacheModel, CapacityError, copy_blocks  # noqa: F401

@@ -472,3 +472,36 @@ def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens
             p = np.exp(s - s.max())
             out[i, h] = (p @ V[:, kvh, :]) / p.sum()
     return out
+
+
+def decode_multi_fp8(q_rows, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens,
+                     q_start, scale: float) -> np.ndarray:
+    """:func:`decode_multi` over an e4m3 pool: the K/V rows read back as
+    value(code) * scale of their head, then for row q_start[b] + i (position
+    p = context_lens[b] - n_b + i) and query head h, softmax(scale * K[0..p,
+    h // G] q) @ V[0..p, h // G]; rows with p < 0 are zero."""
+    G = _group(q_rows, k_codes)
+    R, hq, d = q_rows.shape
+    ks = np.asarray(k_scale, dtype=np.float64)
+    vs = np.asarray(v_scale, dtype=np.float64)
+    out = np.zeros((R, hq, d), dtype=np.float64)
+    for b in range(len(context_lens)):
+        r0, r1 = int(q_start[b]), int(q_start[b + 1])
+        n = r1 - r0
+        ctx = int(context_lens[b])
+        if n == 0 or ctx == 0:
+            continue
+        K = e4m3_decode(gather_sequence(k_codes, block_tables[b], ctx)) * ks[:, None]
+        V = e4m3_decode(gather_sequence(v_codes, block_tables[b], ctx)) * vs[:, None]
+        for i in range(n):
+            pos = ctx - n + i
+            if pos < 0:
+                continue
+            qi = bf16_bits_to_f64(q_rows[r0 + i])
+            for h in range(hq):
+                kvh = h // G
+                sc = scale * (K[:pos + 1, kvh, :] @ qi[h])
+                w = np.exp(sc - sc.max())
+                out[r0 + i, h] = (w @ V[:pos + 1, kvh, :]) / w.sum()
+    return out
+
