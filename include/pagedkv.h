@@ -371,6 +371,31 @@ pa_status pa_decode_multi_balanced(const void* q, const void* k_cache, const voi
                                    void* workspace, size_t workspace_bytes, void* out,
                                    void* stream);
 
+/* pa_decode_multi over an FP8 (e4m3) pool: several new query tokens per
+ * sequence under the causal mask ([SPEED], section "Speculative decoding: more
+ * than one token per weight-read"; [TGI], "Advanced Pattern: Chunked Prefill
+ * (TGI v3)") with the K/V codes read back as value(code) * scale of their KV
+ * head ([SPEED], "The KV cache: the memory problem that runs the show"), as in
+ * pa_decode_balanced_fp8: 32-token e4m3 tiles widened exactly to f16 for f16
+ * MMAs, k_scale folded into the score factor and v_scale into the output.
+ *   k_codes, v_codes  uint8 [num_blocks, block_size, num_kv_heads, 128]
+ *              (written by pa_kv_append_fp8); k_scale, v_scale float
+ *              [num_kv_heads], device.
+ *   split_tokens  0, or a multiple of 32 (then part_out / part_lse /
+ *              row_lens and pa_decode_splitk_reduce as in pa_decode_multi).
+ * Supported: head_dim 128 and max_q_len * (num_q_heads / num_kv_heads) <= 64;
+ * otherwise PA_ERR_UNSUPPORTED. Other arguments, layouts and errors as
+ * pa_decode_multi. */
+pa_status pa_decode_multi_fp8(const void* q, const void* k_codes, const void* v_codes,
+                              const float* k_scale, const float* v_scale,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, const int32_t* q_start,
+                              int32_t num_seqs, int32_t num_q_rows, int32_t max_q_len,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t block_size, int32_t num_blocks, float scale,
+                              int32_t split_tokens, int32_t max_splits, float* part_out,
+                              float* part_lse, int32_t* row_lens, void* out, void* stream);
+
 /* Workspace bytes pa_decode_multi_balanced needs on the current device. */
 size_t pa_decode_multi_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads,
                                                 int32_t head_dim);

@@ -55,6 +55,8 @@ _SIGS = {
     "pa_decode_multi_balanced": (_i32, [_p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32,
                                         _i32, _i32, _i32, _i32, _f32, _p, _sz, _p, _p]),
     "pa_decode_multi_balanced_workspace_bytes": (_sz, [_i32, _i32, _i32]),
+    "pa_decode_multi_fp8": (_i32, [_p, _p, _p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32,
+                                   _i32, _i32, _i32, _i32, _f32, _i32, _i32, _p, _p, _p, _p, _p]),
     "pa_prefix_cache_create": (_i32, [_i32, _i32, _p]),
     "pa_prefix_cache_destroy": (None, [_p]),
     "pa_prefix_admit": (_i32, [_p, _p, _i32, _p, _p]),
@@ -200,6 +202,32 @@ def pa_decode_multi(q, k_cache, v_cache, block_tables, context_lens, q_start, ma
         _stream(stream)))
 
 
+def pa_decode_multi_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens,
+                        q_start, max_q_len: int, scale: float, out, split_tokens: int = 0,
+                        max_splits: int = 0, part_out=None, part_lse=None, row_lens=None,
+                        stream=None) -> None:
+    """pa_decode_multi over an e4m3 pool (uint8 codes, per-KV-head fp32 scales)."""
+    R, hq, d = q.shape
+    nb, bs, hkv, d2 = k_codes.shape
+    B = context_lens.numel()
+    if d2 != d or tuple(v_codes.shape) != tuple(k_codes.shape):
+        raise ValueError("cache shapes do not match q")
+    if tuple(out.shape) != (R, hq, d) or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("out / block_tables shape mismatch")
+    if q_start.numel() != B + 1 or k_scale.numel() != hkv or v_scale.numel() != hkv:
+        raise ValueError("q_start / scale sizes do not match")
+    _check("pa_decode_multi_fp8", _lib.pa_decode_multi_fp8(
+        _t(q, torch.bfloat16, "q"), _t(k_codes, torch.uint8, "k_codes"),
+        _t(v_codes, torch.uint8, "v_codes"), _t(k_scale, torch.float32, "k_scale"),
+        _t(v_scale, torch.float32, "v_scale"), _t(block_tables, torch.int32, "block_tables"),
+        int(block_tables.shape[1]), _t(context_lens, torch.int32, "context_lens"),
+        _t(q_start, torch.int32, "q_start"), B, R, int(max_q_len), hq, hkv, d, bs, nb,
+        float(scale), int(split_tokens), int(max_splits),
+        _opt(part_out, torch.float32, "part_out"), _opt(part_lse, torch.float32, "part_lse"),
+        _opt(row_lens, torch.int32, "row_lens"), _t(out, torch.bfloat16, "out"),
+        _stream(stream)))
+
+
 def pa_decode_multi_balanced(q, k_cache, v_cache, block_tables, context_lens, q_start,
                              max_q_len: int, scale: float, workspace, out, stream=None) -> None:
     """pa_decode_multi on the balanced persistent schedule; ``workspace`` a
@@ -257,6 +285,30 @@ def decode_multi(q, k_cache, v_cache, block_tables, context_lens, q_start, max_q
     row_lens = torch.empty(R, dtype=torch.int32, device=q.device)
     pa_decode_multi(q, k_cache, v_cache, block_tables, context_lens, q_start, max_q_len, scale,
                     out, split_tokens, S, part_out, part_lse, row_lens, stream=stream)
+    pa_decode_splitk_reduce(part_out, part_lse, row_lens, split_tokens, out, stream=stream)
+    return out
+
+
+def decode_multi_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens,
+                     q_start, max_q_len: int, scale: float, split_tokens: int = 0,
+                     max_context: int | None = None, out=None, stream=None):
+    """pa_decode_multi_fp8 with its split-mode buffers and the reduce; returns out."""
+    R, hq, d = q.shape
+    if out is None:
+        out = torch.empty((R, hq, d), dtype=torch.bfloat16, device=q.device)
+    if split_tokens <= 0:
+        pa_decode_multi_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens,
+                            q_start, max_q_len, scale, out, stream=stream)
+        return out
+    if max_context is None:
+        max_context = int(block_tables.shape[1]) * int(k_codes.shape[1])
+    S = pa_decode_num_splits(max_context, split_tokens)
+    part_out = torch.empty((R, hq, S, d), dtype=torch.float32, device=q.device)
+    part_lse = torch.empty((R, hq, S), dtype=torch.float32, device=q.device)
+    row_lens = torch.empty(R, dtype=torch.int32, device=q.device)
+    pa_decode_multi_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens,
+                        q_start, max_q_len, scale, out, split_tokens, S, part_out, part_lse,
+                        row_lens, stream=stream)
     pa_decode_splitk_reduce(part_out, part_lse, row_lens, split_tokens, out, stream=stream)
     return out
 

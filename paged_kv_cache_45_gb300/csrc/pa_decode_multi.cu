@@ -70,6 +70,8 @@ struct MultiParams {
   int max_splits;
   int max_q_len;
   float scale_log2;
+  const float* k_scale;        // [Hkv], e4m3 pools only
+  const float* v_scale;        // [Hkv], e4m3 pools only
 };
 
 template <int D>
@@ -83,16 +85,128 @@ struct MultiSmem {
   static constexpr int kAlloc = kFlagOff + 16 + 1024;
 };
 
+// A 32-token e4m3 tile for query columns with their own causal limits: the
+// score and PV math of attend_tile_fp8 (K and V bytes widened exactly to f16,
+// Q in the e4m3 tiles' k order), with the per-column masks of
+// attend_tile_causal_nt: rows >= valid_a (valid_b) are masked for this lane's
+// column 2 (lane % 4) (its column + 1), V rows >= valid are zeroed, and a
+// column whose every score so far is masked keeps m = -inf, l = 0, O = 0.
+// score_scale_log2 = scale * k_scale * log2(e); O is in the fp8 output dim
+// order (fp8_out_dim) and still to be multiplied by v_scale.
+template <int D>
+__device__ __forceinline__ void attend_tile_causal_fp8(AttnState<D>& st, uint32_t sK,
+                                                       uint32_t sV,
+                                                       const uint32_t (&qf)[D / 16][2],
+                                                       int valid, int valid_a, int valid_b,
+                                                       float score_scale_log2, int lane) {
+  static_assert(D == 128, "e4m3 tiles are one 128-byte row per token");
+  const int r = lane & 15;
+  const int cadd = lane >> 4;
+  float sa[4] = {0.f, 0.f, 0.f, 0.f};  // tokens 0-15
+  float sb[4] = {0.f, 0.f, 0.f, 0.f};  // tokens 16-31
+#pragma unroll
+  for (int sidx = 0; sidx < D / 32; ++sidx) {
+    const uint32_t sw = (uint32_t)(((2 * sidx + cadd) ^ (r & 7)) << 4);
+    uint32_t ka[4], kb[4], a[4];
+    ldsm_x4(sK + r * 128 + sw, ka);
+    ldsm_x4(sK + (r + 16) * 128 + sw, kb);
+    fp8_k_operand(ka, 0, a);
+    mma_f16_16816(sa, a, qf[2 * sidx][0], qf[2 * sidx][1]);
+    fp8_k_operand(kb, 0, a);
+    mma_f16_16816(sb, a, qf[2 * sidx][0], qf[2 * sidx][1]);
+    fp8_k_operand(ka, 2, a);
+    mma_f16_16816(sa, a, qf[2 * sidx + 1][0], qf[2 * sidx + 1][1]);
+    fp8_k_operand(kb, 2, a);
+    mma_f16_16816(sb, a, qf[2 * sidx + 1][0], qf[2 * sidx + 1][1]);
+  }
+  const int r0 = lane >> 2;
+  const int tk = 2 * (lane & 3);
+  float y[8];  // tokens r0 + 8i (i = 0..3) x columns tk (even entries), tk + 1 (odd)
+  const float s8[8] = {sa[0], sa[1], sa[2], sa[3], sb[0], sb[1], sb[2], sb[3]};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    y[2 * i] = r0 + 8 * i < valid_a ? s8[2 * i] * score_scale_log2 : -INFINITY;
+    y[2 * i + 1] = r0 + 8 * i < valid_b ? s8[2 * i + 1] * score_scale_log2 : -INFINITY;
+  }
+  float mx0 = fmaxf(fmaxf(y[0], y[2]), fmaxf(y[4], y[6]));
+  float mx1 = fmaxf(fmaxf(y[1], y[3]), fmaxf(y[5], y[7]));
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+  }
+  const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
+  const float e0 = mn0 == -INFINITY ? 0.f : mn0, e1 = mn1 == -INFINITY ? 0.f : mn1;
+  const float a0 = exp2f(st.m0 - e0), a1 = exp2f(st.m1 - e1);
+  uint32_t pw[4];  // f16 weights of tokens r0 + 8i, columns tk | tk + 1
+#pragma unroll
+  for (int i = 0; i < 4; ++i) pw[i] = pack_f16x2(exp2f(y[2 * i] - e0), exp2f(y[2 * i + 1] - e1));
+  st.l0 = st.l0 * a0 + ((f16_lo(pw[0]) + f16_lo(pw[1])) + (f16_lo(pw[2]) + f16_lo(pw[3])));
+  st.l1 = st.l1 * a1 + ((f16_hi(pw[0]) + f16_hi(pw[1])) + (f16_hi(pw[2]) + f16_hi(pw[3])));
+  st.m0 = mn0;
+  st.m1 = mn1;
+  if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {  // only when a max moved
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      st.o[mt][0] *= a0;
+      st.o[mt][1] *= a1;
+      st.o[mt][2] *= a0;
+      st.o[mt][3] *= a1;
+    }
+  }
+  uint32_t pb[4];  // B fragments of P^T: tokens 0-7, 8-15, 16-23, 24-31
+#pragma unroll
+  for (int i = 0; i < 4; ++i) pb[i] = movmatrix_trans(pw[i]);
+  uint32_t vm[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+  const bool masked = valid < kFp8Tile;
+  if (masked) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      vm[i] = (tk + 8 * i < valid ? 0x0000ffffu : 0u) | (tk + 8 * i + 1 < valid ? 0xffff0000u : 0u);
+  }
+#pragma unroll
+  for (int sidx = 0; sidx < D / 32; ++sidx) {
+    const uint32_t sw = (uint32_t)(((2 * sidx + cadd) ^ (r & 7)) << 4);
+    uint32_t va[4], vb[4];
+    ldsm_x4_trans(sV + r * 128 + sw, va);
+    ldsm_x4_trans(sV + (r + 16) * 128 + sw, vb);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t x0 = byte_perm(va[2 * hf], 0u, 0x3120u);      // tokens 0-7
+      uint32_t x1 = byte_perm(va[2 * hf + 1], 0u, 0x3120u);  // tokens 8-15
+      uint32_t a[4];
+      e4m3x4_to_f16x2x2(x0, a[0], a[1]);
+      e4m3x4_to_f16x2x2(x1, a[2], a[3]);
+      if (masked) {
+        a[0] &= vm[0]; a[1] &= vm[0]; a[2] &= vm[1]; a[3] &= vm[1];
+      }
+      mma_f16_16816(st.o[2 * sidx + hf], a, pb[0], pb[1]);
+      x0 = byte_perm(vb[2 * hf], 0u, 0x3120u);      // tokens 16-23
+      x1 = byte_perm(vb[2 * hf + 1], 0u, 0x3120u);  // tokens 24-31
+      e4m3x4_to_f16x2x2(x0, a[0], a[1]);
+      e4m3x4_to_f16x2x2(x1, a[2], a[3]);
+      if (masked) {
+        a[0] &= vm[2]; a[1] &= vm[2]; a[2] &= vm[3]; a[3] &= vm[3];
+      }
+      mma_f16_16816(st.o[2 * sidx + hf], a, pb[2], pb[3]);
+    }
+  }
+}
+
 // Column of element d of column row j in a warp's output buffer: XOR-swizzled
 // in 8-float groups so the 4 column rows one store touches use 4 bank groups.
 __device__ __forceinline__ int out_col(int j, int d) { return d ^ ((j >> 1) << 3); }
 
-template <int D, bool kTma>
+template <int D, bool kTma, bool kFp8 = false>
 __global__ void __launch_bounds__((kMaxColumnWarps + 1) * 32, 2)
     multi_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const MultiParams p) {
+  // e4m3 pools: 32-token tiles of 128-byte rows (the same 8 KB stage)
+  constexpr int EB = kFp8 ? 1 : 2;
+  constexpr int TT = kFp8 ? kFp8Tile : kTile;
   using L = MultiSmem<D>;
-  using Gm = TileGeom<D>;
+  using Gm = TileGeom<D, EB, TT>;
+  static_assert(Gm::kStageBytes == TileGeom<D>::kStageBytes, "one ring layout for both");
   constexpr int STAGES = kMultiStages;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -141,7 +255,7 @@ __global__ void __launch_bounds__((kMaxColumnWarps + 1) * 32, 2)
     }
     return;
   }
-  const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
+  const int n_tiles = (t_end - t_begin + TT - 1) / TT;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -174,16 +288,17 @@ __global__ void __launch_bounds__((kMaxColumnWarps + 1) * 32, 2)
         *abort_flag = 1;
         break;
       }
-      const int t0 = t_begin + i * kTile;
+      const int t0 = t_begin + i * TT;
       const int blk_first = t0 >> p.src.log2_bs;
-      const int blk_last = (t0 + kTile - 1) >> p.src.log2_bs;
+      const int blk_last = (t0 + TT - 1) >> p.src.log2_bs;
       if (blk_first < tc_base || blk_last >= tc_base + 32) {  // warp-uniform refill
         tc_base = blk_first;
         const int idx = tc_base + lane;
         tc_val = idx < n_seq_blocks ? bt[idx] : -1;
       }
-      issue_tile<D, kTma>(ring + stage * Gm::kStageBytes, &full[stage], &tmap_k, &tmap_v, p.src,
-                          kvh, t0, t_end, n_seq_blocks, tc_base, tc_val, lane);
+      issue_tile<D, kTma, EB, TT>(ring + stage * Gm::kStageBytes, &full[stage], &tmap_k,
+                                  &tmap_v, p.src, kvh, t0, t_end, n_seq_blocks, tc_base, tc_val,
+                                  lane);
       ++issued;
     }
     const int first = issued > STAGES ? issued - STAGES : 0;
@@ -206,15 +321,26 @@ __global__ void __launch_bounds__((kMaxColumnWarps + 1) * 32, 2)
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) qf[ks][0] = qf[ks][1] = 0u;
     if (i < n) {
-      const unsigned int* rowp = reinterpret_cast<const unsigned int*>(
-          p.q + ((size_t)(row0 + i) * p.num_q_heads + kvh * G + c % G) * D + 2 * (lane & 3));
+      const __nv_bfloat16* qrow = p.q + ((size_t)(row0 + i) * p.num_q_heads + kvh * G + c % G) * D;
+      if constexpr (kFp8) {  // f16, in the e4m3 tiles' k order (dims 4c .. 4c + 3 of a step)
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        qf[ks][0] = __ldg(rowp + ks * 8);
-        qf[ks][1] = __ldg(rowp + ks * 8 + 4);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint2 v = __ldg(reinterpret_cast<const uint2*>(qrow + ks * 16 + 4 * (lane & 3)));
+          qf[ks][0] = pack_f16x2(bf16_lo(v.x), bf16_hi(v.x));
+          qf[ks][1] = pack_f16x2(bf16_lo(v.y), bf16_hi(v.y));
+        }
+      } else {
+        const unsigned int* rowp = reinterpret_cast<const unsigned int*>(qrow + 2 * (lane & 3));
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          qf[ks][0] = __ldg(rowp + ks * 8);
+          qf[ks][1] = __ldg(rowp + ks * 8 + 4);
+        }
       }
     }
   }
+  const float score_scale_log2 = kFp8 ? p.scale_log2 * p.k_scale[kvh] : p.scale_log2;
+  const float out_scale = kFp8 ? p.v_scale[kvh] : 1.f;
   // causal limits (last attended position) of this lane's two score columns
   const int tk = 2 * (lane & 3);
   const int ca = 8 * warp + tk;
@@ -237,12 +363,16 @@ __global__ void __launch_bounds__((kMaxColumnWarps + 1) * 32, 2)
       break;
     }
     const uint32_t sK = ring + stage * Gm::kStageBytes;
-    const int t0 = t_begin + i * kTile;
-    const int valid = min(kTile, t_end - t0);
+    const int t0 = t_begin + i * TT;
+    const int valid = min(TT, t_end - t0);
     const int va[1] = {max(0, min(valid, lim_a - t0 + 1))};
     const int vb[1] = {max(0, min(valid, lim_b - t0 + 1))};
-    attend_tile_causal_nt<D, 1>(sts, sK, sK + Gm::kKVBytes, qfs, valid, va, vb, p.scale_log2,
-                                lane);
+    if constexpr (kFp8)
+      attend_tile_causal_fp8<D>(st, sK, sK + Gm::kKVBytes, qf, valid, va[0], vb[0],
+                                score_scale_log2, lane);
+    else
+      attend_tile_causal_nt<D, 1>(sts, sK, sK + Gm::kKVBytes, qfs, valid, va, vb,
+                                  score_scale_log2, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
   }
@@ -252,16 +382,19 @@ __global__ void __launch_bounds__((kMaxColumnWarps + 1) * 32, 2)
   named_barrier_sync(1, NC * 32);  // every consumer is done with the ring
   if (__any_sync(0xffffffffu, aborted) || *abort_flag) return;
   float* buf = reinterpret_cast<float*>(smem) + (size_t)warp * 8 * D;
-  const float inv0 = st.l0 > 0.f ? 1.f / st.l0 : 0.f;
-  const float inv1 = st.l1 > 0.f ? 1.f / st.l1 : 0.f;
+  const float inv0 = st.l0 > 0.f ? out_scale / st.l0 : 0.f;
+  const float inv1 = st.l1 > 0.f ? out_scale / st.l1 : 0.f;
   const int r0 = lane >> 2;
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) {
-    const int d0 = mt * 16 + r0;
+    // the dims of this lane's accumulators: rows r0 and r0 + 8 of the output
+    // tile (bf16 tiles) or dims 2 r0 and 2 r0 + 1 (e4m3 tiles)
+    const int d0 = kFp8 ? fp8_out_dim(mt, lane, false) : mt * 16 + r0;
+    const int d1 = kFp8 ? fp8_out_dim(mt, lane, true) : mt * 16 + r0 + 8;
     buf[tk * D + out_col(tk, d0)] = st.o[mt][0] * inv0;
     buf[(tk + 1) * D + out_col(tk + 1, d0)] = st.o[mt][1] * inv1;
-    buf[tk * D + out_col(tk, d0 + 8)] = st.o[mt][2] * inv0;
-    buf[(tk + 1) * D + out_col(tk + 1, d0 + 8)] = st.o[mt][3] * inv1;
+    buf[tk * D + out_col(tk, d1)] = st.o[mt][2] * inv0;
+    buf[(tk + 1) * D + out_col(tk + 1, d1)] = st.o[mt][3] * inv1;
   }
   // log-sum-exp (natural log) of the 8 columns: lanes 0..3 hold them
   float lse_a = -INFINITY, lse_b = -INFINITY;
@@ -302,11 +435,11 @@ __global__ void __launch_bounds__((kMaxColumnWarps + 1) * 32, 2)
   }
 }
 
-template <int D, bool kTma>
+template <int D, bool kTma, bool kFp8 = false>
 pa_status launch_multi(const CUtensorMap& mk, const CUtensorMap& mv, const MultiParams& prm,
                        int nc, int B, int num_kv_heads, cudaStream_t stream) {
   using L = MultiSmem<D>;
-  auto kern = multi_decode_kernel<D, kTma>;
+  auto kern = multi_decode_kernel<D, kTma, kFp8>;
   const int threads = (nc + 1) * 32;
   const pa_status s = prepare_kernel(reinterpret_cast<const void*>(kern), threads, L::kAlloc,
                                      nullptr);
@@ -1045,7 +1178,7 @@ extern "C" pa_status pa_decode_multi(const void* q, const void* k_cache, const v
     s = check_q_start(q_start, context_lens, num_seqs, num_q_rows, max_q_len, st);
     if (s != PA_OK) return s;
   }
-  MultiParams prm;
+  MultiParams prm{};
   prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.q_start = q_start;
   prm.block_tables = block_tables;
@@ -1100,6 +1233,80 @@ extern "C" pa_status pa_decode_multi(const void* q, const void* k_cache, const v
                : launch_multi<128, false>(mk, mv, prm, nc, num_seqs, num_kv_heads, st);
   return tma ? launch_multi<64, true>(mk, mv, prm, nc, num_seqs, num_kv_heads, st)
              : launch_multi<64, false>(mk, mv, prm, nc, num_seqs, num_kv_heads, st);
+}
+
+extern "C" pa_status pa_decode_multi_fp8(
+    const void* q, const void* k_codes, const void* v_codes, const float* k_scale,
+    const float* v_scale, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, const int32_t* q_start, int32_t num_seqs, int32_t num_q_rows,
+    int32_t max_q_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int32_t num_blocks, float scale, int32_t split_tokens, int32_t max_splits,
+    float* part_out, float* part_lse, int32_t* row_lens, void* out, void* stream) {
+  using namespace pa;
+  if (split_tokens < 0 || num_q_rows < 0 || max_q_len < 1) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0 || num_q_rows == 0) return PA_OK;
+  pa_status s = check_decode_args(q, k_codes, v_codes, block_tables, max_blocks_per_seq,
+                                  context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                  block_size, num_blocks, scale, out);
+  if (s != PA_OK) return s;
+  if (!q_start || !k_scale || !v_scale) return PA_ERR_INVALID_ARG;
+  if (head_dim != 128) return PA_ERR_UNSUPPORTED;  // one 128-byte e4m3 row per token
+  const int G = num_q_heads / num_kv_heads;
+  if ((long long)max_q_len * G > kMaxColumnWarps * 8) return PA_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  if (split_tokens > 0) {
+    if (split_tokens % kFp8Tile) return PA_ERR_INVALID_ARG;
+    if (max_splits <= 0 || max_splits > 65535) return PA_ERR_INVALID_ARG;
+    if (!part_out || !part_lse || !row_lens) return PA_ERR_WORKSPACE;
+    if (!aligned16(part_out)) return PA_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = as_stream(stream);
+  if (validating()) {
+    s = check_tables(block_tables, max_blocks_per_seq, context_lens, num_seqs, num_blocks,
+                     block_size, split_tokens, max_splits, st);
+    if (s != PA_OK) return s;
+    s = check_q_start(q_start, context_lens, num_seqs, num_q_rows, max_q_len, st);
+    if (s != PA_OK) return s;
+  }
+  MultiParams prm{};
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.q_start = q_start;
+  prm.block_tables = block_tables;
+  prm.context_lens = context_lens;
+  prm.part_out = part_out;
+  prm.part_lse = part_lse;
+  prm.row_lens = row_lens;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.src.k_cache = static_cast<const unsigned char*>(k_codes);
+  prm.src.v_cache = static_cast<const unsigned char*>(v_codes);
+  prm.src.num_kv_heads = num_kv_heads;
+  prm.src.block_size = block_size;
+  prm.src.log2_bs = ilog2(block_size);
+  prm.src.num_blocks = num_blocks;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.num_q_heads = num_q_heads;
+  prm.group = G;
+  prm.split_tokens = split_tokens;
+  prm.max_splits = split_tokens > 0 ? max_splits : 1;
+  prm.max_q_len = max_q_len;
+  prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  prm.k_scale = k_scale;
+  prm.v_scale = v_scale;
+  const int nc = (max_q_len * G + 7) / 8;
+
+  CUtensorMap mk, mv;
+  std::memset(&mk, 0, sizeof(mk));
+  std::memset(&mv, 0, sizeof(mv));
+  const bool tma = block_size >= 8;
+  if (tma) {
+    const long long rows = (long long)num_blocks * block_size;
+    const int box_rows = block_size < kFp8Tile ? block_size : kFp8Tile;
+    if (!make_cache_map(&mk, k_codes, num_kv_heads, head_dim, rows, box_rows, 1) ||
+        !make_cache_map(&mv, v_codes, num_kv_heads, head_dim, rows, box_rows, 1))
+      return PA_ERR_CUDA;
+  }
+  return tma ? launch_multi<128, true, true>(mk, mv, prm, nc, num_seqs, num_kv_heads, st)
+             : launch_multi<128, false, true>(mk, mv, prm, nc, num_seqs, num_kv_heads, st);
 }
 
 extern "C" size_t pa_decode_multi_balanced_workspace_bytes(int32_t num_seqs,
