@@ -292,6 +292,8 @@ KERNEL_SOURCES = {   # the files whose change invalidates a kernel's recorded DR
                                      "pa_device.cuh", "pa_api.cu"),
     "paged_decode_kernel": ("pa_decode.cu", "pa_tile.cuh", "pa_device.cuh", "pa_api.cu"),
     "multi_decode_kernel": ("pa_decode_multi.cu", "pa_tile.cuh", "pa_device.cuh", "pa_api.cu"),
+    "multi_decode_kernel[e4m3]": ("pa_decode_multi.cu", "pa_tile.cuh", "pa_device.cuh",
+                                  "pa_api.cu"),
     "balanced_multi_kernel": ("pa_decode_multi.cu", "pa_balance.cuh", "pa_tile.cuh",
                               "pa_device.cuh", "pa_api.cu"),
     "rowblock_decode_kernel": ("pa_decode_multi.cu", "pa_tile.cuh", "pa_device.cuh",
@@ -396,8 +398,12 @@ def run_gpu(args):
         cpu = cpu_baseline_subprocess(args)
 
     steps = Steps(args.workload, args.seed + rank, device, args.batch, args.kv_dtype)
-    if steps.fp8 and args.schedule != "balanced":
+    if steps.fp8 and not steps.multi and args.schedule != "balanced":
         raise SystemExit("--kv-dtype fp8 runs the balanced schedule only")
+    if steps.fp8 and (args.workload == "prefill" or
+                      (steps.multi and args.multi_schedule == "balanced")):
+        raise SystemExit("--kv-dtype fp8 with several query tokens runs the split schedule "
+                         "(--workload spec) only")
     sms = b.num_sms(local)
     if steps.multi:   # -1: the balanced schedule (pa_decode_multi_balanced)
         split = -1 if args.multi_schedule == "balanced" else (args.split if args.split >= 0
@@ -434,10 +440,20 @@ def run_gpu(args):
         if steps.multi:
             if ev is not None:
                 ev[0].record(stream)
-            b.pa_kv_append(dv["k_new"], dv["v_new"], dv["slots"], steps.k_cache, steps.v_cache)
+            if steps.fp8:
+                b.pa_kv_append_fp8(dv["k_new"], dv["v_new"], dv["slots"], steps.k_cache,
+                                   steps.v_cache, steps.k_scale, steps.v_scale)
+            else:
+                b.pa_kv_append(dv["k_new"], dv["v_new"], dv["slots"], steps.k_cache,
+                               steps.v_cache)
             if ev is not None:
                 ev[1].record(stream)
-            if ws.multi_balanced:
+            if steps.fp8:
+                b.pa_decode_multi_fp8(dv["q"], steps.k_cache, steps.v_cache, steps.k_scale,
+                                      steps.v_scale, dv["tables"], dv["lens"], dv["qstart"],
+                                      steps.max_q_len, steps.scale, ws.out, ws.split_tokens,
+                                      ws.max_splits, ws.part_out, ws.part_lse, ws.row_lens)
+            elif ws.multi_balanced:
                 b.pa_decode_multi_balanced(dv["q"], steps.k_cache, steps.v_cache, dv["tables"],
                                            dv["lens"], dv["qstart"], steps.max_q_len,
                                            steps.scale, ws.scratch, ws.out)
@@ -677,7 +693,8 @@ def run_gpu(args):
     dec_gbs_rank0 = dec_bytes / dec_s / 1e9
     kv_tokens_per_launch = kv_tokens / KI
     kernel = ("balanced_decode_kernel" + ("[e4m3]" if steps.fp8 else "")) if ws.balanced \
-        else (("balanced_multi_kernel" if ws.multi_balanced else "multi_decode_kernel")
+        else (("balanced_multi_kernel" if ws.multi_balanced else
+               "multi_decode_kernel" + ("[e4m3]" if steps.fp8 else ""))
               if steps.multi else "paged_decode_kernel")
     if args.workload == "prefill":
         kernel = ("rowblock_decode_kernel" if os.environ.get("PA_PREFILL_KERNEL") == "rowblock"
