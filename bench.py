@@ -878,9 +878,10 @@ def cpu_baseline_child(seed: int, budget_s: float) -> None:
     times, nbytes = oracle_steps(case, budget_s)
     print(json.dumps({"value": round(sum(nbytes) / sum(times) / 1e9, 4), "unit": "GB/s",
                       "cores": 1, "kind": "oracle",
-                      "sample": f"{len(times)} sequences of a 48-sequence sample of the 70B-shape "
-                                f"batch (log-uniform [128, 8192] tokens), fp64 oracle append + "
-                                f"decode, {blas_threads()} BLAS thread(s), {sum(times):.1f} s",
+                      "sample": f"{len(times)} one-sequence append + decode steps, cycling "
+                                f"through a seeded 48-sequence sample of the 70B-shape batch "
+                                f"(log-uniform [128, 8192] tokens), fp64 oracle, "
+                                f"{blas_threads()} BLAS thread(s), {sum(times):.1f} s",
                       "seconds": round(sum(times), 2), "host_cpus": os.cpu_count()}))
 
 
