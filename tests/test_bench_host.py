@@ -1,6 +1,8 @@
-"""Host-side arithmetic of bench.py: the causal (row, key) pair count behind
+"""Host-side parts of bench.py: the causal (row, key) pair count behind
 the chunked-prefill TFLOP/s, checked against a brute-force count of what the
-oracle's multi-token attention reads (row at position p reads keys 0..p)."""
+oracle's multi-token attention reads (row at position p reads keys 0..p); the
+source hash that keys recorded DRAM captures; and the reference arm's JSON
+line."""
 
 import numpy as np
 
@@ -42,3 +44,31 @@ def test_source_hash_ignores_comments_only():
     c = "int f(int x) {\n  return 3 * x;\n}\n"
     assert bench.code_of(a) == bench.code_of(b)
     assert bench.code_of(a) != bench.code_of(c)
+
+
+def test_reference_arm_prints_one_contract_line():
+    # the reference arm times the oracle on the host: one JSON line with the
+    # contract's keys, the bench's own metric, and its oracle baseline
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2",
+                        "--warmup", "1"], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["unit"] == "GB/s" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["n_gpus"] == 1
+    assert d["ms_per_step"] > 0 and d["vs_baseline"] is None and d["scaling"] == "weak"
+    assert d["data"] == "synthetic" and d["dtype"] == "f64" and "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] == 1
+    assert cb["unit"] == "GB/s" and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
