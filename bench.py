@@ -160,6 +160,7 @@ class Steps:
             self.items[-1]["flops"] = 4 * self.d * self.hq * attended
         elif workload == "cb70b":
             cb = wl.ContinuousBatching(seed=seed, batch=batch)
+            self.cb = cb
             self.k_cache, self.v_cache = cb.initial_caches(device)
             self.scale, self.hkv, self.hq, self.d = cb.scale, cb.Hkv, cb.Hq, cb.D
             self.max_context = cb.max_blocks * cb.bs
@@ -793,9 +794,64 @@ def run_gpu(args):
         line["clocks"] = clocks
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if getattr(steps, "cb", None) is not None and rank == 0:
+        host_ms = host_bookkeeping_ms(steps.cb)
+        e2e_ms = e2e_s / E * 1e3
+        line["host_bookkeeping"] = {
+            "ms_per_step": round(host_ms, 4), "steps": steps.cb.iterations,
+            "what": "the step's host side on the native prefix cache (pa_prefix_*): finished "
+                    "sequences discarded, joiners admitted with their prompt slots, one decode "
+                    "slot per sequence, block tables and lengths (median over the schedule)",
+            "wall_steps_per_s_serial": round(1e3 / (host_ms + e2e_ms), 1),
+            "note": "serial bound: the host work, then the e2e step (H2D of the step's inputs "
+                    "with its tables, the kernels, D2H of the output); a serving loop overlaps "
+                    "the two"}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def host_bookkeeping_ms(cb) -> float:
+    """Median host time of one continuous-batching step's scheduler work on
+    the native prefix cache, replaying the schedule's finishes and joins:
+    discard the finished sequences, admit each joiner's prompt (a token
+    stream no other sequence shares, so nothing is matched) and take its
+    slots, one decode slot per running sequence, then the block tables and
+    context lengths. The lengths must equal the schedule's."""
+    import numpy as np
+    from paged_kv_cache_45_gb300 import binding as b
+    pc = b.PrefixCache(cb.num_blocks, cb.bs)
+    uid = [0]
+
+    def prompt(n):
+        uid[0] += 1
+        return (uid[0] << 13) + np.arange(n, dtype=np.int32)   # positions < 8192 = 2^13
+
+    try:
+        ids = np.zeros(cb.B, dtype=np.int64)
+        for i in range(cb.B):      # the running batch before the first iteration (untimed)
+            n = int(cb.initial_lens[i])
+            sid, cached = pc.admit(prompt(n))
+            pc.write_slots(sid, cached, n)
+            ids[i] = sid
+        times = []
+        for it in range(cb.iterations):
+            sch = cb.schedule[it]
+            t0 = time.perf_counter()
+            if sch["finished"]:
+                pc.discard(ids[sch["finished"]])
+                for seq, plen in sch["joins"]:
+                    sid, cached = pc.admit(prompt(plen))
+                    pc.write_slots(sid, cached, plen)
+                    ids[seq] = sid
+            pc.append_tokens(ids)
+            _, lens = pc.tables(ids, cb.max_blocks)
+            times.append(time.perf_counter() - t0)
+            if not np.array_equal(lens, sch["lens"].numpy()):
+                raise RuntimeError(f"prefix cache lengths differ from the schedule at step {it}")
+        return statistics.median(times) * 1e3
+    finally:
+        pc.close()
 
 
 # ---------------------------------------------------------------------------

@@ -634,7 +634,8 @@ class PrefixCache:
         self._status("pa_prefix_write_slots", _lib.pa_prefix_write_slots(
             self._h, int(seq_id), int(p0), int(p1), slots.ctypes.data, src.ctypes.data,
             dst.ctypes.data, len(src), ctypes.byref(nc)))
-        return [int(x) for x in slots[:n]], [(int(src[i]), int(dst[i])) for i in range(nc.value)]
+        k = nc.value
+        return slots[:n].tolist(), list(zip(src[:k].tolist(), dst[:k].tolist()))
 
     def append_tokens(self, seq_ids):
         """One decode position per sequence: (slots int64 array, copies, done)."""
@@ -688,7 +689,7 @@ class PrefixCache:
         nb, nt = _i32(), _i32()
         self._status("pa_prefix_table", _lib.pa_prefix_table(
             self._h, int(seq_id), buf.ctypes.data, cap, ctypes.byref(nb), ctypes.byref(nt)))
-        return [int(x) for x in buf[:nb.value]]
+        return buf[:nb.value].tolist()
 
     def tables(self, seq_ids, max_blocks):
         """(block_tables int32 [n, max_blocks], context_lens int32 [n]) as numpy."""

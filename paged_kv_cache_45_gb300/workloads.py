@@ -28,6 +28,7 @@ Recipe (every draw is seeded):
 from __future__ import annotations
 
 import math
+import time
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -411,10 +412,13 @@ class ContinuousBatching:
         self.initial_lens = ctx0.copy()
         self.initial_blocks = [self.alloc.allocate(-(-int(c) // bs)) for c in ctx0]
 
-        # draw the whole schedule now (host bookkeeping only)
+        # draw the whole schedule now (host bookkeeping only). bookkeeping_seconds:
+        # the host time of the iterations' scheduler work (finishes, joins, one
+        # block table per step), the allocator's conservation check excluded
         lens = ctx0.copy()
         blocks = [list(b) for b in self.initial_blocks]
         self.schedule = []
+        t_start, t_check = time.perf_counter(), 0.0
         for it in range(iterations):
             fin = np.nonzero(rng.random(batch) < p_finish)[0].tolist()
             freed, joins = [], []
@@ -431,12 +435,15 @@ class ContinuousBatching:
                     blocks[b] += self.alloc.allocate(1)
                 slots[b] = token_rows(blocks[b], 1, bs, start=int(lens[b]))[0]
                 lens[b] += 1
+            tc = time.perf_counter()
             self.alloc.check()
+            t_check += time.perf_counter() - tc
             self.schedule.append(dict(
                 finished=fin, freed=freed, joins=joins, slots=slots,
                 tables=pad_tables(blocks, self.max_blocks),
                 lens=torch.from_numpy(lens.astype(np.int32).copy()),
                 blocks=[list(b) for b in blocks]))
+        self.bookkeeping_seconds = time.perf_counter() - t_start - t_check
 
     # -- tensors ---------------------------------------------------------------
     def initial_caches(self, device="cpu") -> tuple[torch.Tensor, torch.Tensor]:

@@ -72,3 +72,14 @@ def test_reference_arm_prints_one_contract_line():
     assert cb["unit"] == "GB/s" and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_host_bookkeeping_replays_the_schedule_on_the_native_cache():
+    # the continuous-batching schedule (finishes, joins, one token a step)
+    # replayed through pa_prefix_*: the native cache's context lengths equal
+    # the schedule's at every step (checked inside), and a time comes back
+    from paged_kv_cache_45_gb300 import workloads as wl
+    cb = wl.ContinuousBatching(seed=5, batch=48, iterations=12, p_finish=0.1)
+    assert sum(len(s["finished"]) for s in cb.schedule) > 0
+    ms = bench.host_bookkeeping_ms(cb)
+    assert 0.0 < ms < 1e3
