@@ -624,9 +624,11 @@ class PrefixCache:
         return sid.value, cached.value
 
     def write_slots(self, seq_id, p0, p1):
+        """Slots of positions [p0, p1) (int64 array) and the (src, dst) block
+        copies to make first."""
         import numpy as np
         n = max(p1 - p0, 0)
-        slots = np.zeros(max(n, 1), dtype=np.int64)
+        slots = np.empty(max(n, 1), dtype=np.int64)             # [0, n) is written
         nb = (p1 - 1) // self.block_size - p0 // self.block_size + 1 if n else 0
         src = np.zeros(max(nb, 1), dtype=np.int32)
         dst = np.zeros(max(nb, 1), dtype=np.int32)
@@ -635,7 +637,7 @@ class PrefixCache:
             self._h, int(seq_id), int(p0), int(p1), slots.ctypes.data, src.ctypes.data,
             dst.ctypes.data, len(src), ctypes.byref(nc)))
         k = nc.value
-        return slots[:n].tolist(), list(zip(src[:k].tolist(), dst[:k].tolist()))
+        return slots[:n], list(zip(src[:k].tolist(), dst[:k].tolist()))
 
     def append_tokens(self, seq_ids):
         """One decode position per sequence: (slots int64 array, copies, done)."""
@@ -695,8 +697,8 @@ class PrefixCache:
         """(block_tables int32 [n, max_blocks], context_lens int32 [n]) as numpy."""
         import numpy as np
         ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
-        t = np.zeros((len(ids), max_blocks), dtype=np.int32)
-        lens = np.zeros(len(ids), dtype=np.int32)
+        t = np.empty((len(ids), max_blocks), dtype=np.int32)    # every entry is written
+        lens = np.empty(len(ids), dtype=np.int32)
         self._status("pa_prefix_tables", _lib.pa_prefix_tables(
             self._h, ids.ctypes.data, len(ids), t.ctypes.data, int(max_blocks),
             lens.ctypes.data))

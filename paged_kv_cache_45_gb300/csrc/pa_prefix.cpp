@@ -23,17 +23,18 @@
 //   * a call needing more fresh blocks than the free blocks plus the blocks
 //     eviction could free at its start fails before changing anything.
 //
-// Data structures: an ordered free set; per-block reference counts, use ticks
+// Data structures: a free-block bitmap (lowest id out first); per-block
+// reference counts, use ticks
 // and (node, index) of cached blocks; children keyed by their first block's
 // tokens; a lazily validated min-heap of (tick, block) eviction candidates.
 
 #include <algorithm>
+#include <cstdint>
 #include <cstring>
 #include <functional>
 #include <map>
 #include <memory>
 #include <queue>
-#include <set>
 #include <unordered_map>
 #include <utility>
 #include <vector>
@@ -55,13 +56,44 @@ struct Seq {
   int32_t ntok = 0;
 };
 
+// The free blocks as a bitmap: freeing sets a bit, taking clears the lowest
+// set one. `low` is a word index below which every word is zero.
+struct FreeBlocks {
+  std::vector<uint64_t> words;
+  int32_t count = 0;
+  size_t low = 0;
+
+  void init(int32_t num_blocks) {
+    words.assign(((size_t)num_blocks + 63) / 64, 0);
+    count = 0;
+    low = words.size();
+  }
+  void insert(int32_t b) {
+    uint64_t& w = words[(size_t)b >> 6];
+    const uint64_t m = 1ull << (b & 63);
+    if (w & m) return;
+    w |= m;
+    ++count;
+    low = std::min(low, (size_t)b >> 6);
+  }
+  bool empty() const { return count == 0; }
+  int32_t size() const { return count; }
+  int32_t take_lowest() {  // callers check empty() first
+    while (words[low] == 0) ++low;
+    const int32_t b = (int32_t)(low * 64) + __builtin_ctzll(words[low]);
+    words[low] &= words[low] - 1;
+    --count;
+    return b;
+  }
+};
+
 }  // namespace
 }  // namespace pa
 
 struct pa_prefix_cache {
   int32_t nb = 0, bs = 0;
   int64_t tick = 0, next_seq = 1;
-  std::set<int32_t> free_set;
+  pa::FreeBlocks free_set;
   std::vector<int32_t> ref;
   std::vector<pa::Node*> node_of;  // cached block -> its node (nullptr: not cached)
   std::vector<int32_t> idx_of;     // index of a cached block in its node
@@ -157,9 +189,7 @@ struct pa_prefix_cache {
       evict_one();
     }
     if (free_set.empty()) return -1;
-    const int32_t b = *free_set.begin();
-    free_set.erase(free_set.begin());
-    return b;
+    return free_set.take_lowest();
   }
 
   // Longest cached block prefix of tokens[0, n): its blocks in order.
@@ -242,12 +272,15 @@ int64_t copies_needed(const pa_prefix_cache* pc, const pa::Seq& s, int32_t p0, i
   return n;
 }
 
-// The write itself (capacity already checked). Copies are appended.
+// The write itself (capacity already checked), one block at a time: a block
+// past the end is taken fresh, a cached or shared one is copied first (its
+// first written position decides, as the later ones then see the fresh
+// block); then the block's positions get their slots. Copies are appended.
 bool do_write(pa_prefix_cache* pc, pa::Seq& s, int32_t p0, int32_t p1, int64_t* slots,
               std::vector<std::pair<int32_t, int32_t>>& copies) {
   const int32_t bs = pc->bs;
-  for (int32_t p = p0; p < p1; ++p) {
-    const int32_t i = p / bs;
+  if (p1 <= p0) return true;
+  for (int32_t i = p0 / bs; i <= (p1 - 1) / bs; ++i) {
     if (i == (int32_t)s.blocks.size()) {
       const int32_t b = pc->take();
       if (b < 0) return false;
@@ -264,8 +297,12 @@ bool do_write(pa_prefix_cache* pc, pa::Seq& s, int32_t p0, int32_t p1, int64_t* 
         pc->drop_ref(old);
       }
     }
-    if (slots) slots[p - p0] = (int64_t)s.blocks[i] * bs + p % bs;
-    s.ntok = std::max(s.ntok, p + 1);
+    const int32_t q0 = std::max(p0, i * bs), q1 = std::min(p1, (i + 1) * bs);
+    if (slots) {
+      int64_t slot = (int64_t)s.blocks[i] * bs + (q0 - i * bs);
+      for (int32_t p = q0; p < q1; ++p) slots[p - p0] = slot++;
+    }
+    s.ntok = std::max(s.ntok, q1);
   }
   return true;
 }
@@ -284,7 +321,8 @@ extern "C" pa_status pa_prefix_cache_create(int32_t num_blocks, int32_t block_si
   pc->node_of.assign(num_blocks, nullptr);
   pc->idx_of.assign(num_blocks, 0);
   pc->last_use.assign(num_blocks, 0);
-  for (int32_t b = 1; b < num_blocks; ++b) pc->free_set.insert(pc->free_set.end(), b);
+  pc->free_set.init(num_blocks);
+  for (int32_t b = 1; b < num_blocks; ++b) pc->free_set.insert(b);
   *out = pc;
   return PA_OK;
 }
