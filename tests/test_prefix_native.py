@@ -14,7 +14,7 @@ from tests.prefix_trace import TraceRunner
 
 @pytest.mark.parametrize("num_blocks,block_size,seed", [
     (24, 4, 0), (24, 4, 1), (24, 4, 2), (40, 1, 3), (40, 2, 4), (64, 16, 5), (12, 4, 6),
-    (200, 4, 7), (200, 8, 8)])
+    (200, 4, 7), (200, 8, 8), (1000, 2, 9)])
 def test_native_matches_the_oracle_call_by_call(num_blocks, block_size, seed):
     model = pc.PrefixCacheModel(num_blocks, block_size)
     native = b.PrefixCache(num_blocks, block_size)
@@ -127,3 +127,33 @@ def test_fork_batch_and_discard_equal_their_single_calls():
     assert a.stats() == c.stats()
     for sa, sc in zip(ids_a, ids_c):
         assert a.table(sa) == c.table(sc)
+
+
+def test_fresh_blocks_lowest_first_across_a_large_pool():
+    # most of a 2000-block pool taken, a random half of the sequences ended
+    # (their blocks back on the free list in scattered order), then refilled:
+    # every table equals the oracle model's, which takes the lowest free id
+    rng = np.random.default_rng(11)
+    nb, bs = 2000, 2
+    model, native = pc.PrefixCacheModel(nb, bs), b.PrefixCache(nb, bs)
+    live, uid = [], 0
+    for rnd in range(3):
+        while True:
+            n = int(rng.integers(1, 60))
+            if native.stats()[0] < -(-n // bs):
+                break
+            uid += 1
+            toks = [uid * 1000 + i for i in range(n)]     # no shared prefixes
+            sid_m, _ = model.admit(toks)
+            sid_n, _ = native.admit(toks)
+            assert sid_m == sid_n
+            live.append(sid_n)
+        for sid in live:
+            assert native.table(sid) == model.table(sid)
+        assert native.stats() == model.stats()
+        ended = [s for s in live if rng.random() < 0.5]
+        for sid in ended:
+            model.release(sid, [])
+        native.discard(ended)
+        live = [s for s in live if s not in ended]
+        assert native.stats() == model.stats()
