@@ -119,3 +119,69 @@ def test_bad_arguments_are_rejected_before_any_launch(lib):
                                        None) == -1
     assert lib.pa_decode_splitk_reduce(fake, fake, fake, T(2), T(8), T(80), T(16), T(4), fake,
                                        None) == -2
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "pagedkv.h"
+
+int main(void) {
+  if (strcmp(pa_status_str(PA_OK), "PA_OK") != 0) return 1;
+  if (pa_kv_bytes_per_token(80, 8, 128, 2) != 327680) return 2;
+  if (pa_decode_num_splits(131073, 4096) != 33) return 3;
+  pa_prefix_cache* pc = NULL;
+  if (pa_prefix_cache_create(64, 4, &pc) != PA_OK || !pc) return 4;
+  int32_t toks[10];
+  for (int i = 0; i < 10; ++i) toks[i] = 100 + i;
+  int64_t sid = 0;
+  int32_t cached = -1;
+  if (pa_prefix_admit(pc, toks, 10, &sid, &cached) != PA_OK || sid <= 0 || cached != 0) return 5;
+  int64_t slots[10];
+  int32_t src[4], dst[4], nc = -1;
+  if (pa_prefix_write_slots(pc, sid, 0, 10, slots, src, dst, 4, &nc) != PA_OK || nc != 0)
+    return 6;
+  for (int p = 0; p < 10; ++p)  /* fresh blocks lowest id first: 1, 2, 3 */
+    if (slots[p] != (int64_t)(1 + p / 4) * 4 + p % 4) return 7;
+  int32_t table[8], lens[1];
+  if (pa_prefix_tables(pc, &sid, 1, table, 8, lens) != PA_OK || lens[0] != 10 ||
+      table[0] != 1 || table[2] != 3 || table[3] != 0)
+    return 8;
+  int32_t free_blocks = -1, cached_blocks = -1, used = -1;
+  if (pa_prefix_stats(pc, &free_blocks, &cached_blocks, &used) != PA_OK || free_blocks != 60 ||
+      used != 3)
+    return 9;
+  if (pa_prefix_discard(pc, &sid, 1) != PA_OK) return 10;
+  if (pa_prefix_stats(pc, &free_blocks, &cached_blocks, &used) != PA_OK || free_blocks != 63 ||
+      used != 0)
+    return 11;
+  pa_prefix_cache_destroy(pc);
+  if (pa_kv_append(NULL, NULL, NULL, 1, NULL, NULL, 16, 16, 8, 128, NULL) != PA_ERR_INVALID_ARG)
+    return 12;
+  printf("ok %s\n", pa_version());
+  return 0;
+}
+"""
+
+
+def test_header_compiles_as_c_and_the_library_links(tmp_path):
+    # the boundary is a plain C ABI: a C11 program includes the header, links
+    # the library and makes host-only calls (no GPU needed)
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    lib_path = pk_build.build()
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi"
+    lib_dir = os.path.dirname(lib_path)
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I",
+                        os.path.join(ROOT, "include"), str(src), "-o", str(exe), "-L", lib_dir,
+                        "-l:" + os.path.basename(lib_path), "-Wl,-rpath," + lib_dir],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    assert r.stdout.startswith("ok ") and "sm_103a" in r.stdout
