@@ -315,7 +315,7 @@ def test_gpu_block_size_1_vs_16_bit_identical(cuda_lib, sched):
 # the full-size 8B and prefix-sharing workloads
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("seed", [0, 1])
+@pytest.mark.parametrize("seed", [0, 1, 2])
 def test_8b_workload_full(cuda_lib, seed):
     case = wl.llama8b_case(seed)
     split = cuda_lib.plan_split(case.context_lens.numpy(), 8, cuda_lib.num_sms())

@@ -14,14 +14,15 @@ from tests import parity as P
 pytestmark = pytest.mark.gpu
 
 
-def test_continuous_batching_70b_shape(cuda_lib):
+@pytest.mark.parametrize("seed,iterations", [(0, 32), (1, 8)])
+def test_continuous_batching_70b_shape(cuda_lib, seed, iterations):
     b = cuda_lib
-    cb = wl.ContinuousBatching(seed=0)
+    cb = wl.ContinuousBatching(seed=seed, iterations=iterations)
     kc_cpu, vc_cpu = cb.initial_caches("cpu")
     kc, vc = kc_cpu.cuda(), vc_cpu.cuda()
     kf, vf = kc_cpu.cuda(), vc_cpu.cuda()          # a second pool for the fused step
     ko, vo = wl.bits(kc_cpu), wl.bits(vc_cpu)          # oracle state (CPU, updated in place)
-    rng = np.random.default_rng(0)
+    rng = np.random.default_rng(seed)
     max_ctx = cb.max_blocks * cb.bs
     ws_bal = b.DecodeWorkspace(cb.B, cb.Hq, cb.D, b.BALANCED, device="cuda", num_kv_heads=cb.Hkv)
     fused_out = torch.empty((cb.B, cb.Hq, cb.D), dtype=torch.bfloat16, device="cuda")
