@@ -114,6 +114,18 @@ def test_every_block_size(cuda_lib, bs, sched):
     P.assert_close(P.to_f64(out), P.oracle_out(case), f"bs={bs} sched={sched}")
 
 
+@pytest.mark.parametrize("sched", [0, BAL], ids=["per_split", "balanced"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_every_short_context(cuda_lib, g, d, sched):
+    # the tiny-shape sweep: every context length 1..40 (40 sequences, one
+    # appended token each) for each block size 1, 8, 16, 32
+    for bs in (1, 8, 16, 32):
+        case = wl.make_case("short", 900 + 10 * g + d + bs, list(range(40)), 2 * g, 2, d, bs)
+        out, _, _ = run_step(cuda_lib, case, split=sched)
+        P.assert_close(P.to_f64(out), P.oracle_out(case), f"G={g} D={d} bs={bs} sched={sched}")
+
+
 @pytest.mark.parametrize("lens", [[5], [0, 0, 3], [1] * 7, [2000, 1, 0, 17, 4096, 33] * 20,
                                   list(range(0, 700, 7))],
                          ids=["one_seq", "mostly_empty", "fewer_tiles_than_workers", "mixed_120",
@@ -281,6 +293,37 @@ def test_gpu_block_permutation_is_bit_invisible(cuda_lib, sched):
     perm.slot_mapping = torch.from_numpy(pi[s // 16] * 16 + s % 16)
     out2, _, _ = run_step(cuda_lib, perm, split=sched)
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def copied_prefix_case(case, prefix_blocks):
+    """The case with every sequence but the first reading its own copy of the
+    shared prefix blocks (appended after the pool), the same rows otherwise."""
+    bt = case.block_tables.numpy()
+    assert (bt[:, :prefix_blocks] == bt[0, :prefix_blocks]).all()
+    B, nb = bt.shape[0], case.num_blocks
+    src = torch.from_numpy(np.tile(bt[0, :prefix_blocks], B - 1).astype(np.int64))
+    bt2 = bt.copy()
+    for i in range(1, B):
+        bt2[i, :prefix_blocks] = nb + (i - 1) * prefix_blocks + np.arange(prefix_blocks)
+    cp = wl.DecodeCase(**{**case.__dict__})
+    cp.k_cache = torch.cat([case.k_cache, case.k_cache[src]])
+    cp.v_cache = torch.cat([case.v_cache, case.v_cache[src]])
+    cp.block_tables = torch.from_numpy(bt2)
+    cp.num_blocks = nb + (B - 1) * prefix_blocks
+    return cp
+
+
+@pytest.mark.parametrize("sched", [0, BAL], ids=["per_split", "balanced"])
+def test_gpu_shared_prefix_equals_copied_prefix(cuda_lib, sched):
+    # sharing is only naming: the same rows reached through one set of
+    # prefix blocks or through private copies give the same bits
+    pref = 256
+    case = wl.make_case("pfxg", 510, [pref + x for x in (0, 5, 16, 100, 700, 1)], 8, 2, 128, 16,
+                        shared_prefix=pref)
+    out1, _, _ = run_step(cuda_lib, case, split=sched)
+    out2, _, _ = run_step(cuda_lib, copied_prefix_case(case, pref // 16), split=sched)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    P.assert_close(P.to_f64(out1), P.oracle_out(case), f"shared prefix sched={sched}")
 
 
 @pytest.mark.parametrize("sched", [0, BAL], ids=["per_split", "balanced"])
