@@ -24,9 +24,9 @@
 //     eviction could free at its start fails before changing anything.
 //
 // Data structures: a free-block bitmap (lowest id out first); per-block
-// reference counts, use ticks
-// and (node, index) of cached blocks; children keyed by their first block's
-// tokens; a lazily validated min-heap of (tick, block) eviction candidates.
+// reference counts, use ticks and (node, index) of cached blocks; children
+// keyed by their first block's tokens; a lazily validated min-heap of
+// (tick, block) eviction candidates.
 
 #include <algorithm>
 #include <cstdint>
