@@ -145,12 +145,14 @@ pa_status pa_decode_splitk_reduce(const float* part_out, const float* part_lse,
 /*
  * pa_decode_balanced -- the same attention as pa_decode, in one launch,
  * scheduled for a continuously batched mix of lengths: the 16-token tiles of
- * all (sequence, KV head) pairs are divided into equal contiguous ranges, one
- * per warp of a persistent grid (two thread blocks per SM, four warps each),
- * so every warp streams the same number of KV bytes whatever the lengths. A
- * (sequence, KV head) pair cut by a range boundary is merged by log-sum-exp
- * (the running-max rescale of [TGI-FA]) by the last warp to finish its part;
- * no separate reduce call is needed. Layouts, supported shapes and error
+ * all (sequence, KV head) pairs are divided into contiguous ranges, one per
+ * thread block of a persistent grid (four blocks per SM; inside a block a
+ * loader warp streams the range and the consumer warps fold its tiles
+ * round-robin). The ranges are equal in tiles plus a fixed charge per pair
+ * for its end-of-pair merge, so every block does the same work whatever the
+ * lengths. A (sequence, KV head) pair cut by a range boundary is merged by
+ * log-sum-exp (the running-max rescale of [TGI-FA]) by the last block to
+ * finish its part; no separate reduce call is needed. Layouts, supported shapes and error
  * behaviour are those of pa_decode; context_lens stay on the device (the
  * schedule is computed there).
  *
@@ -267,9 +269,11 @@ size_t pa_decode_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads
  * until the process exits). Inputs, output, layouts and supported shapes are
  * those of pa_decode_balanced; the output is the same.
  *
- *   - Shapes whose scratch (pa_decode_balanced_workspace_bytes) exceeds
- *     6 MiB return PA_ERR_WORKSPACE without launching. On a 152-SM GB300 at
- *     head_dim 128 that limit is about 310,000 (sequence, KV head) pairs.
+ *   - Shapes whose scratch exceeds 6 MiB return PA_ERR_WORKSPACE without
+ *     launching or writing anything. The test a caller can make beforehand:
+ *     pa_decode_balanced_workspace_bytes(num_seqs, num_kv_heads, head_dim)
+ *     <= 6,291,456. On a 152-SM GB300 that admits up to 317,952
+ *     (sequence, KV head) pairs at head_dim 128 and 940,544 at head_dim 64.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture on the device.

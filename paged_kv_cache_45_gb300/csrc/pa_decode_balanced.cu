@@ -659,7 +659,10 @@ void* static_scratch(int dev) {
   std::lock_guard<std::mutex> lock(g_static_mu);
   if (!g_static_ptr[dev]) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess) {
+      cudaGetLastError();  // leave no error behind for the next launch check
+      return nullptr;
+    }
     g_static_ptr[dev] = ptr;
   }
   return g_static_ptr[dev];
@@ -857,14 +860,19 @@ extern "C" pa_status pa_decode_balanced_static(const void* q, const void* k_cach
   const WsLayout lay = ws_layout(num_seqs, num_kv_heads, head_dim, sms * kMaxBlocksPerSM);
   if (lay.total > kStaticScratchBytes) return PA_ERR_WORKSPACE;  // beyond the built-in 6 MiB
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return PA_ERR_CUDA;
+  }
   unsigned char* scratch = static_cast<unsigned char*>(static_scratch(dev));
   if (!scratch) return PA_ERR_CUDA;
   // The array keeps whatever the previous call left; the per-unit counters
   // must start at zero, so clear them on this call's stream first.
   if (cudaMemsetAsync(scratch + lay.counters, 0, (size_t)num_seqs * num_kv_heads * sizeof(int),
-                      as_stream(stream)) != cudaSuccess)
+                      as_stream(stream)) != cudaSuccess) {
+    cudaGetLastError();
     return PA_ERR_CUDA;
+  }
   return pa_decode_balanced(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                             num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                             scale, scratch, kStaticScratchBytes, out, stream);

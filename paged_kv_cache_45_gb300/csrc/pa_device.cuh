@@ -176,17 +176,6 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two e4m3 bytes (low byte = first element) -> f16x2 (low half = first);
-// exact: every e4m3 value is an f16 value.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
-  uint32_t d;
-  asm volatile(
-      "{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-      : "=r"(d)
-      : "r"(pair16));
-  return d;
-}
-
 // Two floats -> two e4m3 bytes (low byte = lo), round to nearest even,
 // saturating to +-448.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {

@@ -484,8 +484,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float e0 = ex2_approx(x0);
         const float e1 = ex2_approx(x1);
         const int a = (c >> 1) & 3;
-        add2(sum8[2 * a], sum8[2 * a + 1], e0, e1);
-        pk[c >> 1] = pack_bf16x2(e0, e1);
+        // the running sum adds the bf16-rounded weights that multiply V
+        const uint32_t pr = pack_bf16x2(e0, e1);
+        pk[c >> 1] = pr;
+        add2(sum8[2 * a], sum8[2 * a + 1], bf16_lo(pr), bf16_hi(pr));
       }
       tmem_st64_sync(t_s, pk);
       const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
