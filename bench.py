@@ -806,50 +806,106 @@ def run_gpu(args):
             "note": "serial bound: the host work, then the e2e step (H2D of the step's inputs "
                     "with its tables, the kernels, D2H of the output); a serving loop overlaps "
                     "the two"}
+        p_ms, p_ev = host_bookkeeping_ms(steps.cb, pressure=True)
+        line["host_bookkeeping_pressure"] = {
+            "ms_per_step": round(p_ms, 4), "evicted_blocks_per_step": round(p_ev, 1),
+            "what": "the same steps with the pool full of cached prefixes: joiners share 8 "
+                    "system prompts of 512 tokens, finished sequences are released into the "
+                    "cache, and fresh blocks come mostly from LRU eviction",
+            "wall_steps_per_s_serial": round(1e3 / (p_ms + e2e_ms), 1)}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def host_bookkeeping_ms(cb) -> float:
+def host_bookkeeping_ms(cb, pressure: bool = False):
     """Median host time of one continuous-batching step's scheduler work on
     the native prefix cache, replaying the schedule's finishes and joins:
     discard the finished sequences, admit each joiner's prompt (a token
     stream no other sequence shares, so nothing is matched) and take its
     slots, one decode slot per running sequence, then the block tables and
-    context lengths. The lengths must equal the schedule's."""
+    context lengths. The lengths must equal the schedule's.
+
+    pressure=True: the serving case where the prefix cache has filled the
+    pool. Before the first step every free block is taken by cached, unused
+    prefixes; joiners' prompts begin with one of 8 shared 512-token system
+    prompts; finished sequences are released with their tokens (their full
+    blocks stay cached; their partial last blocks go back to the free
+    list). The fresh blocks a step takes then come mostly from evicting the
+    least recently used unreferenced prefixes ([PYS] "The radix prefix
+    cache"). Returns (median ms, blocks evicted per step on average)."""
     import numpy as np
     from paged_kv_cache_45_gb300 import binding as b
     pc = b.PrefixCache(cb.num_blocks, cb.bs)
     uid = [0]
+    sys_len = 512
+    systems = [(1 << 30) + (k << 13) + np.arange(sys_len, dtype=np.int32) for k in range(8)]
 
-    def prompt(n):
+    def private(u, p0, p1):
+        return (u << 13) + np.arange(p0, p1, dtype=np.int32)   # positions < 8192 = 2^13
+
+    def prompt(n, shared):
         uid[0] += 1
-        return (uid[0] << 13) + np.arange(n, dtype=np.int32)   # positions < 8192 = 2^13
+        if not shared:
+            return uid[0], -1, private(uid[0], 0, n)
+        k = uid[0] % len(systems)
+        s = min(sys_len, n - 1)
+        return uid[0], k, np.concatenate([systems[k][:s], private(uid[0], s, n)])
+
+    def tokens_of(u, k, n):     # a sequence's tokens after n positions
+        if k < 0:
+            return private(u, 0, n)
+        s = min(sys_len, n)
+        return np.concatenate([systems[k][:s], private(u, s, n)])
 
     try:
         ids = np.zeros(cb.B, dtype=np.int64)
+        who = [None] * cb.B        # (uid, system prompt or -1) of each slot's sequence
         for i in range(cb.B):      # the running batch before the first iteration (untimed)
             n = int(cb.initial_lens[i])
-            sid, cached = pc.admit(prompt(n))
+            u, k, toks = prompt(n, False)
+            sid, cached = pc.admit(toks)
             pc.write_slots(sid, cached, n)
             ids[i] = sid
-        times = []
+            who[i] = (u, k)
+        if pressure:               # fill the pool with cached, unreferenced prefixes
+            while pc.stats()[0] > 0:
+                n = min(2048, pc.stats()[0] * cb.bs)
+                _, _, toks = prompt(n, False)
+                sid, cached = pc.admit(toks)
+                pc.write_slots(sid, cached, n)
+                pc.release(sid, toks)
+        times, evicted = [], 0
         for it in range(cb.iterations):
             sch = cb.schedule[it]
+            fin = sch["finished"]
+            prev = cb.initial_lens if it == 0 else cb.schedule[it - 1]["lens"].numpy()
+            done = [tokens_of(*who[i], int(prev[i])) for i in fin] if pressure else []
+            joins = [(seq, plen) + prompt(plen, pressure) for seq, plen in sch["joins"]]
+            cached0 = pc.stats()[1]
             t0 = time.perf_counter()
-            if sch["finished"]:
-                pc.discard(ids[sch["finished"]])
-                for seq, plen in sch["joins"]:
-                    sid, cached = pc.admit(prompt(plen))
+            if fin:
+                if pressure:
+                    for i, toks in zip(fin, done):
+                        pc.release(int(ids[i]), toks)
+                else:
+                    pc.discard(ids[fin])
+                for seq, plen, u, k, toks in joins:
+                    sid, cached = pc.admit(toks)
                     pc.write_slots(sid, cached, plen)
                     ids[seq] = sid
+                    who[seq] = (u, k)
             pc.append_tokens(ids)
             _, lens = pc.tables(ids, cb.max_blocks)
             times.append(time.perf_counter() - t0)
             if not np.array_equal(lens, sch["lens"].numpy()):
                 raise RuntimeError(f"prefix cache lengths differ from the schedule at step {it}")
-        return statistics.median(times) * 1e3
+            if pressure:
+                # blocks cached by this step's releases, minus those still cached
+                added = sum(len(t) // cb.bs for t in done)
+                evicted += max(cached0 + added - pc.stats()[1], 0)
+        ms = statistics.median(times) * 1e3
+        return (ms, evicted / cb.iterations) if pressure else ms
     finally:
         pc.close()
 

@@ -509,6 +509,14 @@ pa_status pa_prefix_tables(pa_prefix_cache* cache, const int64_t* seq_ids, int32
 pa_status pa_prefix_stats(const pa_prefix_cache* cache, int32_t* free_blocks,
                           int32_t* cached_blocks, int32_t* used_blocks);
 
+/* Blocks that eviction could free right now: cached, referenced by no live
+ * sequence, with no referenced block after them on their prefix's path (in
+ * their tree node or below it). A call succeeds when the fresh blocks it
+ * needs are at most free_blocks + this count ([PYS] "The radix prefix
+ * cache": least recently used unreferenced prefixes are evicted when the
+ * free list is empty). Kept up to date on every change: O(1). */
+pa_status pa_prefix_evictable(const pa_prefix_cache* cache, int32_t* evictable_blocks);
+
 /* Copy-on-write on the device: for i < num_copies, block dst[i] of both
  * caches becomes a byte copy of block src[i]. src, dst: device int32
  * [num_copies]; a block is block_bytes bytes (block_size * num_kv_heads *

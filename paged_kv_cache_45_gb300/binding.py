@@ -69,6 +69,7 @@ _SIGS = {
     "pa_prefix_table": (_i32, [_p, _i64, _p, _i32, _p, _p]),
     "pa_prefix_tables": (_i32, [_p, _p, _i32, _p, _i32, _p]),
     "pa_prefix_stats": (_i32, [_p, _p, _p, _p]),
+    "pa_prefix_evictable": (_i32, [_p, _p]),
     "pa_copy_blocks": (_i32, [_p, _p, _p, _p, _i32, _i32, _i64, _p]),
     "pa_status_str": (ctypes.c_char_p, [_i32]),
     "pa_version": (ctypes.c_char_p, []),
@@ -709,6 +710,13 @@ class PrefixCache:
         _check("pa_prefix_stats", _lib.pa_prefix_stats(self._h, ctypes.byref(f), ctypes.byref(c),
                                                        ctypes.byref(u)))
         return f.value, c.value, u.value
+
+    def evictable(self) -> int:
+        """Blocks eviction could free now (cached, unreferenced, nothing
+        referenced after them on their prefix path)."""
+        e = _i32()
+        _check("pa_prefix_evictable", _lib.pa_prefix_evictable(self._h, ctypes.byref(e)))
+        return e.value
 
 
 def pa_copy_blocks(k_cache, v_cache, src, dst, stream=None) -> None:

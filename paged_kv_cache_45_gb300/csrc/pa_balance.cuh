@@ -5,9 +5,11 @@
 // Work is a list of units, one per (sequence, KV head), sequence-major; a unit
 // holds the TT-token tiles of its sequence's context. S[b] counts the tiles of
 // the sequences before b, so unit (b, h) starts at global tile
-// Hkv * S[b] + h * n_b. Block c of W owns the global tiles
-// [c N / W, (c + 1) N / W): every block gets the same number of tiles, and a
-// unit cut by a range boundary is merged across blocks by log-sum-exp.
+// Hkv * S[b] + h * n_b. Block c of W owns a contiguous range of that list:
+// the multi-token kernel splits it into equal tile counts
+// [c N / W, (c + 1) N / W); the decode kernel charges each unit a fixed
+// number of extra positions for its end-of-unit merge (Partition). A unit cut
+// by a range boundary is merged across blocks by log-sum-exp.
 #pragma once
 
 #include "pa_device.cuh"
@@ -24,6 +26,63 @@ __device__ __forceinline__ int tiles_of(int ctx, int cap) {
 __device__ __forceinline__ int owner_of(long long g, long long N, long long W) {
   return (int)(((g + 1) * W - 1) / N);
 }
+
+// The block ranges with a fixed charge per unit. A unit's tiles are not all
+// the work it costs: at its end the consumer warps merge their states (and a
+// cut unit publishes a partial), which stalls the block's pipeline for about
+// as long as K tiles take to stream. Unit (b, h) with n_b tiles therefore
+// occupies n_b + K positions on a weighted line, its tiles first:
+//   start(b, h) = Hkv * (S[b] + K b) + h (n_b + K),
+// and block c of W owns the tiles whose positions fall in
+// [c Nw / W, (c + 1) Nw / W), Nw = Hkv (S[B] + K B). (Every sequence is
+// charged K per head, also an empty one: padding rows cost a few idle
+// positions and keep the start a closed form of S.) K = 0 gives equal tile
+// counts. Ownership stays contiguous in the unit list, so a cut unit is still
+// merged by the blocks c0..c1 that own its first and last tiles.
+struct Partition {
+  long long N;   // tiles (Hkv * S[B])
+  long long Nw;  // weighted positions
+  long long W;   // blocks that own a range
+  int K;         // charge per unit, in tiles
+
+  __device__ __forceinline__ void init(const int* S, int B, int hkv, int unit_cost, int grid) {
+    K = unit_cost;
+    N = (long long)hkv * S[B];
+    Nw = (long long)hkv * ((long long)S[B] + (long long)K * B);
+    W = N == 0 ? 0 : min((long long)grid, Nw);
+  }
+  __device__ __forceinline__ long long start(const int* S, int hkv, int b) const {
+    return (long long)hkv * ((long long)S[b] + (long long)K * b);
+  }
+  // weighted position of tile t of unit (b, h), n = the unit's tiles
+  __device__ __forceinline__ long long pos(const int* S, int hkv, int b, int h, int n,
+                                           int t) const {
+    return start(S, hkv, b) + (long long)h * (n + K) + t;
+  }
+  __device__ __forceinline__ int owner(long long x) const { return owner_of(x, Nw, W); }
+  // global tiles (unit-list order) at weighted positions < x
+  __device__ __forceinline__ long long tiles_before(long long x, const int* S, int B,
+                                                    int hkv) const {
+    if (x >= Nw) return N;
+    int lo = 0, hi = B - 1;  // largest b with start(b) <= x
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (start(S, hkv, mid) <= x) lo = mid; else hi = mid - 1;
+    }
+    const long long n = S[lo + 1] - S[lo];
+    const long long r = x - start(S, hkv, lo);
+    const long long w = n + K;  // > 0: an empty last sequence with K = 0 has x >= Nw
+    const long long h = r / w;
+    const long long t = r - h * w;
+    return (long long)hkv * S[lo] + h * n + (t < n ? t : n);
+  }
+  // block c's tiles: global indices [g0, g1)
+  __device__ __forceinline__ void range(int c, const int* S, int B, int hkv, long long& g0,
+                                        long long& g1) const {
+    g0 = tiles_before((long long)c * Nw / W, S, B, hkv);
+    g1 = tiles_before((long long)(c + 1) * Nw / W, S, B, hkv);
+  }
+};
 
 // Position (sequence, KV head, tile) in the unit list.
 struct Cursor {

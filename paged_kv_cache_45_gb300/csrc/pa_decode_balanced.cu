@@ -56,16 +56,20 @@ __device__ __forceinline__ void report(unsigned int bits) { atomicOr(&g_balanced
 // SM (16 tiles in flight per SM). Chosen by measurement on the 70B-shape
 // continuous batch over {4 warps x 8 stages x 2 blocks, 8 x 8 x 2}, which
 // reached 71% and 66% of HBM peak against this shape's 93%.
-// The ring depth must be a multiple of the consumer count: then every stage
-// is always read by the same warp, which polls a stage's "full" barrier only
-// after consuming that stage's previous tile, so the barrier is never more
-// than one phase ahead of the parity the warp waits for.
+// With the ring depth a multiple of the consumer count every stage is always
+// read by the same warp, which polls a stage's "full" barrier only after
+// consuming that stage's previous tile, so the barrier is never more than one
+// phase ahead of the parity the warp waits for. (Other depths need one more
+// wait per tile, in the consumer loop.)
 constexpr int kConsumers = 4;
 constexpr int kStages = 4;
 // e4m3 tiles cost twice the math per byte: two consumer warps with two ring
 // stages each overlap a warp's tile math with its next tile's load (measured
 // on the 70B batch: 0.1875 ms per step against 0.2021 with 4 x 1)
 constexpr int kConsumersFp8 = 2;
+// and five ring stages (the most that fit four blocks per SM): 2.5 stages per
+// warp keep more bytes in flight while a warp computes
+constexpr int kStagesFp8 = 5;
 constexpr int kBlocksPerSM = 4;
 constexpr int kMaxBlocksPerSM = kBlocksPerSM;
 
@@ -82,6 +86,7 @@ struct BalParams {
   int num_seqs;
   int num_q_heads;
   int group;
+  int unit_cost;  // tiles charged per unit for its merge (the Partition's K)
   float scale_log2;
   // fused append (pa_append_decode): one new K/V row per sequence
   const __nv_bfloat16* k_new;  // [num_seqs, Hkv, D]
@@ -138,7 +143,11 @@ template <int D, bool kTma, int NC, int STAGES, int BPS, bool kMma, bool kAppend
 __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     balanced_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const BalParams p) {
-  static_assert(STAGES % NC == 0, "each ring stage must belong to one consumer warp");
+  // A stage read by different warps on successive uses (STAGES % NC != 0) is
+  // safe when the warp that reads tile j also read tile j - 2 STAGES: then it
+  // waits for the stage's previous tile to be released before it polls the
+  // stage's "full" barrier (see the consumer loop).
+  static_assert((2 * STAGES) % NC == 0, "tile j - 2 STAGES must belong to tile j's warp");
   static_assert(BPS <= kMaxBlocksPerSM, "workspace is sized for kMaxBlocksPerSM blocks per SM");
   static_assert(!kFp8 || (D == 128 && kMma), "FP8 tiles: head_dim 128, tensor-core math");
   constexpr int EB = kFp8 ? 1 : 2;  // bytes per cache element
@@ -231,12 +240,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
   }
 
   // ---- this block's tile range -----------------------------------------------
-  const long long N = (long long)S[B] * hkv;
-  const long long W = min((long long)gridDim.x, N);
+  Partition part;
+  part.init(S, B, hkv, p.unit_cost, gridDim.x);
   const int c = blockIdx.x;
-  if (c >= W) return;
-  const long long g0 = (long long)c * N / W, g1 = (long long)(c + 1) * N / W;
+  if (c >= part.W) return;
+  long long g0, g1;
+  part.range(c, S, B, hkv, g0, g1);
   const int count = (int)(g1 - g0);
+  if (count == 0) return;
   const uint32_t ring = smem_u32(smem);
   const uint32_t q_bytes = (uint32_t)(G * D * 2);
 
@@ -394,6 +405,19 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     for (int j = j0 + ((warp - j0) % NC + NC) % NC; j < j0 + m; j += NC) {
       if (__any_sync(0xffffffffu, *abort_flag)) break;
       const int stage = j % STAGES;
+      if constexpr (STAGES % NC != 0) {
+        // The stage's previous tile (j - STAGES) belongs to another warp and
+        // may not have landed yet; "full" must not be polled two phases
+        // ahead, so first wait until that tile was released (its release
+        // implies it landed). Tile j - 2 STAGES was this warp's, so "empty"
+        // is at most one phase behind the parity waited for here.
+        if (j >= STAGES &&
+            !__all_sync(0xffffffffu, mbar_wait(&empty[stage], ((j / STAGES) - 1) & 1))) {
+          if (lane == 0) report(kErrWaitFull);
+          *abort_flag = 1;
+          break;
+        }
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], (j / STAGES) & 1))) {
         if (lane == 0) report(kErrWaitFull);
         *abort_flag = 1;
@@ -488,8 +512,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     // whether to stop after this unit (the loader may set it at any time)
     if (tid == 0) *stop_s = *abort_flag;
 
-    const long long U = (long long)hkv * S[b] + (long long)kvh * uc.n;
-    const int c0 = owner_of(U, N, W), c1 = owner_of(U + uc.n - 1, N, W);
+    const long long U = part.pos(S, hkv, b, kvh, uc.n, 0);
+    const int c0 = part.owner(U), c1 = part.owner(U + uc.n - 1);
     const bool cut = c0 != c1;
     const int rec = 2 * c + (c == c0 ? 1 : 0);
     __nv_bfloat16* orow = p.out + ((size_t)b * p.num_q_heads + kvh * G) * D;
@@ -608,6 +632,20 @@ pa_status launch_shape(const CUtensorMap& mk, const CUtensorMap& mv, const BalPa
   return launch_status();
 }
 
+// Tiles charged per (sequence, KV head) unit in the block ranges, for the
+// merge at the unit's end (measured on the 70B-shape continuous batch).
+// PA_BALANCE_UNIT_COST=<n> overrides it (read once), for tuning.
+constexpr int kUnitCostBf16 = 2;
+constexpr int kUnitCostFp8 = 2;
+int unit_cost(bool fp8) {
+  static const int over = [] {
+    const char* v = std::getenv("PA_BALANCE_UNIT_COST");
+    return v && *v ? std::atoi(v) : -1;
+  }();
+  if (over >= 0 && over <= 64) return over;
+  return fp8 ? kUnitCostFp8 : kUnitCostBf16;
+}
+
 // PA_DECODE_MATH=fma selects the CUDA-core ablation of the tile math (kept
 // to measure what the tensor-core form buys); anything else, the default.
 bool fma_ablation() {
@@ -624,9 +662,9 @@ pa_status launch_balanced(const CUtensorMap& mk, const CUtensorMap& mv, const Ba
   if (prm.k_scale) {
     if constexpr (D == 128) {
       if (prm.slot_mapping)
-        return launch_shape<D, kTma, kConsumersFp8, kStages, kBlocksPerSM, true, true, true>(
+        return launch_shape<D, kTma, kConsumersFp8, kStagesFp8, kBlocksPerSM, true, true, true>(
             mk, mv, prm, sms, stream);
-      return launch_shape<D, kTma, kConsumersFp8, kStages, kBlocksPerSM, true, false, true>(
+      return launch_shape<D, kTma, kConsumersFp8, kStagesFp8, kBlocksPerSM, true, false, true>(
           mk, mv, prm, sms, stream);
     } else {
       return PA_ERR_UNSUPPORTED;
@@ -744,6 +782,7 @@ pa_status balanced_entry(const void* q, const void* k_new, const void* v_new,
   prm.num_seqs = num_seqs;
   prm.num_q_heads = num_q_heads;
   prm.group = num_q_heads / num_kv_heads;
+  prm.unit_cost = unit_cost(fp8);
   prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
   prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
   prm.v_new = static_cast<const __nv_bfloat16*>(v_new);

@@ -26,7 +26,13 @@
 // Data structures: a free-block bitmap (lowest id out first); per-block
 // reference counts, use ticks and (node, index) of cached blocks; children
 // keyed by their first block's tokens; a lazily validated min-heap of
-// (tick, block) eviction candidates.
+// (tick, block) eviction candidates; and the number of blocks eviction could
+// free, kept up to date on every reference, cache and eviction change so
+// that a capacity check under pressure costs O(1), not a walk of the tree.
+// Per node: its referenced blocks (nref), the highest index among them
+// (last_ref) and its children whose subtrees hold a referenced block
+// (pinned_children). A node's evictable blocks are then the ones after
+// last_ref, unless a child is pinned (then none).
 
 #include <algorithm>
 #include <cstdint>
@@ -49,6 +55,9 @@ struct Node {
   std::vector<int32_t> tokens;  // block_size tokens per block
   std::vector<int32_t> blocks;
   std::map<std::vector<int32_t>, std::unique_ptr<Node>> children;  // by first block's tokens
+  int32_t nref = 0;             // blocks of this node a live sequence references
+  int32_t last_ref = -1;        // highest index of such a block (-1: none)
+  int32_t pinned_children = 0;  // children whose subtree holds a referenced block
 };
 
 struct Seq {
@@ -99,6 +108,7 @@ struct pa_prefix_cache {
   std::vector<int32_t> idx_of;     // index of a cached block in its node
   std::vector<int64_t> last_use;   // tick of a cached block
   int32_t cached = 0, used = 0;
+  int64_t evictable = 0;  // blocks repeated eviction could free
   pa::Node root;
   std::unordered_map<int64_t, pa::Seq> seqs;
   using Cand = std::pair<int64_t, int32_t>;
@@ -115,35 +125,88 @@ struct pa_prefix_cache {
   void maybe_push(int32_t b) {
     if (evictable_now(b)) heap.push({last_use[b], b});
   }
+  // ---- the evictable count ------------------------------------------------
+  // Blocks repeated eviction could free: cached, unreferenced, with nothing
+  // referenced after them in their node or below it.
+  int64_t node_evictable(const pa::Node& n) const {
+    if (&n == &root || n.pinned_children > 0) return 0;
+    return (int64_t)n.blocks.size() - 1 - n.last_ref;
+  }
+  static bool active(const pa::Node& n) { return n.nref > 0 || n.pinned_children > 0; }
+  // n's subtree went from holding a referenced block (`was`) to active(*n):
+  // tell the ancestors, up to the first whose own state does not change.
+  void propagate(pa::Node* n, bool was) {
+    while (n != &root) {
+      const bool now = active(*n);
+      if (now == was) return;
+      pa::Node* p = n->parent;
+      const bool p_was = active(*p);
+      const int64_t e0 = node_evictable(*p);
+      p->pinned_children += now ? 1 : -1;
+      evictable += node_evictable(*p) - e0;
+      n = p;
+      was = p_was;
+    }
+  }
+  // Cached block b just became referenced (ref 0 -> 1) or unreferenced (1 -> 0).
+  void ref_changed(int32_t b, bool referenced) {
+    pa::Node* n = node_of[b];
+    const bool was = active(*n);
+    const int64_t e0 = node_evictable(*n);
+    const int32_t i = idx_of[b];
+    if (referenced) {
+      ++n->nref;
+      if (i > n->last_ref) n->last_ref = i;
+    } else {
+      --n->nref;
+      if (i == n->last_ref) {
+        int32_t k = i - 1;
+        while (k >= 0 && ref[n->blocks[k]] == 0) --k;
+        n->last_ref = k;
+      }
+    }
+    evictable += node_evictable(*n) - e0;
+    propagate(n, was);
+  }
+  // nref and last_ref of n from its blocks' reference counts.
+  void recount(pa::Node& n) {
+    n.nref = 0;
+    n.last_ref = -1;
+    for (int32_t i = 0; i < (int32_t)n.blocks.size(); ++i)
+      if (ref[n.blocks[i]] > 0) {
+        ++n.nref;
+        n.last_ref = i;
+      }
+  }
+
   void add_ref(int32_t b) {
-    if (ref[b]++ == 0) ++used;
+    if (ref[b]++ == 0) {
+      ++used;
+      if (node_of[b]) ref_changed(b, true);
+    }
   }
   void drop_ref(int32_t b) {
     if (--ref[b] == 0) {
       --used;
-      if (node_of[b]) maybe_push(b); else free_set.insert(b);
+      if (node_of[b]) {
+        ref_changed(b, false);
+        maybe_push(b);
+      } else {
+        free_set.insert(b);
+      }
+    }
+  }
+  // A reference taken back before anything else changed (no heap push: the
+  // block's tick and its candidate entry are as they were).
+  void undo_ref(int32_t b) {
+    if (--ref[b] == 0) {
+      --used;
+      if (node_of[b]) ref_changed(b, false);
     }
   }
 
-  // Blocks repeated eviction could free: cached, unreferenced, with nothing
-  // referenced after them in their node or below it.
-  int64_t evictable_count() const {
-    int64_t count = 0;
-    std::function<bool(const pa::Node&)> visit = [&](const pa::Node& n) -> bool {
-      bool below = false;  // a referenced block after this point
-      for (const auto& kv : n.children) below = visit(*kv.second) || below;
-      for (int i = (int)n.blocks.size() - 1; i >= 0; --i) {
-        if (ref[n.blocks[i]] > 0) below = true;
-        else if (!below) ++count;
-      }
-      return below;
-    };
-    visit(root);
-    return count;
-  }
   bool reserve(int64_t needed) const {
-    if (needed <= (int64_t)free_set.size()) return true;
-    return needed <= (int64_t)free_set.size() + evictable_count();
+    return needed <= (int64_t)free_set.size() + evictable;
   }
 
   void evict_one() {
@@ -155,15 +218,17 @@ struct pa_prefix_cache {
       pa::Node* n = node_of[b];
       node_of[b] = nullptr;
       --cached;
+      --evictable;  // b was the last unreferenced block of an unpinned leaf
       free_set.insert(b);
-      n->blocks.pop_back();
-      n->tokens.resize(n->blocks.size() * bs);
-      if (!n->blocks.empty()) {
+      if (n->blocks.size() > 1) {
+        n->blocks.pop_back();
+        n->tokens.resize(n->blocks.size() * bs);
         maybe_push(n->blocks.back());
       } else {
+        // the node empties: erase it from its parent by its key (it held no
+        // referenced block, so the parent's pinned count does not change)
         pa::Node* parent = n->parent;
-        for (auto it = parent->children.begin(); it != parent->children.end(); ++it)
-          if (it->second.get() == n) { parent->children.erase(it); break; }
+        parent->children.erase(key_at(n->tokens.data()));  // destroys n
         if (parent != &root && parent->children.empty()) maybe_push(parent->blocks.back());
       }
       return;
@@ -216,6 +281,7 @@ struct pa_prefix_cache {
 
   // Split c so that its first j blocks form a new node; returns that node.
   pa::Node* split(pa::Node* c, size_t j) {
+    const int64_t e0 = node_evictable(*c);
     pa::Node* parent = c->parent;
     auto it = parent->children.find(key_at(c->tokens.data()));
     std::unique_ptr<pa::Node> own = std::move(it->second);
@@ -232,6 +298,10 @@ struct pa_prefix_cache {
     for (size_t i = 0; i < c->blocks.size(); ++i) idx_of[c->blocks[i]] = (int32_t)i;
     c->parent = up.get();
     pa::Node* u = up.get();
+    recount(*u);
+    recount(*c);
+    u->pinned_children = active(*c) ? 1 : 0;  // u is as active as c was: the parent is unchanged
+    evictable += node_evictable(*u) + node_evictable(*c) - e0;
     u->children[key_at(c->tokens.data())] = std::move(own);
     it->second = std::move(up);
     return u;
@@ -338,8 +408,7 @@ extern "C" pa_status pa_prefix_admit(pa_prefix_cache* pc, const int32_t* tokens,
   for (int32_t b : matched) pc->add_ref(b);  // references first: no eviction can take them
   const int64_t need = ((int64_t)num_tokens + pc->bs - 1) / pc->bs - (int64_t)matched.size();
   if (!pc->reserve(need)) {
-    for (int32_t b : matched)
-      if (--pc->ref[b] == 0) --pc->used;
+    for (int32_t b : matched) pc->undo_ref(b);
     return PA_ERR_CAPACITY;
   }
   for (int32_t b : matched) pc->last_use[b] = pc->tick;
@@ -509,7 +578,13 @@ extern "C" pa_status pa_prefix_release(pa_prefix_cache* pc, int64_t seq_id,
       pc->last_use[b] = pc->tick;
       ++pc->cached;
     }
+    // the releasing sequence still references every block of the new leaf:
+    // nothing in it is evictable yet, and its parent's subtree is pinned
+    pa::Node* leaf = n.get();
+    pc->recount(*leaf);
     parent->children[pc->key_at(tokens + (size_t)i * bs)] = std::move(n);
+    pc->evictable += pc->node_evictable(*leaf);
+    pc->propagate(leaf, false);
   }
   for (int32_t b : s.blocks) pc->drop_ref(b);
   return PA_OK;
@@ -546,6 +621,12 @@ extern "C" pa_status pa_prefix_tables(pa_prefix_cache* pc, const int64_t* seq_id
     std::fill(row + s.blocks.size(), row + max_blocks, 0);
     context_lens[i] = s.ntok;
   }
+  return PA_OK;
+}
+
+extern "C" pa_status pa_prefix_evictable(const pa_prefix_cache* pc, int32_t* evictable_blocks) {
+  if (!pc || !evictable_blocks) return PA_ERR_INVALID_ARG;
+  *evictable_blocks = (int32_t)pc->evictable;
   return PA_OK;
 }
 

@@ -83,3 +83,14 @@ def test_host_bookkeeping_replays_the_schedule_on_the_native_cache():
     assert sum(len(s["finished"]) for s in cb.schedule) > 0
     ms = bench.host_bookkeeping_ms(cb)
     assert 0.0 < ms < 1e3
+
+
+def test_host_bookkeeping_under_eviction_pressure():
+    # the same schedule with the pool full of cached prefixes: shared system
+    # prompts, finished sequences released into the cache, every fresh block
+    # evicted from it; the lengths still equal the schedule's (checked inside)
+    from paged_kv_cache_45_gb300 import workloads as wl
+    cb = wl.ContinuousBatching(seed=5, batch=48, iterations=12, p_finish=0.1)
+    ms, evicted = bench.host_bookkeeping_ms(cb, pressure=True)
+    assert 0.0 < ms < 1e3
+    assert evicted > 1.0

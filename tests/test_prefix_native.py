@@ -29,6 +29,36 @@ def test_native_matches_the_oracle_call_by_call(num_blocks, block_size, seed):
     assert any(e[0] == "write" and e[5] for e in run_m.log)
 
 
+@pytest.mark.parametrize("num_blocks,block_size,seed,n_prompts", [
+    (48, 4, 21, 12), (96, 2, 22, 16), (160, 8, 23, 24), (64, 1, 24, 10)])
+def test_native_matches_the_oracle_under_eviction_pressure(num_blocks, block_size, seed,
+                                                           n_prompts):
+    # many distinct system prompts in a small pool: the cache fills it and
+    # most admits and writes must evict least recently used prefixes first.
+    # Besides the call-by-call log, the count of blocks eviction could free
+    # (kept incrementally by the native cache) equals the model's walk.
+    model = pc.PrefixCacheModel(num_blocks, block_size)
+    native = b.PrefixCache(num_blocks, block_size)
+    evictions = []
+    evict = model._evict_one
+
+    def counting_evict():
+        evictions.append(1)
+        return evict()
+
+    model._evict_one = counting_evict
+    run_m = TraceRunner(model, num_blocks, block_size, seed, n_prompts=n_prompts)
+    run_n = TraceRunner(native, num_blocks, block_size, seed, n_prompts=n_prompts)
+    for step in range(1200):
+        run_m.step(pc.CapacityError)
+        run_n.step(b.CapacityError)
+        assert run_n.log == run_m.log, f"diverged at step {step}: {run_n.log[-2:]} vs {run_m.log[-2:]}"
+        assert native.evictable() == model._evictable(), f"evictable count at step {step}"
+        run_n.verify_live()
+    assert len(evictions) > 100
+    assert any(e[0] == "admit-full" for e in run_m.log) or len(evictions) > 300
+
+
 def test_append_tokens_equals_one_write_per_sequence():
     bs = 4
     a, c = b.PrefixCache(64, bs), pc.PrefixCacheModel(64, bs)
