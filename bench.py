@@ -49,6 +49,7 @@ if ROOT not in sys.path:
 
 METRIC = "paged-decode KV GB/s (% of GB300 HBM peak) and decode steps/s, 70B-shape batch"
 FALLBACK_HBM_GBS = 6800.0
+TIMED_SECONDS = 1.5   # wall time the repeated timed blocks aim for
 
 
 def parse_args():
@@ -78,6 +79,9 @@ def parse_args():
     ap.add_argument("--split", type=int, default=-1,
                     help="split_tokens for --schedule split (-1: planned; 0: no split)")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--repeats", type=int, default=0,
+                    help="times the K-step block is timed (median reported); 0: enough blocks "
+                         "for about 1.5 s of timed work, 3..200")
     ap.add_argument("--batch", type=int, default=256,
                     help="sequences of the continuous batch (256 is the workload; smaller "
                          "values are for profiling captures)")
@@ -300,6 +304,7 @@ KERNEL_SOURCES = {   # the files whose change invalidates a kernel's recorded DR
     "rowblock_decode_kernel": ("pa_decode_multi.cu", "pa_tile.cuh", "pa_device.cuh",
                                "pa_api.cu"),
     "prefill_tc_kernel": ("pa_prefill_tc.cu", "pa_umma.cuh", "pa_device.cuh"),
+    "prefill_tc_kernel[e4m3]": ("pa_prefill_tc.cu", "pa_umma.cuh", "pa_device.cuh"),
 }
 
 
@@ -340,6 +345,22 @@ def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "paged_kv_cache_45_gb300", "csrc", name)) as fh:
+            h.update(code_of(fh.read()).encode())
+    return h.hexdigest()[:16]
+
+
+def library_source_hash() -> str:
+    """sha256 (16 hex digits) of the library's whole source (csrc and the
+    public header, comments and blank lines removed), so that a recorded bench
+    line can be matched with the code that produced it."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_45_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc)
+                   if f.endswith((".cu", ".cuh", ".h", ".cpp")))
+    files.append(os.path.join(ROOT, "include", "pagedkv.h"))
+    for path in files:
+        with open(path) as fh:
+            h.update(os.path.basename(path).encode())
             h.update(code_of(fh.read()).encode())
     return h.hexdigest()[:16]
 
@@ -401,10 +422,9 @@ def run_gpu(args):
     steps = Steps(args.workload, args.seed + rank, device, args.batch, args.kv_dtype)
     if steps.fp8 and not steps.multi and args.schedule != "balanced":
         raise SystemExit("--kv-dtype fp8 runs the balanced schedule only")
-    if steps.fp8 and (args.workload == "prefill" or
-                      (steps.multi and args.multi_schedule == "balanced")):
+    if steps.fp8 and steps.multi and args.multi_schedule == "balanced":
         raise SystemExit("--kv-dtype fp8 with several query tokens runs the split schedule "
-                         "(--workload spec) only")
+                         "(--workload spec, --workload prefill) only")
     sms = b.num_sms(local)
     if steps.multi:   # -1: the balanced schedule (pa_decode_multi_balanced)
         split = -1 if args.multi_schedule == "balanced" else (args.split if args.split >= 0
@@ -540,26 +560,40 @@ def run_gpu(args):
     idx = [(args.warmup + k) % n for k in range(K)]
     per_step_launches = 1 if fused else \
         (1 if steps.items[0]["dev"].get("k_new") is not None else 0) + 1 + (1 if ws.split_tokens else 0)
+    # The block of K steps is timed several times back to back (each bracketed
+    # by a barrier and a synchronize) and the median block is reported, so
+    # that even a short K spans enough wall time for the clock sampler: the
+    # repeats after the first fill about TIMED_SECONDS.
     t_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
     if sampler:
         sampler.__enter__()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
+    block_s, repeats = [], args.repeats
     t_wall0 = time.perf_counter()
-    t_ev[0].record(stream)
-    for k in range(K):
-        step(steps.items[idx[k]]["dev"])
-    t_ev[1].record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    while len(block_s) < max(repeats, 1):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_ev[0].record(stream)
+        for k in range(K):
+            step(steps.items[idx[k]]["dev"])
+        t_ev[1].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        block_s.append(t_ev[0].elapsed_time(t_ev[1]) / 1e3)
+        if len(block_s) == 1 and repeats <= 0:   # automatic: from the first block
+            want = min(200, max(3, math.ceil(TIMED_SECONDS / max(block_s[0], 1e-6))))
+            if world > 1:   # every rank runs the same number of blocks
+                w_t = torch.tensor([want], dtype=torch.int64, device=device)
+                dist.all_reduce(w_t, op=dist.ReduceOp.MAX)
+                want = int(w_t.item())
+            repeats = want
     t_wall = time.perf_counter() - t_wall0
     if sampler:
         sampler.__exit__(None, None, None)
     launches = K * per_step_launches
-    total_s = t_ev[0].elapsed_time(t_ev[1]) / 1e3
+    total_s = statistics.median(block_s)
     alg_bytes = sum(steps.items[i]["kv_bytes"] + steps.items[i]["qo_bytes"] for i in idx)
 
     # ------------------ the same K steps replayed from CUDA graphs (one graph
@@ -699,7 +733,8 @@ def run_gpu(args):
               if steps.multi else "paged_decode_kernel")
     if args.workload == "prefill":
         kernel = ("rowblock_decode_kernel" if os.environ.get("PA_PREFILL_KERNEL") == "rowblock"
-                  else "prefill_tc_kernel")
+                  and not steps.fp8 else
+                  "prefill_tc_kernel" + ("[e4m3]" if steps.fp8 else ""))
     traffic = traffic_per_launch(kernel, kv_tokens_per_launch)
     clocks = sampler.summary() if sampler else None
     prefill = args.workload == "prefill"
@@ -767,22 +802,33 @@ def run_gpu(args):
                         "back to pinned memory; double-buffered on three streams so the copies "
                         "of neighbouring steps overlap each step's kernels"},
         "gpu_launches": launches,
+        "source_sha16": library_source_hash(),
+        "timed_blocks": {"blocks": len(block_s), "ms_per_step_min": round(min(block_s) / K * 1e3, 5),
+                         "ms_per_step_median": round(total_s / K * 1e3, 5),
+                         "ms_per_step_max": round(max(block_s) / K * 1e3, 5),
+                         "note": "the K-step block timed back to back this many times; value and "
+                                 "ms_per_step are the median block's; gpu_launches counts one "
+                                 "block"},
         "wall_s_timed_region": round(t_wall, 4),
-        "timing": "CUDA events bracketing the K steps on the launching stream, "
-                  "barrier + synchronize on both sides",
+        "timing": "CUDA events bracketing each block of K steps on the launching stream, "
+                  "barrier + synchronize on both sides; the median block is reported",
     }
     if prefill:
         line["roofline"] = {
             "bound": "tensor", "kernel": kernel, "achieved": round(kern_tflops, 2),
             "peak": tpeak, "unit": "TFLOP/s", "frac": round(kern_tflops / tpeak, 4),
-            "peak_kind": f"{tkind} bf16_tflops (cuBLAS burst)",
+            "peak_kind": f"{tkind} bf16_tflops (cuBLAS burst)" +
+                         ("; the e4m3 pool's MMAs run f16, whose dense rate is bf16's"
+                          if steps.fp8 else ""),
             "traffic": None if traffic is None else int(traffic),
             "algorithmic_flops_per_launch": int(flops),
             "measured": f"CUDA events around each decode launch, {KI} steps"}
         line["kv_gbs"] = round(gbs, 2)
         line["e2e"]["value"] = round(flops * E / e2e_s / 1e12, 2)
         line["e2e"]["unit"] = "TFLOP/s"
-        line["config"]["l2"] = "inputs larger than L2: 268 MB of K/V read every step"
+        line["config"]["l2"] = ("inputs larger than L2: 134 MB of e4m3 K/V read every step"
+                                if steps.fp8 else
+                                "inputs larger than L2: 268 MB of K/V read every step")
         line.pop("pct_of_hbm_peak", None)
         line.pop("pct_of_datasheet_8tbs", None)
     if graph_line is not None:
@@ -1220,6 +1266,7 @@ def run_cow(args):
                 "note": "host prefix cache fork + append (decides the copies), H2D of the "
                         "pairs, copy kernel, host discard; the result stays in the pool"},
         "gpu_launches": K,
+        "source_sha16": library_source_hash(),
         "timing": "CUDA events bracketing the K steps on the launching stream",
     }
     if sampler:

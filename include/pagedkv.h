@@ -387,8 +387,13 @@ pa_status pa_decode_multi_balanced(const void* q, const void* k_cache, const voi
  *              [num_kv_heads], device.
  *   split_tokens  0, or a multiple of 32 (then part_out / part_lse /
  *              row_lens and pa_decode_splitk_reduce as in pa_decode_multi).
- * Supported: head_dim 128 and max_q_len * (num_q_heads / num_kv_heads) <= 64;
- * otherwise PA_ERR_UNSUPPORTED. Other arguments, layouts and errors as
+ * Long chunks (max_q_len * (num_q_heads / num_kv_heads) > 64 rows per KV head,
+ * chunked prefill, [TGI] "Advanced Pattern: Chunked Prefill (TGI v3)") run
+ * on the tcgen05 tensor cores: the e4m3 rows are widened exactly to f16 in
+ * shared memory and the MMAs take f16 q (exact for 2^-14 <= |q| <= 65504)
+ * and f16 weights; unsplit (split_tokens must be 0) and block_size >= 8.
+ * Supported: head_dim 128; otherwise, and for long chunks with a split or
+ * block_size < 8, PA_ERR_UNSUPPORTED. Other arguments, layouts and errors as
  * pa_decode_multi. */
 pa_status pa_decode_multi_fp8(const void* q, const void* k_codes, const void* v_codes,
                               const float* k_scale, const float* v_scale,

@@ -56,20 +56,19 @@ __device__ __forceinline__ void report(unsigned int bits) { atomicOr(&g_balanced
 // SM (16 tiles in flight per SM). Chosen by measurement on the 70B-shape
 // continuous batch over {4 warps x 8 stages x 2 blocks, 8 x 8 x 2}, which
 // reached 71% and 66% of HBM peak against this shape's 93%.
-// With the ring depth a multiple of the consumer count every stage is always
-// read by the same warp, which polls a stage's "full" barrier only after
-// consuming that stage's previous tile, so the barrier is never more than one
-// phase ahead of the parity the warp waits for. (Other depths need one more
-// wait per tile, in the consumer loop.)
+// The ring depth must be a multiple of the consumer count: then every stage
+// is always read by the same warp, which polls a stage's "full" barrier only
+// after consuming that stage's previous tile, so the barrier is never more
+// than one phase ahead of the parity the warp waits for.
 constexpr int kConsumers = 4;
 constexpr int kStages = 4;
 // e4m3 tiles cost twice the math per byte: two consumer warps with two ring
 // stages each overlap a warp's tile math with its next tile's load (measured
 // on the 70B batch: 0.1875 ms per step against 0.2021 with 4 x 1)
 constexpr int kConsumersFp8 = 2;
-// and five ring stages (the most that fit four blocks per SM): 2.5 stages per
-// warp keep more bytes in flight while a warp computes
-constexpr int kStagesFp8 = 5;
+// (five stages, the most that fit four blocks per SM, need one more barrier
+// wait per tile for a stage shared by both warps: 0.1666 against 0.1636 ms)
+constexpr int kStagesFp8 = 4;
 constexpr int kBlocksPerSM = 4;
 constexpr int kMaxBlocksPerSM = kBlocksPerSM;
 
@@ -143,11 +142,7 @@ template <int D, bool kTma, int NC, int STAGES, int BPS, bool kMma, bool kAppend
 __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     balanced_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const BalParams p) {
-  // A stage read by different warps on successive uses (STAGES % NC != 0) is
-  // safe when the warp that reads tile j also read tile j - 2 STAGES: then it
-  // waits for the stage's previous tile to be released before it polls the
-  // stage's "full" barrier (see the consumer loop).
-  static_assert((2 * STAGES) % NC == 0, "tile j - 2 STAGES must belong to tile j's warp");
+  static_assert(STAGES % NC == 0, "each ring stage must belong to one consumer warp");
   static_assert(BPS <= kMaxBlocksPerSM, "workspace is sized for kMaxBlocksPerSM blocks per SM");
   static_assert(!kFp8 || (D == 128 && kMma), "FP8 tiles: head_dim 128, tensor-core math");
   constexpr int EB = kFp8 ? 1 : 2;  // bytes per cache element
@@ -405,19 +400,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
     for (int j = j0 + ((warp - j0) % NC + NC) % NC; j < j0 + m; j += NC) {
       if (__any_sync(0xffffffffu, *abort_flag)) break;
       const int stage = j % STAGES;
-      if constexpr (STAGES % NC != 0) {
-        // The stage's previous tile (j - STAGES) belongs to another warp and
-        // may not have landed yet; "full" must not be polled two phases
-        // ahead, so first wait until that tile was released (its release
-        // implies it landed). Tile j - 2 STAGES was this warp's, so "empty"
-        // is at most one phase behind the parity waited for here.
-        if (j >= STAGES &&
-            !__all_sync(0xffffffffu, mbar_wait(&empty[stage], ((j / STAGES) - 1) & 1))) {
-          if (lane == 0) report(kErrWaitFull);
-          *abort_flag = 1;
-          break;
-        }
-      }
       if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], (j / STAGES) & 1))) {
         if (lane == 0) report(kErrWaitFull);
         *abort_flag = 1;

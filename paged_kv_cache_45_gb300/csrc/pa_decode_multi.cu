@@ -1252,7 +1252,12 @@ extern "C" pa_status pa_decode_multi_fp8(
   if (!q_start || !k_scale || !v_scale) return PA_ERR_INVALID_ARG;
   if (head_dim != 128) return PA_ERR_UNSUPPORTED;  // one 128-byte e4m3 row per token
   const int G = num_q_heads / num_kv_heads;
-  if ((long long)max_q_len * G > kMaxColumnWarps * 8) return PA_ERR_UNSUPPORTED;
+  // more (token, head) rows than the n side holds: the tcgen05 kernel
+  // (block_size >= 8, no context split)
+  const bool long_chunk = (long long)max_q_len * G > kMaxColumnWarps * 8;
+  if (long_chunk && (split_tokens > 0 || !prefill_tc_supported(head_dim, block_size, G)))
+    return PA_ERR_UNSUPPORTED;
+  if ((long long)max_q_len * G > (1LL << 30)) return PA_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
   if (split_tokens > 0) {
     if (split_tokens % kFp8Tile) return PA_ERR_INVALID_ARG;
@@ -1292,6 +1297,14 @@ extern "C" pa_status pa_decode_multi_fp8(
   prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
   prm.k_scale = k_scale;
   prm.v_scale = v_scale;
+  if (long_chunk) {
+    unsigned int* err = multi_error_word();
+    if (!err) return PA_ERR_CUDA;
+    return launch_prefill_tc_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables,
+                                 max_blocks_per_seq, context_lens, q_start, num_seqs, max_q_len,
+                                 num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                 scale, out, err, st);
+  }
   const int nc = (max_q_len * G + 7) / 8;
 
   CUtensorMap mk, mv;

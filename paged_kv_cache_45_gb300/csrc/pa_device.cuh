@@ -176,6 +176,16 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Four e4m3 codes (one u32, low byte first) widened exactly to f16 (every
+// e4m3 value is an f16 value): lo <- codes 0, 1; hi <- codes 2, 3 (the
+// register's 16-bit halves feed the conversions directly).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
+}
+
 // Two floats -> two e4m3 bytes (low byte = lo), round to nearest even,
 // saturating to +-448.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {

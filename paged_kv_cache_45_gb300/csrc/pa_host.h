@@ -74,6 +74,15 @@ pa_status launch_prefill_tc(const void* q, const void* k_cache, const void* v_ca
                             int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
                             int block_size, int num_blocks, float scale, void* out,
                             unsigned int* err, cudaStream_t stream);
+// The same over an e4m3 pool (uint8 codes, per-KV-head fp32 scales on the
+// device); head_dim 128 only.
+pa_status launch_prefill_tc_fp8(const void* q, const void* k_codes, const void* v_codes,
+                                const float* k_scale, const float* v_scale,
+                                const int32_t* block_tables, int max_blocks,
+                                const int32_t* context_lens, const int32_t* q_start, int num_seqs,
+                                int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int num_blocks, float scale, void* out,
+                                unsigned int* err, cudaStream_t stream);
 
 // Reads and clears a translation unit's device error word (synchronous).
 unsigned int take_decode_errors();

@@ -40,6 +40,16 @@
 // of one sequence and head fold its tiles in rotated orders. Keys past a
 // row's own position are masked, and V rows past the block's last position
 // are zeroed before their P.V (they may be unwritten slots).
+//
+// e4m3 pools (head_dim 128): the same block with two more warps. The loader
+// lands each paged block's e4m3 rows (128 bytes a token and head) in a
+// staging ring of two 16 KB slots; warps 10-11 widen every staged tile
+// exactly to f16 (every e4m3 value is an f16 value) into the operand slots,
+// in the layout the bf16 path's TMA writes, zeroing V rows past the block's
+// last position on the way. The MMAs then run kind::f16 on f16 Q (q is
+// converted once: exact for 2^-14 <= |q| <= 65504), f16 K/V and f16 P; the
+// per-head scales go into the score factor (k_scale) and the final division
+// (v_scale).
 
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -60,38 +70,48 @@ constexpr int kTcKeys = 128;                       // keys per K/V tile
 constexpr int kTcPanel = kTcRows * 128;            // Q: one 64-column panel, 16 KB
 constexpr int kKvHalf = 1024;                      // 8 rows of one 64-column panel
 constexpr int kRingBudget = 5 * 32768;             // shared memory of the K/V ring
+constexpr int kTcConvWarps = 2;                    // e4m3: warps widening staged tiles
+constexpr int kStageSlots = 2;                     // e4m3: staging slots ...
+constexpr int kStageBytes = kTcKeys * 128;         // ... of one K or V tile (128 B a key)
 
 // Sizes that follow head_dim (64 or 128): a row is D / 64 panels of 64
 // columns (128 bytes). K/V slots hold 8-row groups of all panels: group g,
 // panel h at g * kKvGroup + h * kKvHalf (each 1 KB = 8 rows of 128 bytes,
 // swizzled), the layout one 4-D TMA box per paged block writes.
-template <int D>
+template <int D, bool kFp8 = false>
 struct TcShape {
   static constexpr int kHalves = D / 64;
   static constexpr int kQBytes = kTcRows * D * 2;     // one Q tile
   static constexpr int kKvBytes = kTcKeys * D * 2;    // one K or V tile: a ring slot
   static constexpr int kKvGroup = kHalves * kKvHalf;
-  static constexpr int kSlots = kRingBudget / kKvBytes;  // 5 at D 128, 10 at D 64
+  // 5 at D 128, 10 at D 64; e4m3 pools: 4 (the staging ring takes the rest)
+  static constexpr int kSlots = kFp8 ? 4 : kRingBudget / kKvBytes;
 };
 constexpr int kTcSoftmaxWarps = 4 * kTcQTiles;
 constexpr int kTcThreads = (2 + kTcSoftmaxWarps) * 32;
 constexpr uint32_t kTcCols = 512;                  // TMEM columns
 constexpr float kRescaleLog2 = 8.0f;               // rescale O when the max grows by > 2^8
 
-template <int D>
+template <bool kFp8>
+constexpr int tc_threads() { return kTcThreads + (kFp8 ? kTcConvWarps * 32 : 0); }
+
+template <int D, bool kFp8 = false>
 struct TcSmem {
-  using S = TcShape<D>;
+  using S = TcShape<D, kFp8>;
   static constexpr int kQ = 0;                                   // Q_0, Q_1
   static constexpr int kRing = kQ + kTcQTiles * S::kQBytes;      // K/V slots
-  static constexpr int kBar = kRing + S::kSlots * S::kKvBytes;
-  // barriers: full[5], empty[5], s_full[2], p_full[2], q_ready, o_final
-  static constexpr int kNumBars = 2 * S::kSlots + 2 * kTcQTiles + 2;
+  static constexpr int kStage = kRing + S::kSlots * S::kKvBytes; // e4m3 staging slots
+  static constexpr int kBar = kStage + (kFp8 ? kStageSlots * kStageBytes : 0);
+  // barriers: full[kSlots], empty[kSlots], s_full[2], p_full[2], q_ready,
+  // o_final; e4m3: st_full[2], st_empty[2]
+  static constexpr int kNumBars = 2 * S::kSlots + 2 * kTcQTiles + 2 + (kFp8 ? 2 * kStageSlots : 0);
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kFlag = kTmemSlot + 8;
   static constexpr int kAlloc = kFlag + 8 + 1024;                // + 1024-byte alignment
 };
 static_assert(TcSmem<128>::kAlloc <= 232448, "over the 227 KB of shared memory per block");
 static_assert(TcSmem<64>::kAlloc <= 232448, "over the 227 KB of shared memory per block");
+static_assert(TcSmem<128, true>::kAlloc <= 232448, "over the 227 KB of shared memory per block");
 
 struct TcParams {
   const __nv_bfloat16* q;       // [R, Hq, D]
@@ -110,6 +130,8 @@ struct TcParams {
   int box_rows;                 // min(block_size, 128)
   int num_blocks;
   float scale_log2;
+  const float* k_scale;         // [Hkv], e4m3 pools only
+  const float* v_scale;
 };
 
 // Waits for the phase of `bar` with the given parity; false once the block
@@ -187,6 +209,30 @@ __device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
       : "f"(a0), "f"(a1));
 }
 
+// (s0, s1) += the two 16-bit halves of `pr` (f16 or bf16, low half to s0),
+// each added to fp32 by one mixed-precision add.
+template <bool kF16>
+__device__ __forceinline__ void add_halves(float& s0, float& s1, uint32_t pr) {
+  if constexpr (kF16)
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.f16 %0, l, %0;\n\tadd.rn.f32.f16 %1, h, %1;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "r"(pr));
+  else
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "r"(pr));
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -199,12 +245,13 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
 __device__ __forceinline__ int k_seq(int i) { return 2 * i; }
 __device__ __forceinline__ int v_seq(int i) { return 2 * i + 1; }
 
-template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int D, bool kFp8>
+__global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const TcParams p) {
-  using Sh = TcShape<D>;
-  using L = TcSmem<D>;
+  static_assert(!kFp8 || D == 128, "e4m3 pools: one 128-byte row per token and head");
+  using Sh = TcShape<D, kFp8>;
+  using L = TcSmem<D, kFp8>;
   constexpr int kSlots = Sh::kSlots;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -245,7 +292,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int quarter = warp & 3;                 // TMEM lanes 32 * quarter ..
   const int r = quarter * 32 + lane;            // row within the Q tile
   const int R = qt * kTcRows + r;               // row within the block
-  const bool row_valid = sw >= 0 && R / G < tok_hi - tok_lo;
+  const bool row_valid = sw >= 0 && sw < kTcSoftmaxWarps && R / G < tok_hi - tok_lo;
   const int tok = tok_lo + R / G;
   const int pos = row_valid ? pos_base + tok : -1;
   const size_t out_off =
@@ -265,15 +312,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* p_full = s_full + kTcQTiles;
   uint64_t* q_ready = p_full + kTcQTiles;
   uint64_t* o_final = q_ready + 1;
+  uint64_t* st_full = o_final + 1;      // e4m3 staging: TMA landed
+  uint64_t* st_empty = st_full + kStageSlots;  // e4m3 staging: widened
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kFlag);
   const uint32_t sQ = smem_u32(smem + L::kQ);
   const uint32_t ring = smem_u32(smem + L::kRing);
+  const uint32_t stage = smem_u32(smem + L::kStage);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], kFp8 ? kTcConvWarps : 1);  // e4m3: one arrival per converter warp
       mbar_init(&empty[s], 1);
+    }
+    if constexpr (kFp8) {
+      for (int s = 0; s < kStageSlots; ++s) {
+        mbar_init(&st_full[s], 1);
+        mbar_init(&st_empty[s], kTcConvWarps);
+      }
     }
     for (int w = 0; w < kTcQTiles; ++w) {
       mbar_init(&s_full[w], 1);
@@ -307,11 +363,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int n_entries = (pos_last >> p.log2_bs) + 1;      // entries the block reads
     int ent_base = -(1 << 30);
     int ent_val = -1;
+    // e4m3 pools land in the staging ring (widened by the converter warps)
+    constexpr int kDst = kFp8 ? kStageSlots : kSlots;
+    uint64_t* landed_bar = kFp8 ? st_full : full;
+    uint64_t* free_bar = kFp8 ? st_empty : empty;
     int L = 0;
     for (; L < 2 * n_tiles; ++L) {
-      const int slot = L % kSlots;
-      if (L >= kSlots &&
-          !__all_sync(0xffffffffu, wait_or_abort(&empty[slot], ((L / kSlots) - 1) & 1,
+      const int slot = L % kDst;
+      if (L >= kDst &&
+          !__all_sync(0xffffffffu, wait_or_abort(&free_bar[slot], ((L / kDst) - 1) & 1,
                                                  abort_flag))) {
         if (lane == 0) give_up(abort_flag, p.err, kErrWaitEmpty);
         break;
@@ -327,10 +387,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int idx = ent_base + lane;
         ent_val = idx < n_entries ? bt[idx] : -1;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(nbox * rb * D * 2));
+      constexpr int kRowBytes = kFp8 ? 128 : D * 2;  // one key's row of this head
+      if (lane == 0) mbar_arrive_expect_tx(&landed_bar[slot], (uint32_t)(nbox * rb * kRowBytes));
       // one box per lane, issued together: a TMA instruction costs a lane a
       // few hundred cycles, and lanes overlap them
-      const uint32_t dst = ring + slot * Sh::kKvBytes;
+      const uint32_t dst = kFp8 ? stage + slot * kStageBytes : ring + slot * Sh::kKvBytes;
       const int i = lane < nbox ? lane : 0;
       const int key0 = j * kTcKeys + i * rb;
       const int blk = __shfl_sync(0xffffffffu, ent_val, (key0 >> p.log2_bs) - ent_base);
@@ -340,23 +401,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int grp = (blk >= 0 && blk < p.num_blocks)
                             ? (blk * p.block_size + (key0 & (p.block_size - 1))) >> 3
                             : -(rb >> 3);
-        tma_load_4d(dst + (i * rb >> 3) * Sh::kKvGroup, map, 0, 0, Sh::kHalves * kvh, grp,
-                    &full[slot]);
+        // e4m3: 1 KB a group (8 rows of 128 codes), the head's single panel
+        constexpr int kGroupBytes = kFp8 ? 1024 : Sh::kKvGroup;
+        tma_load_4d(dst + (i * rb >> 3) * kGroupBytes, map, 0, 0, (kFp8 ? 1 : Sh::kHalves) * kvh,
+                    grp, &landed_bar[slot]);
       }
     }
     // every copy issued must land before the block ends
     if (lane == 0) {
-      for (int s = 0; s < kSlots; ++s) {
+      for (int s = 0; s < kDst; ++s) {
         if (L <= s) continue;
-        const int last = s + ((L - 1 - s) / kSlots) * kSlots;
-        if (!mbar_wait(&full[s], (last / kSlots) & 1)) atomicOr(p.err, kErrDrain);
+        const int last = s + ((L - 1 - s) / kDst) * kDst;
+        if (!mbar_wait(&landed_bar[s], (last / kDst) & 1)) atomicOr(p.err, kErrDrain);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = umma_idesc_bf16(kTcRows, kTcKeys, false);
-      constexpr uint32_t kIdO = umma_idesc_bf16(kTcRows, D, true);
+      constexpr uint32_t kIdS =
+          kFp8 ? umma_idesc_f16(kTcRows, kTcKeys, false) : umma_idesc_bf16(kTcRows, kTcKeys, false);
+      constexpr uint32_t kIdO =
+          kFp8 ? umma_idesc_f16(kTcRows, D, true) : umma_idesc_bf16(kTcRows, D, true);
       // Descriptors are built once; a k-step or a slot moves only the start
       // address (bits 0-13, address >> 4), so each MMA costs one 64-bit add.
       // (Building them per MMA made the issuing thread, not the tensor pipe,
@@ -423,6 +488,69 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       umma_commit(o_final);  // every MMA issued is done: outputs final, TMEM free to go
       if (!mbar_wait(o_final, 0)) atomicOr(p.err, kErrDrain);
     }
+  } else if (kFp8 && warp >= 2 + kTcSoftmaxWarps) {
+    // ------------------------------------------------------------ e4m3 widening
+    // Staged tile L (K_j or V_j of 128 keys: 16 groups of 8 rows x 128 codes,
+    // 128-byte swizzle) -> f16 operand slot L % kSlots ([group][panel][row],
+    // 64 f16 columns a panel, the same swizzle). A thread takes one 16-byte
+    // chunk (16 codes) at a time and writes its two 16-byte f16 chunks. Task
+    // t covers row 2 (t / 16) + r and chunk 4 (r ^ p) + t % 4, r = t / 4 % 2,
+    // p = t / 8 % 2: each group of 8 threads (one 16-byte access phase) then
+    // reads 8 distinct bank quads and writes 8 distinct ones, where a plain
+    // row-major order had two threads on the same quad in every phase.
+    const int ct = threadIdx.x - (2 + kTcSoftmaxWarps) * 32;
+    bool ok = true;
+    for (int L = 0; ok && L < 2 * n_tiles; ++L) {
+      const int st = L % kStageSlots, slot = L % kSlots;
+      ok = __all_sync(0xffffffffu, wait_or_abort(&st_full[st], (L / kStageSlots) & 1, abort_flag));
+      if (ok && L >= kSlots)  // the MMAs are done with the slot's previous tile
+        ok = __all_sync(0xffffffffu,
+                        wait_or_abort(&empty[slot], ((L / kSlots) - 1) & 1, abort_flag));
+      if (!ok) {
+        if (lane == 0) give_up(abort_flag, p.err, kErrWaitFull);
+        break;
+      }
+      const bool is_v = (L & 1) != 0;
+      const int j = tile_of(L >> 1);
+      const int rb = p.box_rows;
+      const int loaded = min(kTcKeys / rb, (pos_last - j * kTcKeys) / rb + 1) * rb;
+      // V rows past the block's last position become zeros (they may be
+      // unwritten slots); K rows there are masked by every row's limit
+      const int keep = is_v ? min(loaded, pos_last - j * kTcKeys + 1) : loaded;
+      const uint32_t src = stage + st * kStageBytes;
+      const uint32_t dst = ring + slot * Sh::kKvBytes;
+#pragma unroll 4
+      for (int t = ct; t < kTcKeys * 8; t += kTcConvWarps * 32) {
+        const int rp = (t >> 2) & 1;
+        const int row = 2 * (t >> 4) + rp;                       // key row
+        const int c = ((rp ^ ((t >> 3) & 1)) << 2) | (t & 3);    // chunk: codes 16c .. 16c + 15
+        const int g = row >> 3, rr = row & 7;
+        const uint32_t d = dst + g * Sh::kKvGroup + (c >> 2) * kKvHalf + rr * 128;
+        const uint32_t d0 = d + ((((2 * c) & 7) ^ rr) << 4);
+        const uint32_t d1 = d + ((((2 * c + 1) & 7) ^ rr) << 4);
+        if (row < keep) {
+          const uint4 v = ld_shared_v4(src + g * 1024 + rr * 128 + ((c ^ rr) << 4));
+          uint32_t h[8];
+          e4m3x4_to_f16x2x2(v.x, h[0], h[1]);
+          e4m3x4_to_f16x2x2(v.y, h[2], h[3]);
+          e4m3x4_to_f16x2x2(v.z, h[4], h[5]);
+          e4m3x4_to_f16x2x2(v.w, h[6], h[7]);
+          st_shared_v4(d0, h[0], h[1], h[2], h[3]);
+          st_shared_v4(d1, h[4], h[5], h[6], h[7]);
+        } else if (is_v) {
+          st_shared_v4(d0, 0, 0, 0, 0);
+          st_shared_v4(d1, 0, 0, 0, 0);
+        }
+      }
+      // the f16 writes become visible to the tensor cores, and the staged
+      // codes are read before the loader may overwrite them
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&full[slot]);
+        mbar_arrive(&st_empty[st]);
+      }
+    }
   } else {
     // ------------------------------------------------------------ softmax
     const uint32_t lanes = tmem + ((uint32_t)(quarter * 32) << 16);
@@ -433,14 +561,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const __nv_bfloat16* src = p.q + out_off;
 #pragma unroll 4
       for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = row_valid ? ld_global_nc_v4(src + 8 * c) : make_uint4(0, 0, 0, 0);
+        uint4 v = row_valid ? ld_global_nc_v4(src + 8 * c) : make_uint4(0, 0, 0, 0);
+        if constexpr (kFp8) {  // the f16 MMA takes f16 q
+          v = make_uint4(pack_f16x2(bf16_lo(v.x), bf16_hi(v.x)), pack_f16x2(bf16_lo(v.y), bf16_hi(v.y)),
+                         pack_f16x2(bf16_lo(v.z), bf16_hi(v.z)), pack_f16x2(bf16_lo(v.w), bf16_hi(v.w)));
+        }
         st_shared_v4(my_q + sw_chunk(r, c), v.x, v.y, v.z, v.w);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(q_ready);
     }
-    const float sl2 = p.scale_log2;
+    const float sl2 = kFp8 ? p.scale_log2 * __ldg(p.k_scale + kvh) : p.scale_log2;
     float m_run = -INFINITY;  // running max, log2 units (the one P and O use)
     float l_run = 0.f;        // running row sum of P
     bool ok = true;
@@ -484,10 +616,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float e0 = ex2_approx(x0);
         const float e1 = ex2_approx(x1);
         const int a = (c >> 1) & 3;
-        // the running sum adds the bf16-rounded weights that multiply V
-        const uint32_t pr = pack_bf16x2(e0, e1);
+        // the running sum adds the rounded weights that multiply V (bf16; f16
+        // for e4m3 pools), each half straight from the packed pair by a
+        // mixed-precision add
+        const uint32_t pr = kFp8 ? pack_f16x2(e0, e1) : pack_bf16x2(e0, e1);
         pk[c >> 1] = pr;
-        add2(sum8[2 * a], sum8[2 * a + 1], bf16_lo(pr), bf16_hi(pr));
+        add_halves<kFp8>(sum8[2 * a], sum8[2 * a + 1], pr);
       }
       tmem_st64_sync(t_s, pk);
       const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
@@ -504,7 +638,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tmem_st32_sync(t_o + c, o);
         }
       }
-      if (qt == 0 && tile == n_tiles - 1) {
+      if (!kFp8 && qt == 0 && tile == n_tiles - 1) {  // (e4m3: the converters zero them)
         // the last V tile: zero its rows past the block's last position
         const int first = pos_last - tile * kTcKeys + 1;
         if (first < kTcKeys) {
@@ -533,7 +667,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       give_up(abort_flag, p.err, kErrWaitFull);
     } else {
       tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float inv = l_run > 0.f ? (kFp8 ? __ldg(p.v_scale + kvh) : 1.f) / l_run : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(p.out + out_off);
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
@@ -578,16 +712,61 @@ bool make_tc_map(CUtensorMap* map, const void* base, int hkv, long long rows, in
          CUDA_SUCCESS;
 }
 
-template <int D>
+// The same view of an e4m3 cache [rows, Hkv, 128] (uint8): (128 columns,
+// 8 rows, Hkv panels, 8-row groups), box {128, 8, 1, box_rows / 8}: one box
+// lands box_rows codes rows of one head as [group][row][128 B] 1 KB swizzled
+// atoms. L2 promotion follows the 128-byte row.
+bool make_tc_map_fp8(CUtensorMap* map, const void* base, int hkv, long long rows, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc || rows % 8 != 0 || box_rows % 8 != 0) return false;
+  const cuuint64_t row_bytes = (cuuint64_t)hkv * 128;
+  cuuint64_t dims[4] = {128, 8, (cuuint64_t)hkv, (cuuint64_t)(rows / 8)};
+  cuuint64_t strides[3] = {row_bytes, 128, 8 * row_bytes};
+  cuuint32_t box[4] = {128, 8, 1, (cuuint32_t)(box_rows / 8)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool kFp8 = false>
 pa_status launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const TcParams& prm,
                     long long tiles, int num_kv_heads, int num_seqs, cudaStream_t stream) {
-  using L = TcSmem<D>;
-  const pa_status s = prepare_kernel(reinterpret_cast<const void*>(prefill_tc_kernel<D>),
-                                     kTcThreads, L::kAlloc, nullptr);
+  using L = TcSmem<D, kFp8>;
+  constexpr int kThreads = tc_threads<kFp8>();
+  const pa_status s = prepare_kernel(reinterpret_cast<const void*>(prefill_tc_kernel<D, kFp8>),
+                                     kThreads, L::kAlloc, nullptr);
   if (s != PA_OK) return s;
   const dim3 grid((unsigned)tiles, num_kv_heads, num_seqs);
-  prefill_tc_kernel<D><<<grid, kTcThreads, L::kAlloc, stream>>>(mk, mv, prm);
+  prefill_tc_kernel<D, kFp8><<<grid, kThreads, L::kAlloc, stream>>>(mk, mv, prm);
   return launch_status();
+}
+
+// Parameters shared by the bf16 and e4m3 launches.
+TcParams tc_params(const void* q, const int32_t* block_tables, int max_blocks,
+                   const int32_t* context_lens, const int32_t* q_start, int max_q_len,
+                   int num_q_heads, int num_kv_heads, int block_size, int num_blocks, float scale,
+                   void* out, unsigned int* err) {
+  TcParams prm;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.q_start = q_start;
+  prm.block_tables = block_tables;
+  prm.context_lens = context_lens;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.err = err;
+  prm.max_blocks = max_blocks;
+  prm.num_q_heads = num_q_heads;
+  prm.group = num_q_heads / num_kv_heads;
+  prm.tokens_per_block = kTcQTiles * kTcRows / prm.group;
+  prm.max_q_len = max_q_len;
+  prm.block_size = block_size;
+  prm.log2_bs = ilog2(block_size);
+  prm.box_rows = block_size < kTcKeys ? block_size : kTcKeys;
+  prm.num_blocks = num_blocks;
+  prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  prm.k_scale = nullptr;
+  prm.v_scale = nullptr;
+  return prm;
 }
 
 }  // namespace
@@ -605,23 +784,9 @@ pa_status launch_prefill_tc(const void* q, const void* k_cache, const void* v_ca
                             unsigned int* err, cudaStream_t stream) {
   const int G = num_q_heads / num_kv_heads;
   if (!prefill_tc_supported(head_dim, block_size, G)) return PA_ERR_UNSUPPORTED;
-  TcParams prm;
-  prm.q = static_cast<const __nv_bfloat16*>(q);
-  prm.q_start = q_start;
-  prm.block_tables = block_tables;
-  prm.context_lens = context_lens;
-  prm.out = static_cast<__nv_bfloat16*>(out);
-  prm.err = err;
-  prm.max_blocks = max_blocks;
-  prm.num_q_heads = num_q_heads;
-  prm.group = G;
-  prm.tokens_per_block = kTcQTiles * kTcRows / G;
-  prm.max_q_len = max_q_len;
-  prm.block_size = block_size;
-  prm.log2_bs = ilog2(block_size);
-  prm.box_rows = block_size < kTcKeys ? block_size : kTcKeys;
-  prm.num_blocks = num_blocks;
-  prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  const TcParams prm = tc_params(q, block_tables, max_blocks, context_lens, q_start, max_q_len,
+                                 num_q_heads, num_kv_heads, block_size, num_blocks, scale, out,
+                                 err);
   const long long tiles = ((long long)max_q_len + prm.tokens_per_block - 1) / prm.tokens_per_block;
   if (tiles > 0x7fffffffLL || num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
   CUtensorMap mk, mv;
@@ -638,6 +803,35 @@ pa_status launch_prefill_tc(const void* q, const void* k_cache, const void* v_ca
       !make_tc_map<64>(&mv, v_cache, num_kv_heads, rows, prm.box_rows))
     return PA_ERR_CUDA;
   return launch_tc<64>(mk, mv, prm, tiles, num_kv_heads, num_seqs, stream);
+}
+
+}  // namespace pa
+
+namespace pa {
+
+pa_status launch_prefill_tc_fp8(const void* q, const void* k_codes, const void* v_codes,
+                                const float* k_scale, const float* v_scale,
+                                const int32_t* block_tables, int max_blocks,
+                                const int32_t* context_lens, const int32_t* q_start, int num_seqs,
+                                int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int num_blocks, float scale, void* out,
+                                unsigned int* err, cudaStream_t stream) {
+  const int G = num_q_heads / num_kv_heads;
+  if (head_dim != 128 || !prefill_tc_supported(head_dim, block_size, G)) return PA_ERR_UNSUPPORTED;
+  TcParams prm = tc_params(q, block_tables, max_blocks, context_lens, q_start, max_q_len,
+                           num_q_heads, num_kv_heads, block_size, num_blocks, scale, out, err);
+  prm.k_scale = k_scale;
+  prm.v_scale = v_scale;
+  const long long tiles = ((long long)max_q_len + prm.tokens_per_block - 1) / prm.tokens_per_block;
+  if (tiles > 0x7fffffffLL || num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+  CUtensorMap mk, mv;
+  std::memset(&mk, 0, sizeof(mk));
+  std::memset(&mv, 0, sizeof(mv));
+  const long long rows = (long long)num_blocks * block_size;
+  if (!make_tc_map_fp8(&mk, k_codes, num_kv_heads, rows, prm.box_rows) ||
+      !make_tc_map_fp8(&mv, v_codes, num_kv_heads, rows, prm.box_rows))
+    return PA_ERR_CUDA;
+  return launch_tc<128, true>(mk, mv, prm, tiles, num_kv_heads, num_seqs, stream);
 }
 
 }  // namespace pa

@@ -312,15 +312,8 @@ __device__ __forceinline__ void load_q_frags_fp8(uint32_t (&qf)[D / 16][2],
 constexpr int kFp8Tile = 32;
 
 // A operand (16 tokens x 16 k) of one e4m3 K ldmatrix result: k[i] holds 4
-// codes (dims 4c..4c+3 of the k step) of token r0 (i even) or r0 + 8 (i odd).
-// Both byte pairs of a u32 widened: lo <- bytes 0, 1; hi <- bytes 2, 3 (the
-// register's 16-bit halves feed the conversions directly).
-__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(x));
-}
+// codes (dims 4c..4c+3 of the k step) of token r0 (i even) or r0 + 8 (i odd),
+// widened by e4m3x4_to_f16x2x2.
 __device__ __forceinline__ void fp8_k_operand(const uint32_t (&k)[4], int i0, uint32_t (&a)[4]) {
   e4m3x4_to_f16x2x2(k[i0], a[0], a[2]);
   e4m3x4_to_f16x2x2(k[i0 + 1], a[1], a[3]);

@@ -94,13 +94,15 @@ def test_multi_fp8_argument_checks(cuda_lib):
     ks, vs = f8["k_scale"].cuda(), f8["v_scale"].cuda()
     bt, cl, qs = case.block_tables.cuda(), case.context_lens.cuda(), case.q_start.cuda()
     out = torch.empty_like(q)
-    with pytest.raises(b.PagedKVError) as e:        # 9 tokens x 8 heads > 64 columns
-        b.pa_decode_multi_fp8(q, kd, vd, ks, vs, bt, cl, qs, 9, case.scale, out)
-    assert e.value.status == -2
     S = 4
     po = torch.empty((q.shape[0], 16, S, 128), dtype=torch.float32, device="cuda")
     pl = torch.empty((q.shape[0], 16, S), dtype=torch.float32, device="cuda")
     rl = torch.empty(q.shape[0], dtype=torch.int32, device="cuda")
+    # 9 tokens x 8 heads > 64 columns: a long chunk, which runs unsplit only
+    with pytest.raises(b.PagedKVError) as e:
+        b.pa_decode_multi_fp8(q, kd, vd, ks, vs, bt, cl, qs, 9, case.scale, out, 32, S, po,
+                              pl, rl)
+    assert e.value.status == -2
     with pytest.raises(b.PagedKVError) as e:        # split not a multiple of the 32-token tile
         b.pa_decode_multi_fp8(q, kd, vd, ks, vs, bt, cl, qs, 8, case.scale, out, 16, S, po,
                               pl, rl)
