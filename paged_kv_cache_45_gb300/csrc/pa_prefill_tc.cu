@@ -42,11 +42,11 @@
 // are zeroed before their P.V (they may be unwritten slots).
 //
 // e4m3 pools (head_dim 128): the same block with two more warps. The loader
-// lands each paged block's e4m3 rows (128 bytes a token and head) in a
-// staging ring of two 16 KB slots; warps 10-11 widen every staged tile
-// exactly to f16 (every e4m3 value is an f16 value) into the operand slots,
-// in the layout the bf16 path's TMA writes, zeroing V rows past the block's
-// last position on the way. The MMAs then run kind::f16 on f16 Q (q is
+// lands each paged block's e4m3 rows (128 bytes a token and head) in the
+// upper half of the tile's operand slot; warps 10-11 widen them in place,
+// exactly, to f16 (every e4m3 value is an f16 value) in the layout the bf16
+// path's TMA writes, zeroing V rows past the block's last position on the
+// way. The MMAs then run kind::f16 on f16 Q (q is
 // converted once: exact for 2^-14 <= |q| <= 65504), f16 K/V and f16 P; the
 // per-head scales go into the score factor (k_scale) and the final division
 // (v_scale).
@@ -70,9 +70,19 @@ constexpr int kTcKeys = 128;                       // keys per K/V tile
 constexpr int kTcPanel = kTcRows * 128;            // Q: one 64-column panel, 16 KB
 constexpr int kKvHalf = 1024;                      // 8 rows of one 64-column panel
 constexpr int kRingBudget = 5 * 32768;             // shared memory of the K/V ring
-constexpr int kTcConvWarps = 2;                    // e4m3: warps widening staged tiles
-constexpr int kStageSlots = 2;                     // e4m3: staging slots ...
-constexpr int kStageBytes = kTcKeys * 128;         // ... of one K or V tile (128 B a key)
+constexpr int kTcConvWarps = 2;                    // e4m3: warps widening the codes
+constexpr int kCodeHalf = kTcKeys * 128;           // e4m3: codes land in a slot's upper 16 KB
+
+// e4m3 tiles are widened in place: code group k (8 keys x 128 codes, 1 KB)
+// lands at kCodeHalf + kCodePos(k) KB of its slot, and f16 group g is written
+// at g * 2 KB. Converter warp 0 widens groups 0-3 and 8-11, warp 1 groups 4-7
+// and 12-15, each in that order and reading a group's codes before writing
+// it; kCodePos puts each warp's codes under the f16 groups the same warp
+// writes later (f16 groups 8-11 cover code positions 0-7, 12-15 cover 8-15),
+// so no warp writes over codes the other has yet to read.
+__host__ __device__ constexpr int kCodePos(int k) {
+  return (k >= 4 && k < 8) ? k + 4 : ((k >= 8 && k < 12) ? k - 4 : k);
+}
 
 // Sizes that follow head_dim (64 or 128): a row is D / 64 panels of 64
 // columns (128 bytes). K/V slots hold 8-row groups of all panels: group g,
@@ -84,8 +94,7 @@ struct TcShape {
   static constexpr int kQBytes = kTcRows * D * 2;     // one Q tile
   static constexpr int kKvBytes = kTcKeys * D * 2;    // one K or V tile: a ring slot
   static constexpr int kKvGroup = kHalves * kKvHalf;
-  // 5 at D 128, 10 at D 64; e4m3 pools: 4 (the staging ring takes the rest)
-  static constexpr int kSlots = kFp8 ? 4 : kRingBudget / kKvBytes;
+  static constexpr int kSlots = kRingBudget / kKvBytes;  // 5 at D 128, 10 at D 64
 };
 constexpr int kTcSoftmaxWarps = 4 * kTcQTiles;
 constexpr int kTcThreads = (2 + kTcSoftmaxWarps) * 32;
@@ -95,16 +104,17 @@ constexpr float kRescaleLog2 = 8.0f;               // rescale O when the max gro
 template <bool kFp8>
 constexpr int tc_threads() { return kTcThreads + (kFp8 ? kTcConvWarps * 32 : 0); }
 
+static_assert(kCodeHalf == TcShape<128>::kKvBytes / 2, "e4m3 codes fill a 128-dim slot's upper half");
+
 template <int D, bool kFp8 = false>
 struct TcSmem {
   using S = TcShape<D, kFp8>;
   static constexpr int kQ = 0;                                   // Q_0, Q_1
   static constexpr int kRing = kQ + kTcQTiles * S::kQBytes;      // K/V slots
-  static constexpr int kStage = kRing + S::kSlots * S::kKvBytes; // e4m3 staging slots
-  static constexpr int kBar = kStage + (kFp8 ? kStageSlots * kStageBytes : 0);
+  static constexpr int kBar = kRing + S::kSlots * S::kKvBytes;
   // barriers: full[kSlots], empty[kSlots], s_full[2], p_full[2], q_ready,
-  // o_final; e4m3: st_full[2], st_empty[2]
-  static constexpr int kNumBars = 2 * S::kSlots + 2 * kTcQTiles + 2 + (kFp8 ? 2 * kStageSlots : 0);
+  // o_final; e4m3: landed[kSlots] (the codes are in; full = widened)
+  static constexpr int kNumBars = 2 * S::kSlots + 2 * kTcQTiles + 2 + (kFp8 ? S::kSlots : 0);
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kFlag = kTmemSlot + 8;
   static constexpr int kAlloc = kFlag + 8 + 1024;                // + 1024-byte alignment
@@ -312,13 +322,11 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
   uint64_t* p_full = s_full + kTcQTiles;
   uint64_t* q_ready = p_full + kTcQTiles;
   uint64_t* o_final = q_ready + 1;
-  uint64_t* st_full = o_final + 1;      // e4m3 staging: TMA landed
-  uint64_t* st_empty = st_full + kStageSlots;  // e4m3 staging: widened
+  uint64_t* landed = o_final + 1;       // e4m3: a slot's codes landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kFlag);
   const uint32_t sQ = smem_u32(smem + L::kQ);
   const uint32_t ring = smem_u32(smem + L::kRing);
-  const uint32_t stage = smem_u32(smem + L::kStage);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
@@ -326,10 +334,7 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       mbar_init(&empty[s], 1);
     }
     if constexpr (kFp8) {
-      for (int s = 0; s < kStageSlots; ++s) {
-        mbar_init(&st_full[s], 1);
-        mbar_init(&st_empty[s], kTcConvWarps);
-      }
+      for (int s = 0; s < kSlots; ++s) mbar_init(&landed[s], 1);
     }
     for (int w = 0; w < kTcQTiles; ++w) {
       mbar_init(&s_full[w], 1);
@@ -363,10 +368,11 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     const int n_entries = (pos_last >> p.log2_bs) + 1;      // entries the block reads
     int ent_base = -(1 << 30);
     int ent_val = -1;
-    // e4m3 pools land in the staging ring (widened by the converter warps)
-    constexpr int kDst = kFp8 ? kStageSlots : kSlots;
-    uint64_t* landed_bar = kFp8 ? st_full : full;
-    uint64_t* free_bar = kFp8 ? st_empty : empty;
+    // e4m3 pools: the codes land in the slot's upper half and complete on
+    // `landed` (the converter warps then widen them and arrive on `full`)
+    constexpr int kDst = kSlots;
+    uint64_t* landed_bar = kFp8 ? landed : full;
+    uint64_t* free_bar = empty;
     int L = 0;
     for (; L < 2 * n_tiles; ++L) {
       const int slot = L % kDst;
@@ -391,7 +397,7 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       if (lane == 0) mbar_arrive_expect_tx(&landed_bar[slot], (uint32_t)(nbox * rb * kRowBytes));
       // one box per lane, issued together: a TMA instruction costs a lane a
       // few hundred cycles, and lanes overlap them
-      const uint32_t dst = kFp8 ? stage + slot * kStageBytes : ring + slot * Sh::kKvBytes;
+      const uint32_t dst = ring + slot * Sh::kKvBytes;
       const int i = lane < nbox ? lane : 0;
       const int key0 = j * kTcKeys + i * rb;
       const int blk = __shfl_sync(0xffffffffu, ent_val, (key0 >> p.log2_bs) - ent_base);
@@ -401,10 +407,11 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
         const int grp = (blk >= 0 && blk < p.num_blocks)
                             ? (blk * p.block_size + (key0 & (p.block_size - 1))) >> 3
                             : -(rb >> 3);
-        // e4m3: 1 KB a group (8 rows of 128 codes), the head's single panel
-        constexpr int kGroupBytes = kFp8 ? 1024 : Sh::kKvGroup;
-        tma_load_4d(dst + (i * rb >> 3) * kGroupBytes, map, 0, 0, (kFp8 ? 1 : Sh::kHalves) * kvh,
-                    grp, &landed_bar[slot]);
+        // e4m3: 1 KB a code group (8 rows of 128 codes), placed by kCodePos
+        // (a box holds at most 4 groups, which stay contiguous there)
+        const uint32_t at = kFp8 ? kCodeHalf + kCodePos(i * rb >> 3) * 1024
+                                 : (uint32_t)((i * rb >> 3) * Sh::kKvGroup);
+        tma_load_4d(dst + at, map, 0, 0, (kFp8 ? 1 : Sh::kHalves) * kvh, grp, &landed_bar[slot]);
       }
     }
     // every copy issued must land before the block ends
@@ -490,22 +497,20 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     }
   } else if (kFp8 && warp >= 2 + kTcSoftmaxWarps) {
     // ------------------------------------------------------------ e4m3 widening
-    // Staged tile L (K_j or V_j of 128 keys: 16 groups of 8 rows x 128 codes,
-    // 128-byte swizzle) -> f16 operand slot L % kSlots ([group][panel][row],
-    // 64 f16 columns a panel, the same swizzle). A thread takes one 16-byte
-    // chunk (16 codes) at a time and writes its two 16-byte f16 chunks. Task
-    // t covers row 2 (t / 16) + r and chunk 4 (r ^ p) + t % 4, r = t / 4 % 2,
-    // p = t / 8 % 2: each group of 8 threads (one 16-byte access phase) then
-    // reads 8 distinct bank quads and writes 8 distinct ones, where a plain
-    // row-major order had two threads on the same quad in every phase.
-    const int ct = threadIdx.x - (2 + kTcSoftmaxWarps) * 32;
+    // Tile L (K_j or V_j of 128 keys) of slot L % kSlots, in place: code
+    // group k (8 rows x 128 codes, 128-byte swizzle) at kCodeHalf +
+    // kCodePos(k) KB -> f16 group k at k * 2 KB ([panel][row], 64 f16 columns
+    // a panel, the same swizzle). Warp w takes groups 4w..4w+3, then 8+4w..;
+    // for each group a lane first reads its two 16-byte code chunks, the warp
+    // syncs, then it writes their four 16-byte f16 chunks. Chunk u of lane l
+    // (t = 32 u + l): row 2 (t / 16) + r and chunk 4 (r ^ p) + t % 4, with
+    // r = t / 4 % 2, p = t / 8 % 2, so that each 8-thread access phase reads
+    // and writes 8 distinct bank quads.
+    const int cw = warp - (2 + kTcSoftmaxWarps);  // converter warp 0 or 1
     bool ok = true;
     for (int L = 0; ok && L < 2 * n_tiles; ++L) {
-      const int st = L % kStageSlots, slot = L % kSlots;
-      ok = __all_sync(0xffffffffu, wait_or_abort(&st_full[st], (L / kStageSlots) & 1, abort_flag));
-      if (ok && L >= kSlots)  // the MMAs are done with the slot's previous tile
-        ok = __all_sync(0xffffffffu,
-                        wait_or_abort(&empty[slot], ((L / kSlots) - 1) & 1, abort_flag));
+      const int slot = L % kSlots;
+      ok = __all_sync(0xffffffffu, wait_or_abort(&landed[slot], (L / kSlots) & 1, abort_flag));
       if (!ok) {
         if (lane == 0) give_up(abort_flag, p.err, kErrWaitFull);
         break;
@@ -517,39 +522,41 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       // V rows past the block's last position become zeros (they may be
       // unwritten slots); K rows there are masked by every row's limit
       const int keep = is_v ? min(loaded, pos_last - j * kTcKeys + 1) : loaded;
-      const uint32_t src = stage + st * kStageBytes;
-      const uint32_t dst = ring + slot * Sh::kKvBytes;
-#pragma unroll 4
-      for (int t = ct; t < kTcKeys * 8; t += kTcConvWarps * 32) {
-        const int rp = (t >> 2) & 1;
-        const int row = 2 * (t >> 4) + rp;                       // key row
-        const int c = ((rp ^ ((t >> 3) & 1)) << 2) | (t & 3);    // chunk: codes 16c .. 16c + 15
-        const int g = row >> 3, rr = row & 7;
-        const uint32_t d = dst + g * Sh::kKvGroup + (c >> 2) * kKvHalf + rr * 128;
-        const uint32_t d0 = d + ((((2 * c) & 7) ^ rr) << 4);
-        const uint32_t d1 = d + ((((2 * c + 1) & 7) ^ rr) << 4);
-        if (row < keep) {
-          const uint4 v = ld_shared_v4(src + g * 1024 + rr * 128 + ((c ^ rr) << 4));
+      const uint32_t base = ring + slot * Sh::kKvBytes;
+#pragma unroll 1
+      for (int gi = 0; gi < 8; ++gi) {
+        const int g = (gi & 3) + 4 * cw + (gi & 4) * 2;  // groups 4cw.. then 8 + 4cw..
+        uint4 v[2];
+        int row[2], c[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int t = 32 * u + lane;
+          const int rp = (t >> 2) & 1;
+          row[u] = 2 * (t >> 4) + rp;                       // row within the group
+          c[u] = ((rp ^ ((t >> 3) & 1)) << 2) | (t & 3);    // codes 16c .. 16c + 15
+          v[u] = 8 * g + row[u] < keep
+                     ? ld_shared_v4(base + kCodeHalf + kCodePos(g) * 1024 + row[u] * 128 +
+                                    ((c[u] ^ row[u]) << 4))
+                     : make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();  // the group's codes are read before any of its f16 writes
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (!is_v && 8 * g + row[u] >= keep) continue;  // masked K rows: left as they are
+          const uint32_t d = base + g * Sh::kKvGroup + (c[u] >> 2) * kKvHalf + row[u] * 128;
           uint32_t h[8];
-          e4m3x4_to_f16x2x2(v.x, h[0], h[1]);
-          e4m3x4_to_f16x2x2(v.y, h[2], h[3]);
-          e4m3x4_to_f16x2x2(v.z, h[4], h[5]);
-          e4m3x4_to_f16x2x2(v.w, h[6], h[7]);
-          st_shared_v4(d0, h[0], h[1], h[2], h[3]);
-          st_shared_v4(d1, h[4], h[5], h[6], h[7]);
-        } else if (is_v) {
-          st_shared_v4(d0, 0, 0, 0, 0);
-          st_shared_v4(d1, 0, 0, 0, 0);
+          e4m3x4_to_f16x2x2(v[u].x, h[0], h[1]);
+          e4m3x4_to_f16x2x2(v[u].y, h[2], h[3]);
+          e4m3x4_to_f16x2x2(v[u].z, h[4], h[5]);
+          e4m3x4_to_f16x2x2(v[u].w, h[6], h[7]);
+          st_shared_v4(d + ((((2 * c[u]) & 7) ^ row[u]) << 4), h[0], h[1], h[2], h[3]);
+          st_shared_v4(d + ((((2 * c[u] + 1) & 7) ^ row[u]) << 4), h[4], h[5], h[6], h[7]);
         }
       }
-      // the f16 writes become visible to the tensor cores, and the staged
-      // codes are read before the loader may overwrite them
+      // the f16 writes become visible to the tensor cores
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&full[slot]);
-        mbar_arrive(&st_empty[st]);
-      }
+      if (lane == 0) mbar_arrive(&full[slot]);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -822,6 +829,7 @@ pa_status launch_prefill_tc_fp8(const void* q, const void* k_codes, const void* 
                            num_q_heads, num_kv_heads, block_size, num_blocks, scale, out, err);
   prm.k_scale = k_scale;
   prm.v_scale = v_scale;
+  prm.box_rows = block_size < 32 ? block_size : 32;  // at most 4 code groups a box (kCodePos)
   const long long tiles = ((long long)max_q_len + prm.tokens_per_block - 1) / prm.tokens_per_block;
   if (tiles > 0x7fffffffLL || num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
   CUtensorMap mk, mv;
