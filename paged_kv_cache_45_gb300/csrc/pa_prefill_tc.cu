@@ -76,8 +76,8 @@ constexpr int kCodeHalf = kTcKeys * 128;           // e4m3: codes land in a slot
 // e4m3 tiles are widened in place: code group k (8 keys x 128 codes, 1 KB)
 // lands at kCodeHalf + kCodePos(k) KB of its slot, and f16 group g is written
 // at g * 2 KB. Converter warp 0 widens groups 0-3 and 8-11, warp 1 groups 4-7
-// and 12-15, each in that order and reading a group's codes before writing
-// it; kCodePos puts each warp's codes under the f16 groups the same warp
+// and 12-15, each in batches of four and reading a batch's codes before
+// writing it; kCodePos puts each warp's codes under the f16 groups the same warp
 // writes later (f16 groups 8-11 cover code positions 0-7, 12-15 cover 8-15),
 // so no warp writes over codes the other has yet to read.
 __host__ __device__ constexpr int kCodePos(int k) {
@@ -501,8 +501,8 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     // group k (8 rows x 128 codes, 128-byte swizzle) at kCodeHalf +
     // kCodePos(k) KB -> f16 group k at k * 2 KB ([panel][row], 64 f16 columns
     // a panel, the same swizzle). Warp w takes groups 4w..4w+3, then 8+4w..;
-    // for each group a lane first reads its two 16-byte code chunks, the warp
-    // syncs, then it writes their four 16-byte f16 chunks. Chunk u of lane l
+    // for each four a lane first reads its eight 16-byte code chunks, the
+    // warp syncs, then it writes their 16-byte f16 chunks. Chunk u of lane l
     // (t = 32 u + l): row 2 (t / 16) + r and chunk 4 (r ^ p) + t % 4, with
     // r = t / 4 % 2, p = t / 8 % 2, so that each 8-thread access phase reads
     // and writes 8 distinct bank quads.
@@ -524,34 +524,47 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       const int keep = is_v ? min(loaded, pos_last - j * kTcKeys + 1) : loaded;
       const uint32_t base = ring + slot * Sh::kKvBytes;
 #pragma unroll 1
-      for (int gi = 0; gi < 8; ++gi) {
-        const int g = (gi & 3) + 4 * cw + (gi & 4) * 2;  // groups 4cw.. then 8 + 4cw..
-        uint4 v[2];
+      for (int half = 0; half < 2; ++half) {
+        // four groups at a time: 4cw..4cw+3, then 8+4cw..; all their codes
+        // are read before any of their f16 writes (those of the second four
+        // cover the codes of this warp's eight groups only)
+        uint4 v[4][2];
         int row[2], c[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int t = 32 * u + lane;
           const int rp = (t >> 2) & 1;
-          row[u] = 2 * (t >> 4) + rp;                       // row within the group
+          row[u] = 2 * (t >> 4) + rp;                       // row within a group
           c[u] = ((rp ^ ((t >> 3) & 1)) << 2) | (t & 3);    // codes 16c .. 16c + 15
-          v[u] = 8 * g + row[u] < keep
-                     ? ld_shared_v4(base + kCodeHalf + kCodePos(g) * 1024 + row[u] * 128 +
-                                    ((c[u] ^ row[u]) << 4))
-                     : make_uint4(0u, 0u, 0u, 0u);
         }
-        __syncwarp();  // the group's codes are read before any of its f16 writes
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (!is_v && 8 * g + row[u] >= keep) continue;  // masked K rows: left as they are
-          const uint32_t d = base + g * Sh::kKvGroup + (c[u] >> 2) * kKvHalf + row[u] * 128;
-          uint32_t h[8];
-          e4m3x4_to_f16x2x2(v[u].x, h[0], h[1]);
-          e4m3x4_to_f16x2x2(v[u].y, h[2], h[3]);
-          e4m3x4_to_f16x2x2(v[u].z, h[4], h[5]);
-          e4m3x4_to_f16x2x2(v[u].w, h[6], h[7]);
-          st_shared_v4(d + ((((2 * c[u]) & 7) ^ row[u]) << 4), h[0], h[1], h[2], h[3]);
-          st_shared_v4(d + ((((2 * c[u] + 1) & 7) ^ row[u]) << 4), h[4], h[5], h[6], h[7]);
+        for (int k = 0; k < 4; ++k) {
+          const int g = 4 * cw + 8 * half + k;
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            v[k][u] = 8 * g + row[u] < keep
+                          ? ld_shared_v4(base + kCodeHalf + kCodePos(g) * 1024 + row[u] * 128 +
+                                         ((c[u] ^ row[u]) << 4))
+                          : make_uint4(0u, 0u, 0u, 0u);
         }
+        __syncwarp();  // every code of the four groups is read before their f16 writes
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int g = 4 * cw + 8 * half + k;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            if (!is_v && 8 * g + row[u] >= keep) continue;  // masked K rows: left as they are
+            const uint32_t d = base + g * Sh::kKvGroup + (c[u] >> 2) * kKvHalf + row[u] * 128;
+            uint32_t h[8];
+            e4m3x4_to_f16x2x2(v[k][u].x, h[0], h[1]);
+            e4m3x4_to_f16x2x2(v[k][u].y, h[2], h[3]);
+            e4m3x4_to_f16x2x2(v[k][u].z, h[4], h[5]);
+            e4m3x4_to_f16x2x2(v[k][u].w, h[6], h[7]);
+            st_shared_v4(d + ((((2 * c[u]) & 7) ^ row[u]) << 4), h[0], h[1], h[2], h[3]);
+            st_shared_v4(d + ((((2 * c[u] + 1) & 7) ^ row[u]) << 4), h[4], h[5], h[6], h[7]);
+          }
+        }
+        __syncwarp();
       }
       // the f16 writes become visible to the tensor cores
       fence_proxy_async_smem();
