@@ -76,8 +76,8 @@ constexpr int kCodeHalf = kTcKeys * 128;           // e4m3: codes land in a slot
 // e4m3 tiles are widened in place: code group k (8 keys x 128 codes, 1 KB)
 // lands at kCodeHalf + kCodePos(k) KB of its slot, and f16 group g is written
 // at g * 2 KB. Converter warp 0 widens groups 0-3 and 8-11, warp 1 groups 4-7
-// and 12-15, each in batches of four and reading a batch's codes before
-// writing it; kCodePos puts each warp's codes under the f16 groups the same warp
+// and 12-15, reading all of its eight groups' codes before writing any;
+// kCodePos puts each warp's codes under the f16 groups the same warp
 // writes later (f16 groups 8-11 cover code positions 0-7, 12-15 cover 8-15),
 // so no warp writes over codes the other has yet to read.
 __host__ __device__ constexpr int kCodePos(int k) {
@@ -500,9 +500,9 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     // Tile L (K_j or V_j of 128 keys) of slot L % kSlots, in place: code
     // group k (8 rows x 128 codes, 128-byte swizzle) at kCodeHalf +
     // kCodePos(k) KB -> f16 group k at k * 2 KB ([panel][row], 64 f16 columns
-    // a panel, the same swizzle). Warp w takes groups 4w..4w+3, then 8+4w..;
-    // for each four a lane first reads its eight 16-byte code chunks, the
-    // warp syncs, then it writes their 16-byte f16 chunks. Chunk u of lane l
+    // a panel, the same swizzle). Warp w takes groups 4w..4w+3 and 8+4w..:
+    // a lane first reads its sixteen 16-byte code chunks of the eight groups,
+    // the warp syncs, then it writes their 16-byte f16 chunks. Chunk u of lane l
     // (t = 32 u + l): row 2 (t / 16) + r and chunk 4 (r ^ p) + t % 4, with
     // r = t / 4 % 2, p = t / 8 % 2, so that each 8-thread access phase reads
     // and writes 8 distinct bank quads.
@@ -523,12 +523,10 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       // unwritten slots); K rows there are masked by every row's limit
       const int keep = is_v ? min(loaded, pos_last - j * kTcKeys + 1) : loaded;
       const uint32_t base = ring + slot * Sh::kKvBytes;
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        // four groups at a time: 4cw..4cw+3, then 8+4cw..; all their codes
-        // are read before any of their f16 writes (those of the second four
-        // cover the codes of this warp's eight groups only)
-        uint4 v[4][2];
+      {
+        // all eight of this warp's groups (4cw..4cw+3 and 8+4cw..): every
+        // code is read before any f16 write
+        uint4 v[8][2];
         int row[2], c[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
@@ -538,8 +536,8 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
           c[u] = ((rp ^ ((t >> 3) & 1)) << 2) | (t & 3);    // codes 16c .. 16c + 15
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int g = 4 * cw + 8 * half + k;
+        for (int k = 0; k < 8; ++k) {
+          const int g = 4 * cw + 8 * (k >> 2) + (k & 3);
 #pragma unroll
           for (int u = 0; u < 2; ++u)
             v[k][u] = 8 * g + row[u] < keep
@@ -547,10 +545,10 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
                                          ((c[u] ^ row[u]) << 4))
                           : make_uint4(0u, 0u, 0u, 0u);
         }
-        __syncwarp();  // every code of the four groups is read before their f16 writes
+        __syncwarp();  // every code of the eight groups is read before their f16 writes
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int g = 4 * cw + 8 * half + k;
+        for (int k = 0; k < 8; ++k) {
+          const int g = 4 * cw + 8 * (k >> 2) + (k & 3);
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             if (!is_v && 8 * g + row[u] >= keep) continue;  // masked K rows: left as they are
@@ -564,7 +562,6 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
             st_shared_v4(d + ((((2 * c[u] + 1) & 7) ^ row[u]) << 4), h[4], h[5], h[6], h[7]);
           }
         }
-        __syncwarp();
       }
       // the f16 writes become visible to the tensor cores
       fence_proxy_async_smem();
