@@ -334,9 +334,10 @@ pa_status pa_selftest_wait_timeout(int32_t limit_us, void* stream);
  *              that (long prompt chunks) the rows are tiled, unsplit, each
  *              tile with a causal key range of its own: 256 (token, head)
  *              rows a block on the tcgen05 tensor cores (scores and outputs
- *              in tensor memory) for block_size >= 8, 64
- *              rows a block on warp MMAs otherwise (or when the environment
- *              sets PA_PREFILL_KERNEL=rowblock); split_tokens must then be 0,
+ *              in tensor memory; K/V rows by TMA for block_size >= 8, by
+ *              16-byte cp.async copies below), or, when the environment sets
+ *              PA_PREFILL_KERNEL=rowblock, 64 rows a block on warp MMAs;
+ *              split_tokens must then be 0,
  *              else PA_ERR_UNSUPPORTED. A sequence with more rows than
  *              max_q_len is skipped and sets bit 16 of the device error word
  *              (rejected in validating mode).
@@ -391,9 +392,9 @@ pa_status pa_decode_multi_balanced(const void* q, const void* k_cache, const voi
  * chunked prefill, [TGI] "Advanced Pattern: Chunked Prefill (TGI v3)") run
  * on the tcgen05 tensor cores: the e4m3 rows are widened exactly to f16 in
  * shared memory and the MMAs take f16 q (exact for 2^-14 <= |q| <= 65504)
- * and f16 weights; unsplit (split_tokens must be 0) and block_size >= 8.
- * Supported: head_dim 128; otherwise, and for long chunks with a split or
- * block_size < 8, PA_ERR_UNSUPPORTED. Other arguments, layouts and errors as
+ * and f16 weights; unsplit (split_tokens must be 0).
+ * Supported: head_dim 128; otherwise, and for long chunks with a split,
+ * PA_ERR_UNSUPPORTED. Other arguments, layouts and errors as
  * pa_decode_multi. */
 pa_status pa_decode_multi_fp8(const void* q, const void* k_codes, const void* v_codes,
                               const float* k_scale, const float* v_scale,

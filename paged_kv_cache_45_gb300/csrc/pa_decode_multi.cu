@@ -1253,7 +1253,7 @@ extern "C" pa_status pa_decode_multi_fp8(
   if (head_dim != 128) return PA_ERR_UNSUPPORTED;  // one 128-byte e4m3 row per token
   const int G = num_q_heads / num_kv_heads;
   // more (token, head) rows than the n side holds: the tcgen05 kernel
-  // (block_size >= 8, no context split)
+  // (no context split)
   const bool long_chunk = (long long)max_q_len * G > kMaxColumnWarps * 8;
   if (long_chunk && (split_tokens > 0 || !prefill_tc_supported(head_dim, block_size, G)))
     return PA_ERR_UNSUPPORTED;

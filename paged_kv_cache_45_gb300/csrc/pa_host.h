@@ -64,8 +64,8 @@ pa_status check_decode_args(const void* q, const void* k_cache, const void* v_ca
 pa_status prepare_kernel(const void* func, int threads, int smem_bytes, int* blocks_per_sm);
 
 // Long query chunks on the tcgen05 tensor cores (pa_prefill_tc.cu): supported
-// for head_dim 64 or 128, block_size >= 8 and a query group of at most 256
-// heads. Runs pa_decode_multi's unsplit causal attention with the same
+// for head_dim 64 or 128, any block size (TMA boxes from 8 rows, cp.async
+// copies below) and a query group of at most 256 heads. Runs pa_decode_multi's unsplit causal attention with the same
 // arguments; device errors are ORed into *err.
 bool prefill_tc_supported(int head_dim, int block_size, int group);
 pa_status launch_prefill_tc(const void* q, const void* k_cache, const void* v_cache,

@@ -104,6 +104,19 @@ constexpr float kRescaleLog2 = 8.0f;               // rescale O when the max gro
 template <bool kFp8>
 constexpr int tc_threads() { return kTcThreads + (kFp8 ? kTcConvWarps * 32 : 0); }
 
+// Shared-memory offset, within an operand slot, of 16-byte chunk c of key row
+// `key` of a bf16 K/V tile ([group][panel][row], 128-byte swizzle), or of a
+// code row of an e4m3 tile (the slot's upper half, group k at kCodePos(k)).
+template <int D, bool kFp8>
+__device__ __forceinline__ uint32_t kv_chunk_offset(int key, int c) {
+  const int g = key >> 3, r = key & 7;
+  if constexpr (kFp8)
+    return (uint32_t)(kCodeHalf + kCodePos(g) * 1024 + r * 128 + ((c ^ r) << 4));
+  else
+    return (uint32_t)(g * (D / 64) * kKvHalf + (c >> 3) * kKvHalf + r * 128 +
+                      (((c & 7) ^ r) << 4));
+}
+
 static_assert(kCodeHalf == TcShape<128>::kKvBytes / 2, "e4m3 codes fill a 128-dim slot's upper half");
 
 template <int D, bool kFp8 = false>
@@ -142,6 +155,9 @@ struct TcParams {
   float scale_log2;
   const float* k_scale;         // [Hkv], e4m3 pools only
   const float* v_scale;
+  const void* k_src;            // the caches, for the gather path (block sizes < 8)
+  const void* v_src;
+  int num_kv_heads;
 };
 
 // Waits for the phase of `bar` with the given parity; false once the block
@@ -255,7 +271,10 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
 __device__ __forceinline__ int k_seq(int i) { return 2 * i; }
 __device__ __forceinline__ int v_seq(int i) { return 2 * i + 1; }
 
-template <int D, bool kFp8>
+// kGather: block sizes below 8, where a paged block holds less than one
+// 8-row group of a TMA box: the loader warp gathers the tile's rows with
+// 16-byte cp.async copies into the same slot layout instead.
+template <int D, bool kFp8, bool kGather>
 __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const TcParams p) {
@@ -329,12 +348,15 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
   const uint32_t ring = smem_u32(smem + L::kRing);
 
   if (threadIdx.x == 0) {
+    // the loads complete on `landed` (e4m3) or `full` (bf16): one arrival
+    // with the byte count for a TMA tile, one per loader lane for a gathered one
+    constexpr int kLoadArrivals = kGather ? 32 : 1;
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(&full[s], kFp8 ? kTcConvWarps : 1);  // e4m3: one arrival per converter warp
+      mbar_init(&full[s], kFp8 ? kTcConvWarps : kLoadArrivals);  // e4m3: one per converter
       mbar_init(&empty[s], 1);
     }
     if constexpr (kFp8) {
-      for (int s = 0; s < kSlots; ++s) mbar_init(&landed[s], 1);
+      for (int s = 0; s < kSlots; ++s) mbar_init(&landed[s], kLoadArrivals);
     }
     for (int w = 0; w < kTcQTiles; ++w) {
       mbar_init(&s_full[w], 1);
@@ -358,7 +380,7 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     // ------------------------------------------------------------ loader
     // The whole warp holds 32 consecutive block-table entries (one coalesced
     // read per refill, bt[ent_base + lane]); lane i issues the tile's box i.
-    if (lane == 0) {
+    if (!kGather && lane == 0) {  // (the gather path has no tensor maps)
       prefetch_tensormap(&tmap_k);
       prefetch_tensormap(&tmap_v);
     }
@@ -384,6 +406,32 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       }
       const bool is_v = (L & 1) != 0;  // L = 2 j: K_j, L = 2 j + 1: V_j
       const int j = tile_of(L >> 1);
+      if constexpr (kGather) {
+        // rows j*128 .. pos_last (at most 128) of this head, 16 bytes a copy;
+        // each lane reads its rows' table entries itself (a block holds at
+        // most 4 rows here). Ids outside the pool give zeros. (Reading the
+        // tile's entries once and passing them by shuffles measured slower:
+        // 27.3 against 19.7 ms for the 8 x 2048-token chunk step at block
+        // size 4.)
+        constexpr int kRowBytes = kFp8 ? 128 : D * 2;
+        constexpr int kCpr = kRowBytes / 16;  // 16-byte chunks per row
+        const unsigned char* cache = static_cast<const unsigned char*>(is_v ? p.v_src : p.k_src);
+        const int n_rows = min(kTcKeys, pos_last - j * kTcKeys + 1);
+        const uint32_t dst = ring + (L % kDst) * Sh::kKvBytes;
+        for (int idx = lane; idx < n_rows * kCpr; idx += 32) {
+          const int r = idx / kCpr, c = idx % kCpr;
+          const int key = j * kTcKeys + r;
+          const int blk = __ldg(bt + (key >> p.log2_bs));
+          const bool ok = blk >= 0 && blk < p.num_blocks;
+          const unsigned char* src =
+              ok ? cache + ((size_t)(blk * p.block_size + (key & (p.block_size - 1))) *
+                                p.num_kv_heads + kvh) * kRowBytes + c * 16
+                 : cache;
+          cp_async_16_zfill(dst + kv_chunk_offset<D, kFp8>(r, c), src, ok);
+        }
+        cp_async_arrive_noinc(&landed_bar[L % kDst]);
+        continue;
+      }
       const CUtensorMap* map = is_v ? &tmap_v : &tmap_k;
       const int nbox = min(boxes, (pos_last - j * kTcKeys) / rb + 1);
       const int e_first = (j * kTcKeys) >> p.log2_bs;
@@ -746,17 +794,27 @@ bool make_tc_map_fp8(CUtensorMap* map, const void* base, int hkv, long long rows
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int D, bool kFp8, bool kGather>
+pa_status launch_tc_as(const CUtensorMap& mk, const CUtensorMap& mv, const TcParams& prm,
+                       long long tiles, int num_kv_heads, int num_seqs, cudaStream_t stream) {
+  using L = TcSmem<D, kFp8>;
+  constexpr int kThreads = tc_threads<kFp8>();
+  auto kern = prefill_tc_kernel<D, kFp8, kGather>;
+  const pa_status s =
+      prepare_kernel(reinterpret_cast<const void*>(kern), kThreads, L::kAlloc, nullptr);
+  if (s != PA_OK) return s;
+  const dim3 grid((unsigned)tiles, num_kv_heads, num_seqs);
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(mk, mv, prm);
+  return launch_status();
+}
+
+// TMA boxes for block sizes >= 8, the cp.async gather below.
 template <int D, bool kFp8 = false>
 pa_status launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const TcParams& prm,
                     long long tiles, int num_kv_heads, int num_seqs, cudaStream_t stream) {
-  using L = TcSmem<D, kFp8>;
-  constexpr int kThreads = tc_threads<kFp8>();
-  const pa_status s = prepare_kernel(reinterpret_cast<const void*>(prefill_tc_kernel<D, kFp8>),
-                                     kThreads, L::kAlloc, nullptr);
-  if (s != PA_OK) return s;
-  const dim3 grid((unsigned)tiles, num_kv_heads, num_seqs);
-  prefill_tc_kernel<D, kFp8><<<grid, kThreads, L::kAlloc, stream>>>(mk, mv, prm);
-  return launch_status();
+  if (prm.block_size < 8)
+    return launch_tc_as<D, kFp8, true>(mk, mv, prm, tiles, num_kv_heads, num_seqs, stream);
+  return launch_tc_as<D, kFp8, false>(mk, mv, prm, tiles, num_kv_heads, num_seqs, stream);
 }
 
 // Parameters shared by the bf16 and e4m3 launches.
@@ -783,13 +841,16 @@ TcParams tc_params(const void* q, const int32_t* block_tables, int max_blocks,
   prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
   prm.k_scale = nullptr;
   prm.v_scale = nullptr;
+  prm.k_src = nullptr;
+  prm.v_src = nullptr;
+  prm.num_kv_heads = num_kv_heads;
   return prm;
 }
 
 }  // namespace
 
 bool prefill_tc_supported(int head_dim, int block_size, int group) {
-  return (head_dim == 64 || head_dim == 128) && block_size >= 8 && group >= 1 &&
+  return (head_dim == 64 || head_dim == 128) && block_size >= 1 && group >= 1 &&
          group <= kTcQTiles * kTcRows;
 }
 
@@ -801,15 +862,20 @@ pa_status launch_prefill_tc(const void* q, const void* k_cache, const void* v_ca
                             unsigned int* err, cudaStream_t stream) {
   const int G = num_q_heads / num_kv_heads;
   if (!prefill_tc_supported(head_dim, block_size, G)) return PA_ERR_UNSUPPORTED;
-  const TcParams prm = tc_params(q, block_tables, max_blocks, context_lens, q_start, max_q_len,
-                                 num_q_heads, num_kv_heads, block_size, num_blocks, scale, out,
-                                 err);
+  TcParams prm = tc_params(q, block_tables, max_blocks, context_lens, q_start, max_q_len,
+                           num_q_heads, num_kv_heads, block_size, num_blocks, scale, out, err);
+  prm.k_src = k_cache;
+  prm.v_src = v_cache;
   const long long tiles = ((long long)max_q_len + prm.tokens_per_block - 1) / prm.tokens_per_block;
   if (tiles > 0x7fffffffLL || num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
   CUtensorMap mk, mv;
   std::memset(&mk, 0, sizeof(mk));
   std::memset(&mv, 0, sizeof(mv));
   const long long rows = (long long)num_blocks * block_size;
+  if (block_size < 8) {  // the cp.async gather: no tensor maps
+    return head_dim == 128 ? launch_tc<128>(mk, mv, prm, tiles, num_kv_heads, num_seqs, stream)
+                           : launch_tc<64>(mk, mv, prm, tiles, num_kv_heads, num_seqs, stream);
+  }
   if (head_dim == 128) {
     if (!make_tc_map<128>(&mk, k_cache, num_kv_heads, rows, prm.box_rows) ||
         !make_tc_map<128>(&mv, v_cache, num_kv_heads, rows, prm.box_rows))
@@ -839,6 +905,8 @@ pa_status launch_prefill_tc_fp8(const void* q, const void* k_codes, const void* 
                            num_q_heads, num_kv_heads, block_size, num_blocks, scale, out, err);
   prm.k_scale = k_scale;
   prm.v_scale = v_scale;
+  prm.k_src = k_codes;
+  prm.v_src = v_codes;
   prm.box_rows = block_size < 32 ? block_size : 32;  // at most 4 code groups a box (kCodePos)
   const long long tiles = ((long long)max_q_len + prm.tokens_per_block - 1) / prm.tokens_per_block;
   if (tiles > 0x7fffffffLL || num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
@@ -846,6 +914,8 @@ pa_status launch_prefill_tc_fp8(const void* q, const void* k_codes, const void* 
   std::memset(&mk, 0, sizeof(mk));
   std::memset(&mv, 0, sizeof(mv));
   const long long rows = (long long)num_blocks * block_size;
+  if (block_size < 8)  // the cp.async gather: no tensor maps
+    return launch_tc<128, true>(mk, mv, prm, tiles, num_kv_heads, num_seqs, stream);
   if (!make_tc_map_fp8(&mk, k_codes, num_kv_heads, rows, prm.box_rows) ||
       !make_tc_map_fp8(&mv, v_codes, num_kv_heads, rows, prm.box_rows))
     return PA_ERR_CUDA;

@@ -3,8 +3,9 @@ pa_decode_multi, and on the mma.sync row-block kernel it replaces
 (PA_PREFILL_KERNEL=rowblock), against the fp64 oracle's causal attention.
 
 Covers head_dim 128 and 64, query groups that divide the 256-row block and
-ones that leave padding rows (G = 6), block sizes 8..256 (one TMA box
-per block, or a 128-key tile inside one block), chunks spanning many 128-key
+ones that leave padding rows (G = 6), block sizes 1..256 (rows gathered by
+cp.async below 8, one TMA box per block from 8, a 128-key tile inside one
+block from 128), chunks spanning many 128-key
 tiles with ragged tails, cached prefixes that are not tile multiples, pools
 whose unowned slots are NaN (masked keys and zeroed V rows must keep them
 out), rows before position 0, repeatability, and the chunked-prefill bench
@@ -58,6 +59,9 @@ def run(b, case, context_lens=None):
     (16, 2, 8, [0, 31], [100, 70]),                            # block_size 8
     (16, 2, 128, [0, 200], [160, 300]),                        # one block per 128-key tile
     (16, 2, 256, [100, 0, 600], [200, 90, 40]),                # a tile inside one block
+    (16, 2, 4, [0, 37], [130, 90]),                            # block_size 4 (cp.async rows)
+    (64, 8, 2, [5, 0], [70, 33]),                              # block_size 2
+    (12, 2, 1, [50, 0], [90, 43]),                             # block_size 1, G 6
 ])
 def test_long_chunks_match_oracle(cuda_lib, kernel, hq, hkv, bs, ctx0, qlens):
     case = wl.make_multi_case("tc", 7 + hq + bs + len(ctx0), ctx0, qlens, hq, hkv, 128, bs)
@@ -74,6 +78,7 @@ def test_long_chunks_match_oracle(cuda_lib, kernel, hq, hkv, bs, ctx0, qlens):
     (8, 8, 8, [0, 250], [600, 513]),                           # G 1, block_size 8
     (12, 2, 64, [50, 0], [90, 43]),                            # G 6, padding rows
     (16, 2, 256, [100, 0, 600], [200, 90, 40]),                # a tile inside one block
+    (16, 2, 2, [0, 31], [150, 70]),                            # block_size 2 (cp.async rows)
 ])
 def test_head_dim_64_long_chunks_match_oracle(cuda_lib, kernel, hq, hkv, bs, ctx0, qlens):
     case = wl.make_multi_case("tc64", 11 + hq + bs, ctx0, qlens, hq, hkv, 64, bs)
@@ -146,18 +151,20 @@ def test_rows_above_max_q_len_set_the_shape_bit(cuda_lib, kernel):
     P.assert_close(got[40:], want[40:], f"{kernel} the other sequence")
 
 
-def test_block_ids_outside_the_pool_read_zeros(cuda_lib):
+@pytest.mark.parametrize("bs", [16, 2])
+def test_block_ids_outside_the_pool_read_zeros(cuda_lib, bs):
     # a table entry inside the context that points past the pool: the kernel
-    # reads zero K/V rows there (a TMA box wholly out of range) and faults
-    # nothing; the oracle sees the same once that entry names a zero block
+    # reads zero K/V rows there (a TMA box wholly out of range, or zero-filled
+    # cp.async copies at block size 2) and faults nothing; the oracle sees the
+    # same once that entry names a zero block
     b = cuda_lib
-    case = wl.make_multi_case("tcoob", 17, [100, 40], [300, 90], 16, 2, 128, 16)
+    case = wl.make_multi_case("tcoob", 17, [100, 40], [300, 90], 16, 2, 128, bs)
     nb = case.k_cache.shape[0]
     k, v = case.k_cache.cuda(), case.v_cache.cuda()
     b.pa_kv_append(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), k, v)
     kc, vc = appended(case)
     bt = case.block_tables.clone()
-    bt[0, 3] = nb + 7                            # keys 48..63 of sequence 0
+    bt[0, 3] = nb + 7                            # keys 3 bs .. 4 bs - 1 of sequence 0
     out = b.decode_multi(case.q.cuda(), k, v, bt.cuda(), case.context_lens.cuda(),
                          case.q_start.cuda(), case.max_q_len, case.scale)
     torch.cuda.synchronize()
@@ -178,7 +185,7 @@ def _random_shapes(n):
         hkv = int(rng.choice([1, 2, 4, 8]))
         g = int(rng.integers(1, 9))
         d = int(rng.choice([64, 128]))
-        bs = int(rng.choice([8, 16, 32, 64, 128, 256]))
+        bs = int(rng.choice([1, 2, 4, 8, 16, 32, 64, 128, 256]))
         B = int(rng.integers(1, 5))
         ctx0 = [int(x) for x in rng.integers(0, 900, B)]
         qlens = [int(x) for x in rng.integers(1, 400, B)]

@@ -4,7 +4,8 @@ pa_decode_multi_fp8, against the oracle's causal attention over the
 read-back pool (value(code) * scale of the head).
 
 Covers query groups that divide the 256-row block and one that leaves
-padding rows (G = 6), block sizes 8..256, chunks spanning many 128-key tiles
+padding rows (G = 6), block sizes 1..256 (rows gathered by cp.async below
+8, TMA boxes from 8), chunks spanning many 128-key tiles
 with ragged tails, pools whose unowned slots hold NaN codes (masked keys and
 zeroed V rows must keep them out), rows before position 0, a seeded sweep of
 random shapes, and the chunked-prefill bench step (8 x 2048 new tokens after
@@ -60,6 +61,9 @@ def want(case, f8, kc, vc, context_lens=None):
     (16, 2, 8, [0, 31], [100, 70]),                            # block_size 8
     (16, 2, 128, [0, 200], [160, 300]),                        # one block per 128-key tile
     (16, 2, 256, [100, 0, 600], [200, 90, 40]),                # a tile inside one block
+    (16, 2, 4, [0, 37], [130, 90]),                            # block_size 4 (cp.async rows)
+    (64, 8, 2, [5, 0], [70, 33]),                              # block_size 2
+    (12, 2, 1, [50, 0], [90, 43]),                             # block_size 1, G 6
 ])
 def test_e4m3_long_chunks_match_oracle(cuda_lib, hq, hkv, bs, ctx0, qlens):
     case = wl.make_multi_case("tc8", 31 + hq + bs + len(ctx0), ctx0, qlens, hq, hkv, 128, bs)
@@ -89,17 +93,22 @@ def test_e4m3_repeatable_bit_for_bit(cuda_lib):
     assert torch.equal(a.view(torch.int16), b_.view(torch.int16))
 
 
-def test_e4m3_long_chunks_with_splits_or_small_blocks_are_refused(cuda_lib):
+def test_e4m3_long_chunks_with_splits_are_refused(cuda_lib):
     b = cuda_lib
-    case = wl.make_multi_case("tc8u", 12, [10, 40], [100, 90], 16, 2, 128, 4)
+    case = wl.make_multi_case("tc8u", 12, [10, 40], [100, 90], 16, 2, 128, 16)
     f8, _, _ = pools(case, 6)
     k, v = f8["k_codes"].cuda(), f8["v_codes"].cuda()
     ks, vs = f8["k_scale"].cuda(), f8["v_scale"].cuda()
+    R = int(case.q.shape[0])
     out = torch.zeros_like(case.q).cuda()
-    with pytest.raises(b.PagedKVError) as e:      # block_size 4: no tcgen05 path
+    S = 8
+    po = torch.empty((R, 16, S, 128), dtype=torch.float32, device="cuda")
+    pl = torch.empty((R, 16, S), dtype=torch.float32, device="cuda")
+    rl = torch.empty(R, dtype=torch.int32, device="cuda")
+    with pytest.raises(b.PagedKVError) as e:      # long chunks run unsplit only
         b.pa_decode_multi_fp8(case.q.cuda(), k, v, ks, vs, case.block_tables.cuda(),
                               case.context_lens.cuda(), case.q_start.cuda(), case.max_q_len,
-                              case.scale, out)
+                              case.scale, out, 32, S, po, pl, rl)
     assert e.value.status == -2
 
 
@@ -109,7 +118,7 @@ def _random_shapes(n):
     for i in range(n):
         hkv = int(rng.choice([1, 2, 4, 8]))
         g = int(rng.integers(1, 9))
-        bs = int(rng.choice([8, 16, 32, 64, 128, 256]))
+        bs = int(rng.choice([1, 2, 4, 8, 16, 32, 64, 128, 256]))
         B = int(rng.integers(1, 5))
         ctx0 = [int(x) for x in rng.integers(0, 900, B)]
         qlens = [int(x) for x in rng.integers(1, 400, B)]
