@@ -156,6 +156,7 @@ class Steps:
                                                      case.num_q_heads, case.head_dim)
             self.max_context = int(case.block_tables.shape[1]) * case.block_size
             self.max_q_len = case.max_q_len
+            self.block_size = case.block_size
             self.items.append(dict(fill=None, q=case.q, k_new=case.k_new, v_new=case.v_new,
                                    slots=case.slot_mapping, tables=case.block_tables,
                                    lens=case.context_lens, qstart=case.q_start))
@@ -303,9 +304,26 @@ KERNEL_SOURCES = {   # the files whose change invalidates a kernel's recorded DR
                               "pa_device.cuh", "pa_api.cu"),
     "rowblock_decode_kernel": ("pa_decode_multi.cu", "pa_tile.cuh", "pa_device.cuh",
                                "pa_api.cu"),
-    "prefill_tc_kernel": ("pa_prefill_tc.cu", "pa_umma.cuh", "pa_device.cuh"),
-    "prefill_tc_kernel[e4m3]": ("pa_prefill_tc.cu", "pa_umma.cuh", "pa_device.cuh"),
+    "prefill_tc_kernel": ("pa_prefill_tc.cu", "pa_tc_common.cuh", "pa_umma.cuh",
+                          "pa_device.cuh"),
+    "prefill_tc_kernel[e4m3]": ("pa_prefill_tc.cu", "pa_tc_common.cuh", "pa_umma.cuh",
+                                "pa_device.cuh"),
+    "verify_tc_kernel": ("pa_verify_tc.cu", "pa_tc_common.cuh", "pa_umma.cuh", "pa_device.cuh"),
 }
+
+
+def multi_kernel_name(steps, ws) -> str:
+    """The kernel pa_decode_multi(_fp8) runs for a short-chunk step: the
+    tcgen05 keys-on-M kernel for bf16 caches (head_dim 128, block sizes >= 8,
+    <= 32 (token, head) columns per KV head, splits of 128 tokens), else the
+    column-warp kernel."""
+    if steps.fp8:
+        return "multi_decode_kernel[e4m3]"
+    tc = (steps.d == 128 and steps.block_size >= 8
+          and steps.max_q_len * (steps.hq // steps.hkv) <= 32
+          and ws.split_tokens % 128 == 0
+          and os.environ.get("PA_MULTI_KERNEL") != "columns")
+    return "verify_tc_kernel" if tc else "multi_decode_kernel"
 
 
 class MultiWorkspace:
@@ -729,7 +747,7 @@ def run_gpu(args):
     kv_tokens_per_launch = kv_tokens / KI
     kernel = ("balanced_decode_kernel" + ("[e4m3]" if steps.fp8 else "")) if ws.balanced \
         else (("balanced_multi_kernel" if ws.multi_balanced else
-               "multi_decode_kernel" + ("[e4m3]" if steps.fp8 else ""))
+               multi_kernel_name(steps, ws))
               if steps.multi else "paged_decode_kernel")
     if args.workload == "prefill":
         kernel = ("rowblock_decode_kernel" if os.environ.get("PA_PREFILL_KERNEL") == "rowblock"
@@ -770,8 +788,11 @@ def run_gpu(args):
                    "balanced" if ws.balanced else
                    (("multi, balanced persistent (pa_decode_multi_balanced)"
                      if ws.multi_balanced else
-                     f"multi (one block per KV head, split, sequence; split_tokens="
-                     f"{ws.split_tokens})") if steps.multi else
+                     (f"multi, tcgen05 keys-on-M kernel (persistent, one block per SM, units "
+                      f"of (sequence, split, KV head); split_tokens={ws.split_tokens})"
+                      if multi_kernel_name(steps, ws) == "verify_tc_kernel" else
+                      f"multi (one block per KV head, split, sequence; split_tokens="
+                      f"{ws.split_tokens})")) if steps.multi else
                     f"split (pa_decode split_tokens={ws.split_tokens} + pa_decode_splitk_reduce)"),
                    "step": "fused: pa_append_decode, one launch" if fused else
                    "separate: pa_kv_append + decode launches",

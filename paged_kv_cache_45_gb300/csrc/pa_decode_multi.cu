@@ -1111,6 +1111,20 @@ bool prefill_rowblock_forced() {
   return v && std::strcmp(v, "rowblock") == 0;
 }
 
+// PA_MULTI_KERNEL=columns keeps short chunks over bf16 caches on the
+// column-warp kernel instead of the tcgen05 one (read at every call).
+bool columns_forced() {
+  const char* v = std::getenv("PA_MULTI_KERNEL");
+  return v && std::strcmp(v, "columns") == 0;
+}
+
+// The tcgen05 kernel takes a short-chunk launch (see verify_tc_supported).
+bool use_verify_tc(int head_dim, int block_size, int group, int max_q_len, int split_tokens,
+                   int num_q_rows, int num_q_heads) {
+  return !columns_forced() && (long long)num_q_rows * num_q_heads < (1LL << 31) &&
+         verify_tc_supported(head_dim, block_size, group, max_q_len, split_tokens);
+}
+
 // Device address of this unit's error word (looked up once per device).
 unsigned int* multi_error_word() {
   static std::mutex mu;
@@ -1227,6 +1241,14 @@ extern "C" pa_status pa_decode_multi(const void* q, const void* k_cache, const v
                  : launch_rowblock<128, false>(mk, mv, prm, num_seqs, num_kv_heads, max_rows, st);
     return tma ? launch_rowblock<64, true>(mk, mv, prm, num_seqs, num_kv_heads, max_rows, st)
                : launch_rowblock<64, false>(mk, mv, prm, num_seqs, num_kv_heads, max_rows, st);
+  }
+  if (use_verify_tc(head_dim, block_size, G, max_q_len, split_tokens, num_q_rows, num_q_heads)) {
+    unsigned int* err = multi_error_word();
+    if (!err) return PA_ERR_CUDA;
+    return launch_verify_tc(q, k_cache, v_cache, block_tables,
+                            max_blocks_per_seq, context_lens, q_start, num_seqs, max_q_len,
+                            num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                            split_tokens, max_splits, part_out, part_lse, row_lens, out, err, st);
   }
   if (head_dim == 128)
     return tma ? launch_multi<128, true>(mk, mv, prm, nc, num_seqs, num_kv_heads, st)

@@ -18,6 +18,7 @@ enum : unsigned int {
   kErrDrain = 4u,      // the loader could not confirm its copies had landed
   kErrSelfTest = 8u,   // pa_selftest_wait_timeout's wait ran out, as intended
   kErrShape = 16u,     // a sequence brought more query tokens than the launch was sized for
+  kErrLayout = 32u,    // a block's dynamic shared memory was not 1024-byte aligned
 };
 
 // A wait that runs this long is treated as lost and reported (≈1 s).

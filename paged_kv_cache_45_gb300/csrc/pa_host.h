@@ -84,6 +84,23 @@ pa_status launch_prefill_tc_fp8(const void* q, const void* k_codes, const void* 
                                 int block_size, int num_blocks, float scale, void* out,
                                 unsigned int* err, cudaStream_t stream);
 
+// A few query tokens per sequence on the tcgen05 tensor cores with the keys
+// on the MMA's M side (pa_verify_tc.cu), bf16 caches: head_dim 128, block
+// sizes >= 8, at most 32 (token, head) columns per KV head (max_q_len *
+// group), split_tokens 0 or a multiple of 128, fewer than 2^31 units
+// (sequences * splits * KV heads). Runs pa_decode_multi with the same
+// arguments as a persistent launch (one block per SM); device errors are ORed
+// into *err.
+bool verify_tc_supported(int head_dim, int block_size, int group, int max_q_len,
+                         int split_tokens);
+pa_status launch_verify_tc(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, int max_blocks,
+                           const int32_t* context_lens, const int32_t* q_start, int num_seqs,
+                           int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                           int block_size, int num_blocks, float scale, int split_tokens,
+                           int max_splits, float* part_out, float* part_lse, int32_t* row_lens,
+                           void* out, unsigned int* err, cudaStream_t stream);
+
 // Reads and clears a translation unit's device error word (synchronous).
 unsigned int take_decode_errors();
 unsigned int take_balanced_errors();

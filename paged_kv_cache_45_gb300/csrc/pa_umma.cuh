@@ -50,6 +50,20 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int m, int n, bool b_mn_ma
          ((uint32_t)(m >> 4) << 24);
 }
 
+// Either operand layout, either 16-bit type: f16 selects f16 A and B
+// (formats 0) instead of bf16; a_mn_major sets bit 15 (A read with M
+// contiguous, e.g. V^T from V rows of 64-column panels), b_mn_major bit 16.
+__host__ __device__ constexpr uint32_t umma_idesc_16bit(int m, int n, bool f16, bool a_mn_major,
+                                                        bool b_mn_major) {
+  return (1u << 4) | (f16 ? 0u : (1u << 7) | (1u << 10)) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+static_assert(umma_idesc_16bit(128, 64, false, false, true) == umma_idesc_bf16(128, 64, true),
+              "one encoding for both helpers");
+static_assert(umma_idesc_16bit(128, 64, true, false, true) == umma_idesc_f16(128, 64, true),
+              "one encoding for both helpers");
+
 // D[tmem] (+)= A[smem] * B[smem]^T; issued by one thread.
 __device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                              uint32_t idesc, uint32_t accumulate) {

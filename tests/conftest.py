@@ -21,3 +21,15 @@ def cuda_lib():
         pytest.skip("no CUDA device")
     from paged_kv_cache_45_gb300 import binding
     return binding
+
+
+@pytest.fixture(params=["tcgen05", "columns"])
+def multi_kernel(request, monkeypatch):
+    """Short query chunks on the tcgen05 kernel (keys on M; the default where it
+    applies: head_dim 128, block sizes >= 8, <= 32 columns per KV head, splits
+    of 128 tokens) or on the column-warp kernel (PA_MULTI_KERNEL=columns)."""
+    if request.param == "columns":
+        monkeypatch.setenv("PA_MULTI_KERNEL", "columns")
+    else:
+        monkeypatch.delenv("PA_MULTI_KERNEL", raising=False)
+    return request.param

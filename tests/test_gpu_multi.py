@@ -44,13 +44,14 @@ CTX = [0, 1, 15, 16, 17, 40, 100, 257, 700]
     (1, 8, 1, 128, 16), (4, 8, 1, 128, 16), (8, 64, 8, 128, 16), (3, 8, 2, 128, 16),
     (16, 8, 2, 64, 16), (64, 4, 4, 128, 16), (5, 16, 2, 64, 8), (7, 8, 2, 128, 1),
     (2, 8, 8, 128, 32), (6, 32, 8, 128, 16)])
-def test_multi_matches_oracle(cuda_lib, qlen, hq, hkv, d, bs):
+def test_multi_matches_oracle(cuda_lib, multi_kernel, qlen, hq, hkv, d, bs):
     rng = np.random.default_rng(qlen * 100 + hq + bs)
     qlens = [int(x) for x in rng.integers(1, qlen + 1, len(CTX))]
     qlens[0] = qlen
     case = wl.make_multi_case("mq", 40 + qlen + bs, CTX, qlens, hq, hkv, d, bs)
     out = run_multi(cuda_lib, case)
-    P.assert_close(P.to_f64(out), oracle_multi(case), f"q_len<={qlen} G={hq // hkv} bs={bs}")
+    P.assert_close(P.to_f64(out), oracle_multi(case),
+                   f"{multi_kernel} q_len<={qlen} G={hq // hkv} bs={bs}")
 
 
 @pytest.mark.parametrize("qlen,hq,hkv,d,bs", [
@@ -145,15 +146,15 @@ def test_long_chunks_refuse_context_splits(cuda_lib):
     assert e.value.status == -2
 
 
-@pytest.mark.parametrize("split", [16, 64, 256])
-def test_multi_with_context_splits(cuda_lib, split):
+@pytest.mark.parametrize("split", [16, 64, 128, 256, 1024])
+def test_multi_with_context_splits(cuda_lib, multi_kernel, split):
     case = wl.make_multi_case("mqs", 50 + split, [0, 3, 60, 300, 1000, 33], [4, 2, 8, 1, 8, 5],
                               64, 8, 128, 16)
     out = run_multi(cuda_lib, case, split=split)
-    P.assert_close(P.to_f64(out), oracle_multi(case), f"split {split}")
+    P.assert_close(P.to_f64(out), oracle_multi(case), f"{multi_kernel} split {split}")
 
 
-def test_prompt_fed_chunk_by_chunk_equals_full_causal_attention(cuda_lib):
+def test_prompt_fed_chunk_by_chunk_equals_full_causal_attention(cuda_lib, multi_kernel):
     b = cuda_lib
     n, hq, hkv, d, bs = 96, 16, 2, 128, 16
     full = wl.make_multi_case("chunks", 61, [0], [n], hq, hkv, d, bs)
@@ -178,10 +179,11 @@ def test_prompt_fed_chunk_by_chunk_equals_full_causal_attention(cuda_lib):
     assert a == n
 
 
-@pytest.mark.parametrize("balanced", [False, True], ids=["split", "balanced"])
-def test_speculative_verify_70b_shape_sampled(cuda_lib, balanced):
+@pytest.mark.parametrize("schedule", ["unsplit", "split1024", "balanced"])
+def test_speculative_verify_70b_shape_sampled(cuda_lib, multi_kernel, schedule):
     case = wl.spec_verify_case(seed=0, batch=256, q_len=4)
-    out = P.to_f64(run_multi(cuda_lib, case, split=cuda_lib.BALANCED_MULTI if balanced else 0))
+    split = {"unsplit": 0, "split1024": 1024, "balanced": cuda_lib.BALANCED_MULTI}[schedule]
+    out = P.to_f64(run_multi(cuda_lib, case, split=split))
     sub = [0, 17, 101, 199, 255]
     qs = case.q_start.numpy()
     kc, vc = pa.kv_append(wl.bits(case.k_cache), wl.bits(case.v_cache), wl.bits(case.k_new),
@@ -191,7 +193,7 @@ def test_speculative_verify_70b_shape_sampled(cuda_lib, balanced):
     want = oracle.decode_multi(q_rows, kc, vc, case.block_tables.numpy()[sub],
                                case.context_lens.numpy()[sub], starts, case.scale)
     got = np.concatenate([out[qs[s]:qs[s + 1]] for s in sub])
-    P.assert_close(got, want, "70B spec verify")
+    P.assert_close(got, want, f"70B spec verify, {multi_kernel}, {schedule}")
     assert np.isfinite(out).all()
 
 
@@ -218,7 +220,7 @@ def test_multi_argument_checks(cuda_lib):
     assert e.value.status == -4
 
 
-def test_rows_above_max_q_len_set_the_shape_bit(cuda_lib):
+def test_rows_above_max_q_len_set_the_shape_bit(cuda_lib, multi_kernel):
     b = cuda_lib
     case = wl.make_multi_case("shape", 71, [20, 30], [1, 5], 8, 2, 128, 16)
     q, k, v = case.q.cuda(), case.k_cache.cuda(), case.v_cache.cuda()

@@ -59,7 +59,7 @@ def test_multi_fp8_matches_oracle(cuda_lib, qlen, hq, hkv, bs):
     assert cuda_lib.pa_last_device_error() == 0
 
 
-@pytest.mark.parametrize("split", [32, 256, 1024])
+@pytest.mark.parametrize("split", [32, 128, 256, 1024])
 def test_multi_fp8_with_context_splits(cuda_lib, split):
     case = wl.make_multi_case("mqf8s", 330 + split, [0, 3, 60, 300, 1000, 33],
                               [4, 2, 8, 1, 8, 5], 64, 8, 128, 16)
