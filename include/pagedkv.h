@@ -329,8 +329,15 @@ pa_status pa_selftest_wait_timeout(int32_t limit_us, void* stream);
  *   q_start    int32 [num_seqs + 1], q_start[0] = 0, q_start[num_seqs] =
  *              num_q_rows, non-decreasing.
  *   max_q_len  an upper bound of every n_b. With max_q_len * (num_q_heads /
- *              num_kv_heads) <= 64 (drafted tokens, short chunks) one block
- *              holds a sequence's whole query group for one KV head; above
+ *              num_kv_heads) <= 64 (drafted tokens, short chunks) a
+ *              sequence's whole query group for one KV head is one unit: at
+ *              most 32 (token, head) columns, head_dim 128, block_size >= 8
+ *              and split_tokens 0 or a multiple of 128 run on the tcgen05
+ *              tensor cores (keys on the MMA's M side, a persistent launch
+ *              of one block per SM walking the (sequence, split, KV head)
+ *              units), other short chunks, or all of them when the
+ *              environment sets PA_MULTI_KERNEL=columns, on warp MMAs (one
+ *              block per unit); above
  *              that (long prompt chunks) the rows are tiled, unsplit, each
  *              tile with a causal key range of its own: 256 (token, head)
  *              rows a block on the tcgen05 tensor cores (scores and outputs
