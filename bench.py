@@ -308,7 +308,10 @@ KERNEL_SOURCES = {   # the files whose change invalidates a kernel's recorded DR
                           "pa_device.cuh"),
     "prefill_tc_kernel[e4m3]": ("pa_prefill_tc.cu", "pa_tc_common.cuh", "pa_umma.cuh",
                                 "pa_device.cuh"),
-    "verify_tc_kernel": ("pa_verify_tc.cu", "pa_tc_common.cuh", "pa_umma.cuh", "pa_device.cuh"),
+    "verify_tc_kernel": ("pa_verify_tc.cu", "pa_tc_common.cuh", "pa_umma.cuh", "pa_device.cuh",
+                         "pa_balance.cuh"),
+    "verify_tc_kernel[balanced]": ("pa_verify_tc.cu", "pa_tc_common.cuh", "pa_umma.cuh",
+                                   "pa_device.cuh", "pa_balance.cuh"),
 }
 
 
@@ -323,6 +326,9 @@ def multi_kernel_name(steps, ws) -> str:
           and steps.max_q_len * (steps.hq // steps.hkv) <= 32
           and ws.split_tokens % 128 == 0
           and os.environ.get("PA_MULTI_KERNEL") != "columns")
+    if ws.multi_balanced:
+        return "verify_tc_kernel[balanced]" if tc and steps.batch <= 8192 else \
+            "balanced_multi_kernel"
     return "verify_tc_kernel" if tc else "multi_decode_kernel"
 
 
@@ -746,8 +752,7 @@ def run_gpu(args):
     dec_gbs_rank0 = dec_bytes / dec_s / 1e9
     kv_tokens_per_launch = kv_tokens / KI
     kernel = ("balanced_decode_kernel" + ("[e4m3]" if steps.fp8 else "")) if ws.balanced \
-        else (("balanced_multi_kernel" if ws.multi_balanced else
-               multi_kernel_name(steps, ws))
+        else (multi_kernel_name(steps, ws)
               if steps.multi else "paged_decode_kernel")
     if args.workload == "prefill":
         kernel = ("rowblock_decode_kernel" if os.environ.get("PA_PREFILL_KERNEL") == "rowblock"
@@ -786,7 +791,11 @@ def run_gpu(args):
                                 "tcgen05 blocks (256 (token, head) rows x KV head x sequence, "
                                 "unsplit)") if args.workload == "prefill" else
                    "balanced" if ws.balanced else
-                   (("multi, balanced persistent (pa_decode_multi_balanced)"
+                   ((("multi, balanced persistent (pa_decode_multi_balanced) on the tcgen05 "
+                      "keys-on-M kernel: equal ranges of 128-key tiles, cut units merged in "
+                      "the kernel"
+                      if multi_kernel_name(steps, ws) == "verify_tc_kernel[balanced]" else
+                      "multi, balanced persistent (pa_decode_multi_balanced)")
                      if ws.multi_balanced else
                      (f"multi, tcgen05 keys-on-M kernel (persistent, one block per SM, units "
                       f"of (sequence, split, KV head); split_tokens={ws.split_tokens})"

@@ -1384,6 +1384,16 @@ extern "C" pa_status pa_decode_multi_balanced(
     if (s != PA_OK) return s;
   }
   unsigned char* ws = static_cast<unsigned char*>(workspace);
+  if (!columns_forced() &&
+      verify_tc_balanced_supported(head_dim, block_size, G, max_q_len, num_seqs)) {
+    unsigned int* err = multi_error_word();
+    if (!err) return PA_ERR_CUDA;
+    return launch_verify_tc_balanced(
+        q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, q_start, num_seqs,
+        max_q_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+        reinterpret_cast<int*>(ws + lay.counters), reinterpret_cast<float*>(ws + lay.rec_lse),
+        reinterpret_cast<float*>(ws + lay.rec_o), kMaxCols, out, err, st);
+  }
   BalMultiParams prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.q_start = q_start;

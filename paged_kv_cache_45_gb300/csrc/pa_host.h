@@ -100,6 +100,22 @@ pa_status launch_verify_tc(const void* q, const void* k_cache, const void* v_cac
                            int block_size, int num_blocks, float scale, int split_tokens,
                            int max_splits, float* part_out, float* part_lse, int32_t* row_lens,
                            void* out, unsigned int* err, cudaStream_t stream);
+// The same kernel on pa_decode_multi_balanced's schedule: every block an
+// equal range of the 128-key tiles of all (sequence, KV head) units; a unit
+// cut by ranges leaves records (normalised partial outputs and base-2
+// log-sum-exps, record 2 c + (c is the unit's first block) of block c) that
+// the last block to finish it merges, tickets in counters [B * Hkv * 8]
+// (zero between launches, left zero). Up to 8192 sequences; rec_cols >= 32.
+bool verify_tc_balanced_supported(int head_dim, int block_size, int group, int max_q_len,
+                                  int num_seqs);
+pa_status launch_verify_tc_balanced(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, int max_blocks,
+                                    const int32_t* context_lens, const int32_t* q_start,
+                                    int num_seqs, int max_q_len, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, float scale, int* counters, float* rec_lse,
+                                    float* rec_o, int rec_cols, void* out, unsigned int* err,
+                                    cudaStream_t stream);
 
 // Reads and clears a translation unit's device error word (synchronous).
 unsigned int take_decode_errors();

@@ -60,6 +60,7 @@
 
 #include <cstring>
 
+#include "pa_balance.cuh"
 #include "pa_device.cuh"
 #include "pa_host.h"
 #include "pa_tc_common.cuh"
@@ -70,7 +71,6 @@ namespace pa {
 namespace {
 
 constexpr int kVfCols = 32;            // (token, head) columns of a unit: the MMAs' N
-constexpr int kVfSlots = 6;            // K/V operand slots of 32 KB
 constexpr int kVfSoftmaxWarps = 4;     // warps 2-5
 constexpr int kVfEpiWarps = 4;         // warps 6-9
 constexpr int kVfFirstSoftmax = 2;
@@ -81,10 +81,14 @@ constexpr int kVfPanel = kVfCols * 128;  // Q and P: bytes of one 64-element pan
 constexpr int kVfOpBytes = 2 * kVfPanel; // one Q or P buffer (two panels)
 constexpr uint32_t kVfTmemCols = 4 * kVfCols;  // S^T x 2, O^T x 2
 
+// kBal: the balanced schedule (a range of tiles per block), whose per-block
+// prefix sum over the sequences takes the room of one ring slot.
+template <bool kBal>
 struct VfSmem {
-  static constexpr int kSlotBytes = TcShape<128>::kKvBytes;   // 32 KB
+  static constexpr int kSlots = kBal ? 5 : 6;                 // K/V operand slots of 32 KB
+  static constexpr int kSlotBytes = TcShape<128>::kKvBytes;
   static constexpr int kRing = 0;
-  static constexpr int kQ = kRing + kVfSlots * kSlotBytes;    // 2 x Q: [panel][column][128 B]
+  static constexpr int kQ = kRing + kSlots * kSlotBytes;      // 2 x Q: [panel][column][128 B]
   static constexpr int kP = kQ + 2 * kVfOpBytes;              // 2 x P: [key panel][column][128 B]
   static constexpr int kRed = kP + 2 * kVfOpBytes;            // 2 x [warp][column] fp32 maxima
   static constexpr int kLm = kRed + 2 * kVfSoftmaxWarps * kVfCols * 4;  // 2 x (l [4][32], m [32])
@@ -92,14 +96,20 @@ struct VfSmem {
   static constexpr int kBar = kLm + 2 * kLmFloats * 4;
   // full[S], empty[S], q_ready[2], s_full[2], p_full[2], lm_full[2], o_full[2],
   // o_free[2], pv_done[2], red_full, mma_done
-  static constexpr int kNumBars = 2 * kVfSlots + 14 + 2;
+  static constexpr int kNumBars = 2 * kSlots + 14 + 2;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kFlag = kTmemSlot + 8;
-  static constexpr int kAlloc = kFlag + 8;  // the base must be 1024-byte aligned (checked)
+  static constexpr int kTot = kFlag + 8;                      // balanced: warp totals of the scan
+  static constexpr int kScan = kTot + 48;                     // balanced: S[B + 1]
+  // the base must be 1024-byte aligned (checked)
+  static constexpr int bytes(int B) { return kScan + (kBal ? (B + 1) * 4 : 0); }
 };
-static_assert(VfSmem::kQ % 1024 == 0 && VfSmem::kP % 1024 == 0,
+constexpr int kVfMaxBalSeqs = 8192;  // sequences whose prefix sum fits beside the 5-slot ring
+static_assert(VfSmem<false>::kQ % 1024 == 0 && VfSmem<false>::kP % 1024 == 0 &&
+                  VfSmem<true>::kQ % 1024 == 0 && VfSmem<true>::kP % 1024 == 0,
               "swizzled operands start on 1024-byte boundaries");
-static_assert(VfSmem::kAlloc <= 232448, "over the 227 KB of shared memory per block");
+static_assert(VfSmem<false>::bytes(0) <= 232448 && VfSmem<true>::bytes(kVfMaxBalSeqs) <= 232448,
+              "over the 227 KB of shared memory per block");
 
 struct VfParams {
   const __nv_bfloat16* q;       // [R, Hq, 128]
@@ -124,6 +134,11 @@ struct VfParams {
   int split_tokens;             // 0 or a multiple of 128
   int max_splits;               // 1 when split_tokens is 0
   float scale_log2;
+  // balanced schedule: the records of units cut by block ranges
+  int* counters;                // [B * Hkv * 8] tickets, zero between launches
+  float* rec_lse;               // [blocks][2][rec_cols], base 2
+  float* rec_o;                 // [blocks][2][rec_cols][128]
+  int rec_cols;
 };
 
 // A (sequence, split, KV head) unit of the launch: unit u is sequence
@@ -135,6 +150,10 @@ struct VfUnit {
   int ctx, t_begin, t_end;
   int n_tiles;          // 128-key tiles of [t_begin, t_end); 0: nothing to attend
   bool bad;             // more tokens than the launch was sized for (skipped, reported)
+  // balanced schedule: a segment of the unit (b, kvh), whose first and last
+  // tiles the blocks c0 and c1 own; cut: c0 != c1, partial records merged
+  bool cut;
+  int c0, c1;
 };
 
 __device__ __forceinline__ VfUnit vf_unit(const VfParams& p, int u) {
@@ -160,8 +179,79 @@ __device__ __forceinline__ VfUnit vf_unit(const VfParams& p, int u) {
   w.n_tiles = (w.n > 0 && !w.bad && w.t_begin < w.t_end)
                   ? (w.t_end - w.t_begin + kTcKeys - 1) / kTcKeys
                   : 0;
+  w.cut = false;
+  w.c0 = w.c1 = blockIdx.x;
   return w;
 }
+
+// Sequence b's tiles in the balanced schedule: none for a sequence without
+// query rows or with more than the launch was sized for.
+__device__ __forceinline__ int vf_seq_tiles(const VfParams& p, int b) {
+  const int n = p.q_start[b + 1] - p.q_start[b];
+  if (n <= 0 || n > p.max_q_len || n * p.group > kVfCols) return 0;
+  return tiles_of<kTcKeys>(p.context_lens[b], p.max_blocks << p.log2_bs);
+}
+
+// The block's work items in order. Split mode: units blockIdx.x,
+// blockIdx.x + gridDim.x, ... Balanced mode: the segments of the block's
+// range [c N / W, (c + 1) N / W) of the N 128-key tiles of all (sequence,
+// KV head) units (unit (b, h) holds tiles Hkv S[b] + h n_b ..).
+template <bool kBal>
+struct VfWalk {
+  int u;
+  Cursor cur;
+  long long left, N, W;
+
+  __device__ __forceinline__ void init(const VfParams& p, const int* S) {
+    u = blockIdx.x;
+    left = 0;
+    if constexpr (kBal) {
+      N = (long long)S[p.num_seqs] * p.num_kv_heads;
+      W = min((long long)gridDim.x, N);
+      if ((long long)blockIdx.x < W) {
+        const long long g0 = (long long)blockIdx.x * N / W;
+        left = (long long)(blockIdx.x + 1) * N / W - g0;
+        if (left > 0) cur.seek(g0, S, p.num_seqs, p.num_kv_heads);
+      }
+    }
+  }
+
+  // The next item with tiles, or (split mode, all) the next unit.
+  __device__ __forceinline__ bool next(const VfParams& p, const int* S, VfUnit& w, bool all) {
+    if constexpr (kBal) {
+      if (left <= 0) return false;
+      w.b = cur.b;
+      w.kvh = cur.kvh;
+      w.split = 0;
+      w.row0 = p.q_start[w.b];
+      w.n = p.q_start[w.b + 1] - w.row0;
+      w.nG = w.n * p.group;
+      const int cap = p.max_blocks << p.log2_bs;
+      const int ctx = p.context_lens[w.b];
+      w.ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
+      const int m = (int)min((long long)(cur.n - cur.t), left);
+      w.t_begin = cur.t * kTcKeys;
+      w.t_end = min((cur.t + m) * kTcKeys, w.ctx);
+      w.n_tiles = m;
+      w.bad = false;
+      const long long u0 = (long long)p.num_kv_heads * S[w.b] + (long long)w.kvh * cur.n;
+      w.c0 = owner_of(u0, N, W);
+      w.c1 = owner_of(u0 + cur.n - 1, N, W);
+      w.cut = w.c0 != w.c1;
+      left -= m;
+      if (cur.t + m == cur.n) cur.next_unit(S, p.num_seqs, p.num_kv_heads); else cur.t += m;
+      return true;
+    } else {
+      const int U = p.num_seqs * p.max_splits * p.num_kv_heads;
+      while (u < U) {
+        w = vf_unit(p, u);
+        u += gridDim.x;
+        if (all || w.n_tiles > 0) return true;
+      }
+      return false;
+    }
+  }
+};
 
 __device__ __forceinline__ void st_shared_b16(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"((unsigned short)(v & 0xffffu))
@@ -205,32 +295,41 @@ __device__ __forceinline__ float warp_transpose_reduce(const float (&x)[32], int
 __device__ __forceinline__ void vf_stage_q(const VfParams& p, const VfUnit& w, uint32_t dst,
                                            int t) {
   constexpr int D = 128;
-  for (int idx = t; idx < kVfCols * (D / 8); idx += 128) {
+  constexpr int kPer = kVfCols * (D / 8) / 128;  // 16-byte chunks a thread
+  uint4 v[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {  // every load in flight before the stores
+    const int idx = t + 128 * k;
     const int c = idx >> 4, ch = idx & 15;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    v[k] = make_uint4(0u, 0u, 0u, 0u);
     if (c < w.nG) {
       const int i = c / p.group;
-      v = ld_global_nc_v4(p.q + ((size_t)(w.row0 + i) * p.num_q_heads + w.kvh * p.group +
-                                 (c - i * p.group)) * D + ch * 8);
+      v[k] = ld_global_nc_v4(p.q + ((size_t)(w.row0 + i) * p.num_q_heads + w.kvh * p.group +
+                                    (c - i * p.group)) * D + ch * 8);
     }
-    st_shared_v4(dst + (ch >> 3) * kVfPanel + c * 128 + (((ch & 7) ^ (c & 7)) << 4), v.x, v.y,
-                 v.z, v.w);
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int idx = t + 128 * k;
+    const int c = idx >> 4, ch = idx & 15;
+    st_shared_v4(dst + (ch >> 3) * kVfPanel + c * 128 + (((ch & 7) ^ (c & 7)) << 4), v[k].x,
+                 v[k].y, v[k].z, v[k].w);
   }
 }
 
+template <bool kBal>
 __global__ void __launch_bounds__(kVfThreads, 1)
     verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const VfParams p) {
   constexpr int D = 128;
   constexpr int NC = kVfCols;
-  constexpr int S = kVfSlots;
+  using L = VfSmem<kBal>;
+  constexpr int S = L::kSlots;
   using Sh = TcShape<D>;
-  using L = VfSmem;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.group;
-  const int U = p.num_seqs * p.max_splits * p.num_kv_heads;  // units, round robin over blocks
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrLayout);
     return;
@@ -251,6 +350,7 @@ __global__ void __launch_bounds__(kVfThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kFlag);
   float* red = reinterpret_cast<float*>(smem + L::kRed);
   float* lm = reinterpret_cast<float*>(smem + L::kLm);
+  int* Sc = reinterpret_cast<int*>(smem + L::kScan);  // balanced: tiles before each sequence
   const uint32_t ring = smem_u32(smem + L::kRing);
   const uint32_t sQ = smem_u32(smem + L::kQ);
   const uint32_t sP = smem_u32(smem + L::kP);
@@ -278,6 +378,9 @@ __global__ void __launch_bounds__(kVfThreads, 1)
     tmem_alloc(tmem_slot, kVfTmemCols);
     tmem_relinquish();
   }
+  if constexpr (kBal)  // (ends with the block synchronised)
+    tile_prefix_sum_of<kVfThreads>(Sc, reinterpret_cast<int*>(smem + L::kTot), p.num_seqs,
+                                   [&](int i) { return vf_seq_tiles(p, i); });
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -298,9 +401,10 @@ __global__ void __launch_bounds__(kVfThreads, 1)
     constexpr int kRowBytes = D * 2;  // one key's row of this head
     int Lg = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
-      const VfUnit w = vf_unit(p, u);
-      if (w.n_tiles == 0) continue;
+    VfWalk<kBal> wk;
+    wk.init(p, Sc);
+    VfUnit w;
+    while (ok && wk.next(p, Sc, w, false)) {
       const int32_t* bt = p.block_tables + (size_t)w.b * p.max_blocks;
       const int n_entries = ((w.t_end - 1) >> p.log2_bs) + 1;
       int ent_base = -(1 << 30);
@@ -392,9 +496,10 @@ __global__ void __launch_bounds__(kVfThreads, 1)
       bool ok = true, pending = false;
       Pending pend{0, 0, false, false};
       int jg = 0, ug = 0;
-      for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
-        const VfUnit w = vf_unit(p, u);
-        if (w.n_tiles == 0) continue;
+      VfWalk<kBal> wk;
+      wk.init(p, Sc);
+      VfUnit w;
+      while (ok && wk.next(p, Sc, w, false)) {
         if (!(ok = wait_or_abort(&q_ready[ug & 1], (ug >> 1) & 1, abort_flag))) break;
         const uint64_t qd = d_q + (uint64_t)(ug & 1) * kOpStep;
         for (int j = 0; j < w.n_tiles; ++j, ++jg) {
@@ -437,9 +542,10 @@ __global__ void __launch_bounds__(kVfThreads, 1)
       pb[m] = sP + (key >> 6) * kVfPanel + ((((key & 63) >> 3) ^ m) << 4) + (key & 7) * 2;
     bool ok = true;
     int jg = 0, ug = 0;
-    for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
-      const VfUnit w = vf_unit(p, u);
-      if (w.n_tiles == 0) continue;
+    VfWalk<kBal> wk;
+    wk.init(p, Sc);
+    VfUnit w;
+    while (ok && wk.next(p, Sc, w, false)) {
       const float sl2 = p.scale_log2;
       const int pos0 = w.ctx - w.n;  // column c (token c / G) sees positions <= pos0 + c / G
       const uint32_t t_o = lanes + 2 * NC + (ug & 1) * NC;
@@ -549,34 +655,48 @@ __global__ void __launch_bounds__(kVfThreads, 1)
     if (!ok) give_up(abort_flag, p.err, kErrWaitFull);
   } else if (warp >= kVfFirstEpi) {
     // ------------------------------------------------------------ epilogue
-    // Stages Q of the units two ahead, writes each unit's outputs from its
-    // O^T buffer, and handles the units with nothing to attend (zero rows,
-    // reported shapes) and the per-row context lengths of split mode.
+    // Stages Q of the items two ahead, writes each item's outputs from its
+    // O^T buffer (balanced mode: a cut unit's partial record, merged by the
+    // warp that arrives last on it), and handles the units with nothing to
+    // attend (zero rows, reported shapes) and the per-row context lengths of
+    // split mode.
     const int quad = warp & 3;
     const int dim = quad * 32 + lane;             // O^T row: this thread's head dim
     const int et = (warp - kVfFirstEpi) * 32 + lane;  // 0..127
     const uint32_t lanes = tmem + ((uint32_t)(quad * 32) << 16);
-    int qa = blockIdx.x;  // next unit whose Q is to be staged
-    int qn = 0;           // units with tiles staged so far
+    VfWalk<kBal> qw;  // the next item whose Q is to be staged
+    qw.init(p, Sc);
+    int qn = 0;       // items staged so far
     auto stage_next = [&]() {
-      for (; qa < U; qa += gridDim.x) {
-        const VfUnit w = vf_unit(p, qa);
-        if (w.n_tiles == 0) continue;
-        vf_stage_q(p, w, sQ + (qn & 1) * kVfOpBytes, et);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&q_ready[qn & 1]);
-        ++qn;
-        qa += gridDim.x;
-        return;
-      }
+      VfUnit w;
+      if (!qw.next(p, Sc, w, false)) return;
+      vf_stage_q(p, w, sQ + (qn & 1) * kVfOpBytes, et);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_ready[qn & 1]);
+      ++qn;
     };
     stage_next();
     stage_next();
+    if constexpr (kBal) {
+      // sequences without tiles: zero rows (no context), or reported shapes
+      for (int b = blockIdx.x; b < p.num_seqs; b += gridDim.x) {
+        const int row0 = p.q_start[b], n = p.q_start[b + 1] - row0;
+        if (n <= 0 || Sc[b + 1] != Sc[b]) continue;
+        if (n > p.max_q_len || n * G > NC) {
+          if (et == 0) atomicOr(p.err, kErrShape);
+          continue;
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)row0 * p.num_q_heads * D);
+        for (int i = et; i < n * p.num_q_heads * (D / 8); i += 128) dst[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
     bool ok = true;
     int ug = 0;
-    for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
-      const VfUnit w = vf_unit(p, u);
+    VfWalk<kBal> wk;
+    wk.init(p, Sc);
+    VfUnit w;
+    while (ok && wk.next(p, Sc, w, !kBal)) {
       if (w.n <= 0) continue;
       if (w.bad) {
         if (et == 0 && w.kvh == 0 && w.split == 0) atomicOr(p.err, kErrShape);
@@ -603,13 +723,13 @@ __global__ void __launch_bounds__(kVfThreads, 1)
            __all_sync(0xffffffffu, wait_or_abort(&lm_full[ug & 1], (ug >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      // every S of this unit is done: its Q buffer takes the unit two ahead
+      // every S of this item is done: its Q buffer takes the item two ahead
       stage_next();
       const float* lmb = lm + (ug & 1) * L::kLmFloats;
       const float lsum = (lmb[lane] + lmb[NC + lane]) + (lmb[2 * NC + lane] + lmb[3 * NC + lane]);
       const float m_fin = lmb[kVfSoftmaxWarps * NC + lane];
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      // column `lane`: its output row, and whether this split holds a key of it
+      // column `lane`: its output row, and whether this item holds a key of it
       const int ti = min(lane, w.nG - 1) / G;
       const int pos0 = w.ctx - w.n;
       const int r_lane = (w.row0 + ti) * p.num_q_heads + w.kvh * G + (lane - ti * G);
@@ -622,18 +742,75 @@ __global__ void __launch_bounds__(kVfThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_free[ug & 1]);  // O^T and l/m of buffer ug % 2 read
+      if (kBal && w.cut) {
+        // a unit cut by block ranges: this block's part as a record (the
+        // normalised output and the base-2 log-sum-exp of each column), then
+        // this quarter's ticket; the warp with the last ticket merges the
+        // unit's records for its 32 head dims
+        const int rec = 2 * (int)blockIdx.x + ((int)blockIdx.x == w.c0 ? 1 : 0);
 #pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        const float ic = __shfl_sync(0xffffffffu, inv, c);
-        const int r = __shfl_sync(0xffffffffu, r_lane, c);
-        const bool sc = __shfl_sync(0xffffffffu, seen, c);
-        if (c < w.nG) {
-          if (!sc) {  // no key of this split for the row
-            if (p.split_tokens == 0) p.out[(size_t)r * D + dim] = __float2bfloat16_rn(0.f);
-          } else if (p.split_tokens > 0) {
-            p.part_out[((size_t)r * p.max_splits + w.split) * D + dim] = o[c] * ic;
-          } else {
-            p.out[(size_t)r * D + dim] = __float2bfloat16_rn(o[c] * ic);
+        for (int c = 0; c < NC; ++c) {
+          const float ic = __shfl_sync(0xffffffffu, inv, c);
+          if (c < w.nG) p.rec_o[((size_t)rec * p.rec_cols + c) * D + dim] = o[c] * ic;
+        }
+        if (lane < w.nG)
+          p.rec_lse[rec * p.rec_cols + lane] = seen && lsum > 0.f ? m_fin + log2f(lsum) : -INFINITY;
+        __syncwarp();
+        int* counter = p.counters + ((size_t)w.b * p.num_kv_heads + w.kvh) * 8 + quad;
+        int ticket = 0;
+        if (lane == 0) {
+          fence_acq_rel_gpu();
+          ticket = atomicAdd(counter, 1);
+          fence_acq_rel_gpu();
+        }
+        ticket = __shfl_sync(0xffffffffu, ticket, 0);
+        if (ticket == w.c1 - w.c0) {
+          // lane c: column c's base-2 maximum and weight sum over the parts;
+          // every thread: its head dim of every column, a part at a time
+          float mc = -INFINITY;
+          for (int cc = w.c0; cc <= w.c1; ++cc) {
+            const int rr = 2 * cc + (cc == w.c0 ? 1 : 0);
+            if (lane < w.nG) mc = fmaxf(mc, __ldcg(p.rec_lse + rr * p.rec_cols + lane));
+          }
+          float acc[NC];
+#pragma unroll
+          for (int c = 0; c < NC; ++c) acc[c] = 0.f;
+          float wsum = 0.f;
+          for (int cc = w.c0; cc <= w.c1; ++cc) {
+            const int rr = 2 * cc + (cc == w.c0 ? 1 : 0);
+            const float lk = lane < w.nG ? __ldcg(p.rec_lse + rr * p.rec_cols + lane) : -INFINITY;
+            const float wk = mc == -INFINITY ? 0.f : exp2f(lk - mc);
+            wsum += wk;
+            const float* src = p.rec_o + (size_t)rr * p.rec_cols * D + dim;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+              const float wc = __shfl_sync(0xffffffffu, wk, c);
+              if (c < w.nG) acc[c] += wc * __ldcg(src + (size_t)c * D);
+            }
+          }
+          const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            const float f = __shfl_sync(0xffffffffu, winv, c);
+            const int r = __shfl_sync(0xffffffffu, r_lane, c);
+            if (c < w.nG) p.out[(size_t)r * D + dim] = __float2bfloat16_rn(acc[c] * f);
+          }
+          if (lane == 0) *counter = 0;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const float ic = __shfl_sync(0xffffffffu, inv, c);
+          const int r = __shfl_sync(0xffffffffu, r_lane, c);
+          const bool sc = __shfl_sync(0xffffffffu, seen, c);
+          if (c < w.nG) {
+            if (!sc) {  // no key of this item for the row
+              if (p.split_tokens == 0) p.out[(size_t)r * D + dim] = __float2bfloat16_rn(0.f);
+            } else if (p.split_tokens > 0) {
+              p.part_out[((size_t)r * p.max_splits + w.split) * D + dim] = o[c] * ic;
+            } else {
+              p.out[(size_t)r * D + dim] = __float2bfloat16_rn(o[c] * ic);
+            }
           }
         }
       }
@@ -649,18 +826,22 @@ __global__ void __launch_bounds__(kVfThreads, 1)
   }
 }
 
+template <bool kBal>
 pa_status launch_verify_as(const CUtensorMap& mk, const CUtensorMap& mv, const VfParams& prm,
                            cudaStream_t stream) {
-  const pa_status s = prepare_kernel(reinterpret_cast<const void*>(verify_tc_kernel), kVfThreads,
-                                     VfSmem::kAlloc, nullptr);
+  auto kern = verify_tc_kernel<kBal>;
+  const int smem = VfSmem<kBal>::bytes(prm.num_seqs);
+  const pa_status s =
+      prepare_kernel(reinterpret_cast<const void*>(kern), kVfThreads, smem, nullptr);
   if (s != PA_OK) return s;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return PA_ERR_CUDA;
+  // persistent: one block per SM (split mode: no more blocks than units)
   const long long units = (long long)prm.num_seqs * prm.max_splits * prm.num_kv_heads;
-  const int grid = (int)(units < sms ? units : sms);  // persistent: one block per SM
-  verify_tc_kernel<<<grid, kVfThreads, VfSmem::kAlloc, stream>>>(mk, mv, prm);
+  const int grid = kBal ? sms : (int)(units < sms ? units : sms);
+  kern<<<grid, kVfThreads, smem, stream>>>(mk, mv, prm);
   return launch_status();
 }
 
@@ -673,6 +854,52 @@ bool verify_tc_supported(int head_dim, int block_size, int group, int max_q_len,
          split_tokens % kTcKeys == 0;
 }
 
+bool verify_tc_balanced_supported(int head_dim, int block_size, int group, int max_q_len,
+                                  int num_seqs) {
+  return verify_tc_supported(head_dim, block_size, group, max_q_len, 0) &&
+         num_seqs <= kVfMaxBalSeqs;
+}
+
+namespace {
+
+// Parameters and tensor maps both schedules share.
+pa_status verify_params(VfParams& prm, CUtensorMap& mk, CUtensorMap& mv, const void* q,
+                        const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                        int max_blocks, const int32_t* context_lens, const int32_t* q_start,
+                        int num_seqs, int max_q_len, int num_q_heads, int num_kv_heads,
+                        int block_size, int num_blocks, float scale, void* out,
+                        unsigned int* err) {
+  if (num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+  std::memset(&prm, 0, sizeof(prm));
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.q_start = q_start;
+  prm.block_tables = block_tables;
+  prm.context_lens = context_lens;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.err = err;
+  prm.num_seqs = num_seqs;
+  prm.num_kv_heads = num_kv_heads;
+  prm.max_blocks = max_blocks;
+  prm.num_q_heads = num_q_heads;
+  prm.group = num_q_heads / num_kv_heads;
+  prm.max_q_len = max_q_len;
+  prm.block_size = block_size;
+  prm.log2_bs = ilog2(block_size);
+  prm.box_rows = block_size < kTcKeys ? block_size : kTcKeys;
+  prm.num_blocks = num_blocks;
+  prm.max_splits = 1;
+  prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  std::memset(&mk, 0, sizeof(mk));
+  std::memset(&mv, 0, sizeof(mv));
+  const long long rows = (long long)num_blocks * block_size;
+  if (!make_tc_map<128>(&mk, k_cache, num_kv_heads, rows, prm.box_rows) ||
+      !make_tc_map<128>(&mv, v_cache, num_kv_heads, rows, prm.box_rows))
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+}  // namespace
+
 pa_status launch_verify_tc(const void* q, const void* k_cache, const void* v_cache,
                            const int32_t* block_tables, int max_blocks,
                            const int32_t* context_lens, const int32_t* q_start, int num_seqs,
@@ -683,40 +910,47 @@ pa_status launch_verify_tc(const void* q, const void* k_cache, const void* v_cac
   const int G = num_q_heads / num_kv_heads;
   if (!verify_tc_supported(head_dim, block_size, G, max_q_len, split_tokens))
     return PA_ERR_UNSUPPORTED;
-  if (num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
   if ((long long)num_seqs * (split_tokens > 0 ? max_splits : 1) * num_kv_heads >= (1LL << 31))
     return PA_ERR_UNSUPPORTED;
   VfParams prm;
-  prm.q = static_cast<const __nv_bfloat16*>(q);
-  prm.q_start = q_start;
-  prm.block_tables = block_tables;
-  prm.context_lens = context_lens;
-  prm.out = static_cast<__nv_bfloat16*>(out);
+  CUtensorMap mk, mv;
+  const pa_status s =
+      verify_params(prm, mk, mv, q, k_cache, v_cache, block_tables, max_blocks, context_lens,
+                    q_start, num_seqs, max_q_len, num_q_heads, num_kv_heads, block_size,
+                    num_blocks, scale, out, err);
+  if (s != PA_OK) return s;
   prm.part_out = part_out;
   prm.part_lse = part_lse;
   prm.row_lens = row_lens;
-  prm.err = err;
-  prm.num_seqs = num_seqs;
-  prm.num_kv_heads = num_kv_heads;
-  prm.max_blocks = max_blocks;
-  prm.num_q_heads = num_q_heads;
-  prm.group = G;
-  prm.max_q_len = max_q_len;
-  prm.block_size = block_size;
-  prm.log2_bs = ilog2(block_size);
-  prm.box_rows = block_size < kTcKeys ? block_size : kTcKeys;
-  prm.num_blocks = num_blocks;
   prm.split_tokens = split_tokens;
   prm.max_splits = split_tokens > 0 ? max_splits : 1;
-  prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  return launch_verify_as<false>(mk, mv, prm, stream);
+}
+
+pa_status launch_verify_tc_balanced(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, int max_blocks,
+                                    const int32_t* context_lens, const int32_t* q_start,
+                                    int num_seqs, int max_q_len, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, float scale, int* counters, float* rec_lse,
+                                    float* rec_o, int rec_cols, void* out, unsigned int* err,
+                                    cudaStream_t stream) {
+  const int G = num_q_heads / num_kv_heads;
+  if (!verify_tc_balanced_supported(head_dim, block_size, G, max_q_len, num_seqs) ||
+      rec_cols < kVfCols)
+    return PA_ERR_UNSUPPORTED;
+  VfParams prm;
   CUtensorMap mk, mv;
-  std::memset(&mk, 0, sizeof(mk));
-  std::memset(&mv, 0, sizeof(mv));
-  const long long rows = (long long)num_blocks * block_size;
-  if (!make_tc_map<128>(&mk, k_cache, num_kv_heads, rows, prm.box_rows) ||
-      !make_tc_map<128>(&mv, v_cache, num_kv_heads, rows, prm.box_rows))
-    return PA_ERR_CUDA;
-  return launch_verify_as(mk, mv, prm, stream);
+  const pa_status s =
+      verify_params(prm, mk, mv, q, k_cache, v_cache, block_tables, max_blocks, context_lens,
+                    q_start, num_seqs, max_q_len, num_q_heads, num_kv_heads, block_size,
+                    num_blocks, scale, out, err);
+  if (s != PA_OK) return s;
+  prm.counters = counters;
+  prm.rec_lse = rec_lse;
+  prm.rec_o = rec_o;
+  prm.rec_cols = rec_cols;
+  return launch_verify_as<true>(mk, mv, prm, stream);
 }
 
 }  // namespace pa

@@ -58,18 +58,19 @@ def test_multi_matches_oracle(cuda_lib, multi_kernel, qlen, hq, hkv, d, bs):
     (1, 8, 1, 128, 16), (4, 8, 1, 128, 16), (8, 64, 8, 128, 16), (3, 8, 2, 128, 16),
     (16, 8, 2, 64, 16), (64, 4, 4, 128, 16), (5, 16, 2, 64, 8), (7, 8, 2, 128, 1),
     (2, 8, 8, 128, 32), (6, 32, 8, 128, 16)])
-def test_balanced_multi_matches_oracle(cuda_lib, qlen, hq, hkv, d, bs):
+def test_balanced_multi_matches_oracle(cuda_lib, multi_kernel, qlen, hq, hkv, d, bs):
     rng = np.random.default_rng(qlen * 100 + hq + bs)
     qlens = [int(x) for x in rng.integers(1, qlen + 1, len(CTX))]
     qlens[0] = qlen
     case = wl.make_multi_case("mqb", 40 + qlen + bs, CTX, qlens, hq, hkv, d, bs)
     out = run_multi(cuda_lib, case, split=cuda_lib.BALANCED_MULTI)
-    P.assert_close(P.to_f64(out), oracle_multi(case), f"balanced q_len<={qlen} G={hq // hkv}")
+    P.assert_close(P.to_f64(out), oracle_multi(case),
+                   f"{multi_kernel} balanced q_len<={qlen} G={hq // hkv}")
 
 
 @pytest.mark.parametrize("lens", [[5000, 3, 0, 700, 1], [1] * 40, [9000] * 3 + [17] * 50],
                          ids=["mixed", "tiny_units", "long_and_short"])
-def test_balanced_multi_cut_units_and_sequences_without_rows(cuda_lib, lens):
+def test_balanced_multi_cut_units_and_sequences_without_rows(cuda_lib, multi_kernel, lens):
     # long contexts are cut across many blocks (per-column records merged in
     # the kernel); a sequence with no query rows holds no tiles
     qlens = [(i % 4) for i in range(len(lens))]
@@ -89,7 +90,7 @@ def test_balanced_multi_cut_units_and_sequences_without_rows(cuda_lib, lens):
                                    case.max_q_len, case.scale, ws, out)
         outs.append(out)
     torch.cuda.synchronize()
-    P.assert_close(P.to_f64(outs[0]), oracle_multi(case), "balanced cut units")
+    P.assert_close(P.to_f64(outs[0]), oracle_multi(case), f"{multi_kernel} balanced cut units")
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
     counters = ws[: case.batch * 8 * 8 * 4].view(torch.int32)
     assert torch.all(counters == 0)

@@ -14,7 +14,9 @@ rows before position 0, table entries outside the pool, repeatability, a
 seeded sweep of random shapes, and the speculative-verification batch of the
 bench (70B heads, 4 new tokens, split 1024) with every row checked, and a
 persistent launch whose blocks each walk many units (several hundred
-sequences of mixed lengths and token counts).
+sequences of mixed lengths and token counts); and the balanced schedule
+(pa_decode_multi_balanced) on the same kernel: units cut across blocks and
+merged in the kernel, sequences without query rows, rows above max_q_len.
 Tolerance: the parity bar of the bf16 path (max abs <= 2e-2, per-row
 relative L2 <= 5e-3).
 """
@@ -197,3 +199,63 @@ def test_persistent_blocks_walk_many_units(cuda_lib, pool):
     out, pools = run(cuda_lib, case, pool, split=256, context_lens=short)
     P.assert_close(P.to_f64(out), want(case, pools, context_lens=short), f"{pool} many units")
     assert cuda_lib.pa_last_device_error() == 0
+
+
+def _balanced(b, case, context_lens=None, max_q_len=None, reps=2):
+    cl = case.context_lens if context_lens is None else context_lens
+    ws = torch.zeros(b.pa_decode_multi_balanced_workspace_bytes(case.batch, case.num_kv_heads, 128),
+                     dtype=torch.uint8, device="cuda")
+    k, v = case.k_cache.cuda(), case.v_cache.cuda()
+    b.pa_kv_append(case.k_new.cuda(), case.v_new.cuda(), case.slot_mapping.cuda(), k, v)
+    outs = []
+    for _ in range(reps):                           # the workspace is reusable
+        out = torch.zeros_like(case.q).cuda()
+        b.pa_decode_multi_balanced(case.q.cuda(), k, v, case.block_tables.cuda(), cl.cuda(),
+                                   case.q_start.cuda(), max_q_len or case.max_q_len, case.scale,
+                                   ws, out)
+        outs.append(out)
+    torch.cuda.synchronize()
+    counters = ws[: case.batch * case.num_kv_heads * 8 * 4].view(torch.int32)
+    assert torch.all(counters == 0)                 # the tickets are left zero
+    return outs
+
+
+@pytest.mark.parametrize("split_heads", [(64, 8), (16, 2), (8, 1)])
+def test_balanced_schedule_many_units(cuda_lib, split_heads):
+    # the balanced schedule on the tcgen05 kernel: every block an equal range
+    # of 128-key tiles, units cut across blocks merged in the kernel, long
+    # and short contexts, sequences without query rows, rows before position 0
+    hq, hkv = split_heads
+    g = hq // hkv
+    rng = np.random.default_rng(91 + hq)
+    B = 260
+    ctx0 = [int(x) for x in np.exp(rng.uniform(np.log(1), np.log(20000), B))]
+    qlens = [int(x) for x in rng.integers(0, min(4, 32 // g) + 1, B)]
+    qlens[0] = min(4, 32 // g)
+    case = wl.make_multi_case("vtcbal", 31 + hq, ctx0, qlens, hq, hkv, 128, 16)
+    short = case.context_lens.clone()
+    short[5::41] = 1                                # rows before position 0
+    short = torch.maximum(short, torch.ones_like(short))
+    a, b_ = _balanced(cuda_lib, case, context_lens=short)
+    kc, vc = pa.kv_append(wl.bits(case.k_cache), wl.bits(case.v_cache), wl.bits(case.k_new),
+                          wl.bits(case.v_new), case.slot_mapping.numpy())
+    want_ = oracle.decode_multi(wl.bits(case.q), kc, vc, case.block_tables.numpy(),
+                                short.numpy(), case.q_start.numpy(), case.scale)
+    P.assert_close(P.to_f64(a), want_, f"balanced tcgen05 G={g}")
+    assert torch.equal(a.view(torch.int16), b_.view(torch.int16))
+    assert cuda_lib.pa_last_device_error() == 0
+
+
+def test_balanced_schedule_rows_above_max_q_len(cuda_lib):
+    # a sequence with more rows than max_q_len holds no tiles, is left as it
+    # is and sets bit 16; the others are attended as usual
+    case = wl.make_multi_case("vtcbalbad", 13, [3000, 100, 50], [6, 3, 4], 64, 8, 128, 16)
+    out, = _balanced(cuda_lib, case, max_q_len=4, reps=1)
+    assert cuda_lib.pa_last_device_error() & 16
+    got = P.to_f64(out)
+    assert not got[:6].any()
+    kc, vc = pa.kv_append(wl.bits(case.k_cache), wl.bits(case.v_cache), wl.bits(case.k_new),
+                          wl.bits(case.v_new), case.slot_mapping.numpy())
+    want_ = oracle.decode_multi(wl.bits(case.q), kc, vc, case.block_tables.numpy(),
+                                case.context_lens.numpy(), case.q_start.numpy(), case.scale)
+    P.assert_close(got[6:], want_[6:], "balanced tcgen05, the other sequences")
