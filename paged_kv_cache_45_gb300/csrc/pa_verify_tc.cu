@@ -192,14 +192,52 @@ __device__ __forceinline__ int vf_seq_tiles(const VfParams& p, int b) {
   return tiles_of<kTcKeys>(p.context_lens[b], p.max_blocks << p.log2_bs);
 }
 
+// A place on the balanced schedule's line of 128-key tiles, KV head by KV
+// head: unit (b, h) holds the tiles h T + S[b] .. h T + S[b + 1] - 1, T =
+// S[B]. (Head-major: the blocks W / Hkv apart on the line walk the same
+// sequences' positions of neighbouring heads at the same time, so the heads
+// of one token row are read together.)
+struct VfCursor {
+  int b, kvh, t, n;
+
+  __device__ __forceinline__ void seek(long long g, const int* S, int B) {
+    const long long T = S[B];
+    kvh = (int)(g / T);
+    const int r = (int)(g - (long long)kvh * T);
+    int lo = 0, hi = B - 1;  // largest b with S[b] <= r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (S[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    n = S[b + 1] - S[b];
+    t = r - S[b];
+  }
+
+  // Move to the first tile of the next unit.
+  __device__ __forceinline__ void next_unit(const int* S, int B) {
+    t = 0;
+    do {
+      if (++b == B) {
+        b = 0;
+        ++kvh;
+      }
+    } while (S[b + 1] == S[b] && S[B] > 0);
+    n = S[b + 1] - S[b];
+  }
+
+  __device__ __forceinline__ long long unit_start(const int* S, int B) const {
+    return (long long)kvh * S[B] + S[b];
+  }
+};
+
 // The block's work items in order. Split mode: units blockIdx.x,
 // blockIdx.x + gridDim.x, ... Balanced mode: the segments of the block's
-// range [c N / W, (c + 1) N / W) of the N 128-key tiles of all (sequence,
-// KV head) units (unit (b, h) holds tiles Hkv S[b] + h n_b ..).
+// range [c N / W, (c + 1) N / W) of the N = Hkv S[B] tiles of the line.
 template <bool kBal>
 struct VfWalk {
   int u;
-  Cursor cur;
+  VfCursor cur;
   long long left, N, W;
 
   __device__ __forceinline__ void init(const VfParams& p, const int* S) {
@@ -211,7 +249,7 @@ struct VfWalk {
       if ((long long)blockIdx.x < W) {
         const long long g0 = (long long)blockIdx.x * N / W;
         left = (long long)(blockIdx.x + 1) * N / W - g0;
-        if (left > 0) cur.seek(g0, S, p.num_seqs, p.num_kv_heads);
+        if (left > 0) cur.seek(g0, S, p.num_seqs);
       }
     }
   }
@@ -234,12 +272,16 @@ struct VfWalk {
       w.t_end = min((cur.t + m) * kTcKeys, w.ctx);
       w.n_tiles = m;
       w.bad = false;
-      const long long u0 = (long long)p.num_kv_heads * S[w.b] + (long long)w.kvh * cur.n;
+      const long long u0 = cur.unit_start(S, p.num_seqs);
       w.c0 = owner_of(u0, N, W);
       w.c1 = owner_of(u0 + cur.n - 1, N, W);
       w.cut = w.c0 != w.c1;
       left -= m;
-      if (cur.t + m == cur.n) cur.next_unit(S, p.num_seqs, p.num_kv_heads); else cur.t += m;
+      if (cur.t + m == cur.n) {
+        if (left > 0) cur.next_unit(S, p.num_seqs);
+      } else {
+        cur.t += m;
+      }
       return true;
     } else {
       const int U = p.num_seqs * p.max_splits * p.num_kv_heads;
