@@ -73,9 +73,10 @@ def parse_args():
     ap.add_argument("--step", choices=["fused", "separate"], default="fused",
                     help="fused: pa_append_decode (append + balanced decode in one launch); "
                          "separate: pa_kv_append, then the decode of --schedule")
-    ap.add_argument("--multi-schedule", choices=["split", "balanced"], default="split",
+    ap.add_argument("--multi-schedule", choices=["auto", "split", "balanced"], default="auto",
                     help="spec workload: pa_decode_multi over context splits (--split, default "
-                         "1024) + reduce, or pa_decode_multi_balanced")
+                         "1024) + reduce, or pa_decode_multi_balanced (one launch); auto: "
+                         "balanced over bf16 caches, split over e4m3 pools")
     ap.add_argument("--split", type=int, default=-1,
                     help="split_tokens for --schedule split (-1: planned; 0: no split)")
     ap.add_argument("--seed", type=int, default=0)
@@ -446,6 +447,8 @@ def run_gpu(args):
     steps = Steps(args.workload, args.seed + rank, device, args.batch, args.kv_dtype)
     if steps.fp8 and not steps.multi and args.schedule != "balanced":
         raise SystemExit("--kv-dtype fp8 runs the balanced schedule only")
+    if args.multi_schedule == "auto":
+        args.multi_schedule = "split" if steps.fp8 or args.split >= 0 else "balanced"
     if steps.fp8 and steps.multi and args.multi_schedule == "balanced":
         raise SystemExit("--kv-dtype fp8 with several query tokens runs the split schedule "
                          "(--workload spec, --workload prefill) only")
