@@ -39,16 +39,28 @@ __device__ __forceinline__ int owner_of(long long g, long long N, long long W) {
 // positions and keep the start a closed form of S.) K = 0 gives equal tile
 // counts. Ownership stays contiguous in the unit list, so a cut unit is still
 // merged by the blocks c0..c1 that own its first and last tiles.
-struct Partition {
+//
+// kHM (head-major): the units go KV head by KV head instead, unit (b, h) at
+//   start(b, h) = h (S[B] + K B) + S[b] + K b,
+// tile t of it being global tile h S[B] + S[b] + t of the unit list. The
+// blocks Nw / Hkv positions apart then stream the same sequences' rows at
+// the same time, one KV head each, so the heads of a token row (one
+// Hkv * head_dim row of the pool) are read together.
+template <bool kHM = false>
+struct PartitionT {
   long long N;   // tiles (Hkv * S[B])
   long long Nw;  // weighted positions
   long long W;   // blocks that own a range
   int K;         // charge per unit, in tiles
+  long long T;   // tiles of one KV head (S[B])
+  long long Tw;  // weighted positions of one KV head
 
   __device__ __forceinline__ void init(const int* S, int B, int hkv, int unit_cost, int grid) {
     K = unit_cost;
-    N = (long long)hkv * S[B];
-    Nw = (long long)hkv * ((long long)S[B] + (long long)K * B);
+    T = S[B];
+    Tw = (long long)S[B] + (long long)K * B;
+    N = (long long)hkv * T;
+    Nw = (long long)hkv * Tw;
     W = N == 0 ? 0 : min((long long)grid, Nw);
   }
   __device__ __forceinline__ long long start(const int* S, int hkv, int b) const {
@@ -57,6 +69,7 @@ struct Partition {
   // weighted position of tile t of unit (b, h), n = the unit's tiles
   __device__ __forceinline__ long long pos(const int* S, int hkv, int b, int h, int n,
                                            int t) const {
+    if constexpr (kHM) return (long long)h * Tw + S[b] + (long long)K * b + t;
     return start(S, hkv, b) + (long long)h * (n + K) + t;
   }
   __device__ __forceinline__ int owner(long long x) const { return owner_of(x, Nw, W); }
@@ -64,6 +77,18 @@ struct Partition {
   __device__ __forceinline__ long long tiles_before(long long x, const int* S, int B,
                                                     int hkv) const {
     if (x >= Nw) return N;
+    if constexpr (kHM) {
+      const long long h = x / Tw;
+      const long long r = x - h * Tw;
+      int lo = 0, hi = B - 1;  // largest b with S[b] + K b <= r
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)S[mid] + (long long)K * mid <= r) lo = mid; else hi = mid - 1;
+      }
+      const long long n = S[lo + 1] - S[lo];
+      const long long t = r - ((long long)S[lo] + (long long)K * lo);
+      return h * T + S[lo] + (t < n ? t : n);
+    }
     int lo = 0, hi = B - 1;  // largest b with start(b) <= x
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -83,13 +108,30 @@ struct Partition {
     g1 = tiles_before((long long)(c + 1) * Nw / W, S, B, hkv);
   }
 };
+using Partition = PartitionT<false>;
 
-// Position (sequence, KV head, tile) in the unit list.
-struct Cursor {
+// Position (sequence, KV head, tile) in the unit list (kHM: head-major, as
+// PartitionT<true> orders it).
+template <bool kHM = false>
+struct CursorT {
   int b, kvh, t, n;
 
   // Place the cursor on global tile g (g < N).
   __device__ __forceinline__ void seek(long long g, const int* S, int B, int hkv) {
+    if constexpr (kHM) {
+      const long long T = S[B];
+      kvh = (int)(g / T);
+      const int r = (int)(g - (long long)kvh * T);
+      int lo = 0, hi = B - 1;  // largest b with S[b] <= r: a sequence with tiles
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (S[mid] <= r) lo = mid; else hi = mid - 1;
+      }
+      b = lo;
+      n = S[b + 1] - S[b];
+      t = r - S[b];
+      return;
+    }
     int lo = 0, hi = B - 1;  // largest b with hkv * S[b] <= g
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -102,9 +144,22 @@ struct Cursor {
     t = (int)(r - (long long)kvh * n);
   }
 
-  // Move to the first tile of the next unit.
+  // Move to the first tile of the next unit (past the last unit: n = 0).
   __device__ __forceinline__ void next_unit(const int* S, int B, int hkv) {
     t = 0;
+    if constexpr (kHM) {
+      do {
+        if (++b == B) {
+          b = 0;
+          if (++kvh == hkv) {
+            n = 0;
+            return;
+          }
+        }
+      } while (S[b + 1] == S[b]);
+      n = S[b + 1] - S[b];
+      return;
+    }
     if (++kvh == hkv) {
       kvh = 0;
       do { ++b; } while (b < B && S[b + 1] == S[b]);
@@ -112,6 +167,7 @@ struct Cursor {
     }
   }
 };
+using Cursor = CursorT<false>;
 
 // S[b] = tiles of the sequences before b (exclusive prefix sum), S[B] = all
 // of them, where sequence i holds tiles(i) tiles; kThreads threads of the

@@ -71,6 +71,9 @@ constexpr int kConsumersFp8 = 2;
 constexpr int kStagesFp8 = 4;
 constexpr int kBlocksPerSM = 4;
 constexpr int kMaxBlocksPerSM = kBlocksPerSM;
+// The unit list goes KV head by KV head (PartitionT<true>): the blocks
+// running together then read the heads of the same token rows together.
+constexpr bool kHeadMajorLine = true;
 
 struct BalParams {
   const __nv_bfloat16* q;
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
   }
 
   // ---- this block's tile range -----------------------------------------------
-  Partition part;
+  PartitionT<kHeadMajorLine> part;
   part.init(S, B, hkv, p.unit_cost, gridDim.x);
   const int c = blockIdx.x;
   if (c >= part.W) return;
@@ -254,7 +257,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
       prefetch_tensormap(&tmap_k);
       prefetch_tensormap(&tmap_v);
     }
-    Cursor ic;
+    CursorT<kHeadMajorLine> ic;
     ic.seek(g0, S, B, hkv);
     int ic_ctx = 0, ic_nblk = 0;
     int tc_b = -1, tc_base = 0, tc_val = -1;
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, BPS)
   const int tid = threadIdx.x;  // 0 .. NC*32-1
   const int r0 = lane >> 2;
   const int tk = 2 * (lane & 3);
-  Cursor uc;
+  CursorT<kHeadMajorLine> uc;
   uc.seek(g0, S, B, hkv);
   uint32_t qf[D / 16][2];
   AttnState<D> st;
