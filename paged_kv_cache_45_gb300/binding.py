@@ -729,7 +729,7 @@ def pa_copy_blocks(k_cache, v_cache, src, dst, stream=None) -> None:
     if n == 0:
         return
     nb = k_cache.shape[0]
-    block_bytes = k_cache[0].numel() * k_cache.element_size()
+    block_bytes = k_cache.numel() // max(nb, 1) * k_cache.element_size()
     _check("pa_copy_blocks", _lib.pa_copy_blocks(
         _t(k_cache, k_cache.dtype, "k_cache"), _t(v_cache, v_cache.dtype, "v_cache"),
         _t(src, torch.int32, "src"), _t(dst, torch.int32, "dst"), n, nb, block_bytes,

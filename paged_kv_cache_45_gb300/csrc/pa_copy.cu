@@ -6,10 +6,13 @@
 // one. The prefix cache (pa_prefix.cpp) decides the (src, dst) pairs; this is
 // the device side: a byte copy of block src to block dst in both caches.
 //
-// HBM-bound streaming copy: each thread issues four 16-byte loads (strided by
-// the block size so a warp's accesses stay coalesced) before its four stores,
-// so a 256-thread block keeps 16 KB in flight. Ids outside the pool are
-// skipped.
+// HBM-bound streaming copy. Thread block (x, y, z) copies 16 KB of copy z's
+// block: of the K cache (y = 0) or the V cache (y = 1), chunks
+// 1024 x .. 1024 x + 1023 of 16 bytes; each thread issues its four 16-byte
+// loads (256 apart, so a warp's accesses stay coalesced) before its four
+// stores. The pair (src, dst) is the same for the whole thread block; ids
+// outside the pool are skipped. (Copies past the grid's z extent, 65535, are
+// taken in turn by the same blocks.)
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -28,29 +31,26 @@ constexpr int kCopyUnroll = 4;
 __global__ void __launch_bounds__(kCopyThreads)
     copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                        const int32_t* __restrict__ src, const int32_t* __restrict__ dst,
-                       long long chunks_per_block, long long total, int num_blocks) {
-  const long long base = (long long)blockIdx.x * kCopyThreads * kCopyUnroll + threadIdx.x;
-  uint4 v[kCopyUnroll];
-  uint4* to[kCopyUnroll];
-#pragma unroll
-  for (int u = 0; u < kCopyUnroll; ++u) {
-    to[u] = nullptr;
-    const long long g = base + (long long)u * kCopyThreads;
-    if (g >= total) continue;
-    const long long per_copy = 2 * chunks_per_block;
-    const long long c = g / per_copy;
-    const long long r = g - c * per_copy;
-    const int which = r >= chunks_per_block;  // 0: K, 1: V
-    const long long off = r - which * chunks_per_block;
+                       long long chunks_per_block, int num_copies, int num_blocks) {
+  uint4* pool = blockIdx.y ? v_cache : k_cache;
+  const long long off0 = (long long)blockIdx.x * kCopyThreads * kCopyUnroll + threadIdx.x;
+  for (int c = blockIdx.z; c < num_copies; c += gridDim.z) {
     const int s = __ldg(src + c), d = __ldg(dst + c);
     if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) continue;
-    uint4* pool = which ? v_cache : k_cache;
-    v[u] = pool[(long long)s * chunks_per_block + off];
-    to[u] = pool + (long long)d * chunks_per_block + off;
-  }
+    const uint4* from = pool + (long long)s * chunks_per_block;
+    uint4* to = pool + (long long)d * chunks_per_block;
+    uint4 v[kCopyUnroll];
 #pragma unroll
-  for (int u = 0; u < kCopyUnroll; ++u)
-    if (to[u]) *to[u] = v[u];
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const long long off = off0 + (long long)u * kCopyThreads;
+      if (off < chunks_per_block) v[u] = from[off];
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const long long off = off0 + (long long)u * kCopyThreads;
+      if (off < chunks_per_block) to[off] = v[u];
+    }
+  }
 }
 
 pa_status check_copies(const int32_t* src, const int32_t* dst, int n, int num_blocks,
@@ -92,12 +92,12 @@ extern "C" pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t*
     if (s != PA_OK) return s;
   }
   const long long cpb = block_bytes / 16;
-  const long long total = 2 * cpb * (long long)num_copies;
   const long long per_cta = (long long)kCopyThreads * kCopyUnroll;
-  const long long grid = (total + per_cta - 1) / per_cta;
-  if (grid > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-  copy_blocks_kernel<<<(unsigned)grid, kCopyThreads, 0, st>>>(
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), src, dst, cpb, total,
+  const long long gx = (cpb + per_cta - 1) / per_cta;
+  if (gx > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  const dim3 grid((unsigned)gx, 2, (unsigned)(num_copies < 65535 ? num_copies : 65535));
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, st>>>(
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), src, dst, cpb, num_copies,
       num_blocks);
   return launch_status();
 }
