@@ -30,12 +30,20 @@
 // partial row sums for its key and the column sums are reduced once, at the
 // end.
 //
-// A persistent launch, one block per SM: the (sequence, context split, KV
-// head) units go round robin over the blocks, and every warp role walks the
-// block's units in the same order with counters that run on across units,
-// so the loads of the next unit overlap the work of the current one. Warps:
-//   0     loader: K_j and V_j (128 keys each) of every unit in turn through a
-//         6-slot ring of 32 KB operand slots, one 4-D TMA box per paged
+// A persistent launch, one block per SM, in two schedules. Split mode
+// (pa_decode_multi): the (sequence, context split, KV head) units go round
+// robin over the blocks. Balanced mode (pa_decode_multi_balanced): every
+// block an equal range of the 128-key tiles of all (sequence, KV head) units,
+// on a line ordered KV head by KV head (so the blocks running together read
+// a token row's heads together); a unit cut by ranges leaves per-block
+// records in the caller's workspace, and the epilogue warp with the last
+// ticket on it merges them (log-sum-exp), so one launch needs no reduce.
+// Every warp role walks the block's items in the same order with counters
+// that run on across items, so the loads of the next item overlap the work
+// of the current one. Warps:
+//   0     loader: K_j and V_j (128 keys each) of every item in turn through a
+//         ring of 32 KB operand slots (6; 5 in balanced mode, whose prefix sum
+//         over the sequences takes the room of the sixth), one 4-D TMA box per paged
 //         block, lane i issuing box i (the slot layout of the chunked-prefill
 //         kernel);
 //   1     allocates 128 TMEM columns (two S^T and two O^T buffers of 32); one
@@ -45,9 +53,9 @@
 //         finished means PV(jg - 2) finished (P buffer jg % 2 is free);
 //   2-5   the softmax warpgroup (TMEM lane quarter = warp % 4), one key of
 //         the tile per thread; hands each unit's column sums and maxima on;
-//   6-9   epilogue: stages Q of the units two ahead (two Q buffers), writes
-//         each unit's outputs from its O^T buffer (two, alternating by
-//         unit), zero rows and per-row context lengths.
+//   6-9   epilogue: stages Q of the items two ahead (two Q buffers), writes
+//         each item's outputs from its O^T buffer (two, alternating by
+//         item) or its record, zero rows and per-row context lengths.
 // Arithmetic: bf16 MMA operands with fp32 accumulation, weights rounded to
 // bf16 and their rounded values summed, as in the column-warp kernel; a column's
 // running max moves only when a tile's max exceeds it by more than 2^8 (the
