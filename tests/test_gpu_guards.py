@@ -176,23 +176,27 @@ def test_multi_token_entry_points_stay_inside_their_buffers(cuda_lib, shape):
     b.pa_decode_multi(q, kc.t, vc.t, tables, lens, qs, mc.max_q_len, mc.scale, out.t)
     guards = [(kc, "k_cache"), (vc, "v_cache"), (out, "multi out")]
     outs = [(out, "multi")]
-    if mc.max_q_len * (hq // hkv) <= 64:  # the column kernel: split and balanced forms
-        split = 64
-        S = b.pa_decode_num_splits(int(mc.block_tables.shape[1]) * bs, split)
-        po = Guarded((R, hq, S, d), torch.float32, float("nan"))
-        pl = Guarded((R, hq, S), torch.float32, float("nan"))
-        rl = Guarded((R,), torch.int32, -7)
-        out_s = Guarded((R, hq, d), torch.bfloat16, float("nan"))
-        b.pa_decode_multi(q, kc.t, vc.t, tables, lens, qs, mc.max_q_len, mc.scale, out_s.t,
-                          split, S, po.t, pl.t, rl.t)
-        b.pa_decode_splitk_reduce(po.t, pl.t, rl.t, split, out_s.t)
+    if mc.max_q_len * (hq // hkv) <= 64:  # short chunks: split and balanced forms
+        # split 64 runs the column-warp kernel; split 128 the tcgen05 one where
+        # it applies (head_dim 128, block size >= 8, <= 32 columns a KV head)
+        for split in (64, 128):
+            S = b.pa_decode_num_splits(int(mc.block_tables.shape[1]) * bs, split)
+            po = Guarded((R, hq, S, d), torch.float32, float("nan"))
+            pl = Guarded((R, hq, S), torch.float32, float("nan"))
+            rl = Guarded((R,), torch.int32, -7)
+            out_s = Guarded((R, hq, d), torch.bfloat16, float("nan"))
+            b.pa_decode_multi(q, kc.t, vc.t, tables, lens, qs, mc.max_q_len, mc.scale, out_s.t,
+                              split, S, po.t, pl.t, rl.t)
+            b.pa_decode_splitk_reduce(po.t, pl.t, rl.t, split, out_s.t)
+            guards += [(po, f"part_out, split {split}"), (pl, f"part_lse, split {split}"),
+                       (rl, f"row_lens, split {split}"), (out_s, f"reduce out, split {split}")]
+            outs += [(out_s, f"multi split {split} + reduce")]
         ws = _ws(b.pa_decode_multi_balanced_workspace_bytes(B, hkv, d))
         out_b = Guarded((R, hq, d), torch.bfloat16, float("nan"))
         b.pa_decode_multi_balanced(q, kc.t, vc.t, tables, lens, qs, mc.max_q_len, mc.scale,
                                    ws.t, out_b.t)
-        guards += [(po, "part_out"), (pl, "part_lse"), (rl, "row_lens"), (out_s, "reduce out"),
-                   (ws, "multi workspace"), (out_b, "multi balanced out")]
-        outs += [(out_s, "multi split + reduce"), (out_b, "multi balanced")]
+        guards += [(ws, "multi workspace"), (out_b, "multi balanced out")]
+        outs += [(out_b, "multi balanced")]
     torch.cuda.synchronize()
     for g, what in guards:
         g.check(what)
